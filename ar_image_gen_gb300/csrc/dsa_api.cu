@@ -1,0 +1,518 @@
+// dsa_api.cu -- host side of the C ABI declared in include/dsa.h.
+//
+// Validation, device state (prompt prefix, decode ring, relative-offset skip
+// mask, split partials), the per-step plan (phase, attended counts, split
+// choice) and the kernel launches.  No CPU fallback: every step of the decode
+// path runs in the kernels of dsa_decode.cuh.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/dsa.h"
+#include "dsa_decode.cuh"
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<int> g_fail_after{0};
+
+int fail(int code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device allocation with the test hook of dsa_debug_fail_alloc_after().
+int dev_alloc(void **p, size_t bytes, const char *what)
+{
+    *p = nullptr;
+    int n = g_fail_after.load();
+    if (n > 0) {
+        if (n == 1) {
+            g_fail_after.store(0);
+            return fail(DSA_ERR_OOM, "allocation of %s (%zu bytes) failed (injected)", what, bytes);
+        }
+        g_fail_after.store(n - 1);
+    }
+    cudaError_t e = cudaMalloc(p, bytes ? bytes : 16);
+    if (e != cudaSuccess) {
+        *p = nullptr;
+        cudaGetLastError();
+        if (e == cudaErrorMemoryAllocation)
+            return fail(DSA_ERR_OOM, "allocation of %s (%zu bytes) failed", what, bytes);
+        return cuda_fail(e, what);
+    }
+    return DSA_OK;
+}
+
+constexpr uint32_t kMagic = 0x44534131u;  // "DSA1"
+constexpr uint32_t kDefaultWaitLimit = 0xffffffffu;
+
+int elem_bytes(int dtype) { return dtype == DSA_F32 ? 4 : 2; }
+
+// Stage rows and rows-per-CTA limit of the kernel instantiation.
+int stage_rows(int dtype, int D) { return 16384 / (2 * D * elem_bytes(dtype)); }
+constexpr int kChunkMax = 2048;
+
+}  // namespace
+
+struct dsa_ctx {
+    uint32_t magic;
+    int S, D, L_p, N_r, N_att, sink, dtype;
+    int R, A, Lcap, MW;
+    int t;
+    int prefilled;
+    int last_select;
+    int device, sm_count, ctas_per_sm;
+    int forced_split;
+    int pstride;
+    uint32_t wait_limit;
+    void *prefix, *ring;
+    uint32_t *mask;
+    int32_t *last_sel;
+    float *part_acc;
+    float2 *part_ml, *part_min;
+    int *ticket;
+    int *status;
+};
+
+namespace {
+
+bool valid(dsa_handle h) { return h != nullptr && h->magic == kMagic; }
+
+int validate(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int dtype)
+{
+    if (heads < 1) return fail(DSA_ERR_ARG, "heads must be >= 1 (got %d)", heads);
+    if (head_dim != 64 && head_dim != 128) return fail(DSA_ERR_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
+    if (L_p < 0) return fail(DSA_ERR_ARG, "L_p must be >= 0 (got %d)", L_p);
+    if (sink < 0) return fail(DSA_ERR_ARG, "sink must be >= 0 (got %d)", sink);
+    if (N_att < 1 || N_att > N_r) return fail(DSA_ERR_ARG, "need 1 <= N_att <= N_r (got N_att=%d, N_r=%d)", N_att, N_r);
+    if (sink > 0 && N_att <= sink) return fail(DSA_ERR_ARG, "need N_att > sink (got N_att=%d, sink=%d)", N_att, sink);
+    if (N_r - sink > 65536) return fail(DSA_ERR_ARG, "N_r - sink must be <= 65536 (got %d)", N_r - sink);
+    if (dtype != DSA_BF16 && dtype != DSA_F32) return fail(DSA_ERR_ARG, "dtype must be DSA_BF16 or DSA_F32 (got %d)", dtype);
+    if ((long long)L_p + sink > INT_MAX / 4) return fail(DSA_ERR_ARG, "L_p too large");
+    return DSA_OK;
+}
+
+struct Plan {
+    int phase, tin, P, a, wlen, select, sinkmode, n, nsplit, chunk;
+    unsigned long long bytes;
+};
+
+int auto_splits(const dsa_ctx *h, int n)
+{
+    const int rows = stage_rows(h->dtype, h->D);
+    const int need = (n + kChunkMax - 1) / kChunkMax;
+    const long long slots = (long long)h->sm_count * h->ctas_per_sm;
+    const int want = (int)((4 * slots + h->S - 1) / h->S);
+    const int by_rows = n / (2 * rows) > 1 ? n / (2 * rows) : 1;
+    const int ns = want < by_rows ? want : by_rows;
+    return ns > need ? ns : need;
+}
+
+Plan make_plan(const dsa_ctx *h, int t)
+{
+    Plan p{};
+    if (t < h->sink) {
+        p.phase = 0;
+        p.tin = -1;
+        p.P = h->L_p + t;
+        p.a = 1;
+        p.wlen = 1;
+        p.select = 0;
+        p.sinkmode = 1;
+    } else {
+        const int tin = t - h->sink;
+        p.tin = tin;
+        p.P = h->L_p + h->sink;
+        p.phase = tin < h->A - 1 ? 1 : (tin < h->R ? 2 : 3);
+        p.a = tin + 1 < h->A ? tin + 1 : h->A;
+        p.wlen = tin + 1 < h->R ? tin + 1 : h->R;
+        p.select = (tin >= h->A - 1 && tin <= h->R - 2) ? 1 : 0;
+        p.sinkmode = 0;
+    }
+    p.n = p.P + p.a;
+    const int rows = stage_rows(h->dtype, h->D);
+    int ns = h->forced_split > 0 ? h->forced_split : auto_splits(h, p.n);
+    const int need = (p.n + kChunkMax - 1) / kChunkMax;
+    if (ns < need) ns = need;
+    if (ns > p.n) ns = p.n;
+    int chunk = (p.n + ns - 1) / ns;
+    chunk = (chunk + rows - 1) / rows * rows;
+    if (chunk > kChunkMax) chunk = kChunkMax;
+    p.chunk = chunk;
+    p.nsplit = (p.n + chunk - 1) / chunk;
+    const unsigned long long De = (unsigned long long)h->D * elem_bytes(h->dtype);
+    // K and V rows read (current token through k_new/v_new) + q + k_new, v_new
+    // read + new entry written + out written.
+    p.bytes = (unsigned long long)h->S * (2 * De * (unsigned long long)(p.n - 1) + 6 * De);
+    return p;
+}
+
+int ensure_partials(dsa_ctx *h, int nsplit)
+{
+    if (nsplit <= h->pstride) return DSA_OK;
+    float *acc = nullptr;
+    float2 *ml = nullptr, *mn = nullptr;
+    int rc = dev_alloc((void **)&acc, sizeof(float) * (size_t)h->S * nsplit * h->D, "split partials");
+    if (rc == DSA_OK) rc = dev_alloc((void **)&ml, sizeof(float2) * (size_t)h->S * nsplit, "split partials");
+    if (rc == DSA_OK) rc = dev_alloc((void **)&mn, sizeof(float2) * (size_t)h->S * nsplit, "split partials");
+    if (rc != DSA_OK) {
+        cudaFree(acc);
+        cudaFree(ml);
+        cudaFree(mn);
+        return rc;
+    }
+    cudaFree(h->part_acc);
+    cudaFree(h->part_ml);
+    cudaFree(h->part_min);
+    h->part_acc = acc;
+    h->part_ml = ml;
+    h->part_min = mn;
+    h->pstride = nsplit;
+    return DSA_OK;
+}
+
+void free_ctx(dsa_ctx *h)
+{
+    if (!h) return;
+    cudaFree(h->prefix);
+    cudaFree(h->ring);
+    cudaFree(h->mask);
+    cudaFree(h->last_sel);
+    cudaFree(h->part_acc);
+    cudaFree(h->part_ml);
+    cudaFree(h->part_min);
+    cudaFree(h->ticket);
+    cudaFree(h->status);
+    h->magic = 0;
+    delete h;
+}
+
+template <typename T, int D>
+int occupancy()
+{
+    using C = dsa::KCfg<T, D>;
+    static int cached = -1;
+    if (cached < 0) {
+        cudaError_t e = cudaFuncSetAttribute(dsa::decode_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return -1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dsa::decode_kernel<T, D>, C::THREADS, C::SMEM);
+        if (e != cudaSuccess) return -1;
+        cached = n;
+    }
+    return cached;
+}
+
+int occupancy_for(int dtype, int D)
+{
+    if (dtype == DSA_BF16) return D == 64 ? occupancy<__nv_bfloat16, 64>() : occupancy<__nv_bfloat16, 128>();
+    return D == 64 ? occupancy<float, 64>() : occupancy<float, 128>();
+}
+
+template <typename T, int D>
+cudaError_t launch_decode(const dsa::DecodeParams &p, int grid, cudaStream_t st)
+{
+    using C = dsa::KCfg<T, D>;
+    dsa::decode_kernel<T, D><<<grid, C::THREADS, C::SMEM, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_prefill(const void *K, const void *V, void *prefix, int S, int L_p, int Lcap, cudaStream_t st)
+{
+    const size_t total = (size_t)S * L_p * 2 * (D * sizeof(T) / 16);
+    if (total == 0) return cudaSuccess;
+    size_t blocks = (total + 255) / 256;
+    if (blocks > 65535 * 8) blocks = 65535 * 8;
+    dsa::prefill_kernel<T, D><<<(unsigned)blocks, 256, 0, st>>>((const T *)K, (const T *)V, (T *)prefix, S, L_p, Lcap);
+    return cudaGetLastError();
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char *dsa_last_error(void) { return g_err.c_str(); }
+
+int dsa_debug_fail_alloc_after(int n)
+{
+    g_fail_after.store(n > 0 ? n : 0);
+    return DSA_OK;
+}
+
+size_t dsa_state_bytes(int heads, int head_dim, int L_p, int N_r, int sink, int dtype)
+{
+    if (heads < 1 || (head_dim != 64 && head_dim != 128) || L_p < 0 || sink < 0 || N_r <= sink ||
+        (dtype != DSA_BF16 && dtype != DSA_F32))
+        return 0;
+    const size_t row = 2 * (size_t)head_dim * elem_bytes(dtype);
+    const size_t R = (size_t)(N_r - sink);
+    const size_t MW = (R + 31) / 32;
+    return (size_t)heads * (((size_t)L_p + sink) * row + R * row + MW * 4);
+}
+
+int dsa_create_ex(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int dtype, dsa_handle *out)
+{
+    if (!out) return fail(DSA_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    int rc = validate(heads, head_dim, L_p, N_r, N_att, sink, dtype);
+    if (rc != DSA_OK) return rc;
+
+    dsa_ctx *h = new (std::nothrow) dsa_ctx();
+    if (!h) return fail(DSA_ERR_OOM, "host allocation failed");
+    h->magic = kMagic;
+    h->S = heads;
+    h->D = head_dim;
+    h->L_p = L_p;
+    h->N_r = N_r;
+    h->N_att = N_att;
+    h->sink = sink;
+    h->dtype = dtype;
+    h->R = N_r - sink;
+    h->A = N_att - sink;
+    h->Lcap = L_p + sink;
+    h->MW = (h->R + 31) / 32;
+    h->wait_limit = kDefaultWaitLimit;
+
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) {
+        free_ctx(h);
+        cudaGetLastError();
+        return cuda_fail(e, "cudaGetDevice");
+    }
+    e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device);
+    if (e != cudaSuccess) {
+        free_ctx(h);
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    }
+    h->ctas_per_sm = occupancy_for(dtype, head_dim);
+    if (h->ctas_per_sm < 1) {
+        free_ctx(h);
+        e = cudaGetLastError();
+        return cuda_fail(e, "kernel occupancy query (is this an sm_103 device?)");
+    }
+
+    const size_t row = 2 * (size_t)head_dim * elem_bytes(dtype);
+    const size_t S = (size_t)heads;
+    rc = dev_alloc(&h->prefix, S * h->Lcap * row, "prompt prefix");
+    if (rc == DSA_OK) rc = dev_alloc(&h->ring, S * h->R * row, "decode ring");
+    if (rc == DSA_OK) rc = dev_alloc((void **)&h->mask, S * h->MW * 4, "skip mask");
+    if (rc == DSA_OK) rc = dev_alloc((void **)&h->last_sel, S * 4, "last selection");
+    if (rc == DSA_OK) rc = dev_alloc((void **)&h->ticket, S * 4, "split tickets");
+    if (rc == DSA_OK) rc = dev_alloc((void **)&h->status, 16, "status word");
+    if (rc == DSA_OK) rc = ensure_partials(h, auto_splits(h, L_p + N_att));
+    if (rc != DSA_OK) {
+        std::string msg = g_err;
+        free_ctx(h);
+        g_err = msg;
+        return rc;
+    }
+    if ((e = cudaMemset(h->mask, 0, S * h->MW * 4)) != cudaSuccess ||
+        (e = cudaMemset(h->ticket, 0, S * 4)) != cudaSuccess || (e = cudaMemset(h->status, 0, 16)) != cudaSuccess ||
+        (e = cudaMemset(h->last_sel, 0xff, S * 4)) != cudaSuccess) {
+        free_ctx(h);
+        return cuda_fail(e, "cudaMemset");
+    }
+    *out = h;
+    return DSA_OK;
+}
+
+int dsa_create(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, dsa_handle *out)
+{
+    return dsa_create_ex(heads, head_dim, L_p, N_r, N_att, sink, DSA_BF16, out);
+}
+
+int dsa_destroy(dsa_handle h)
+{
+    if (!h) return DSA_OK;
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    cudaDeviceSynchronize();
+    free_ctx(h);
+    return DSA_OK;
+}
+
+int dsa_prefill(dsa_handle h, const void *K, const void *V, void *stream)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (h->L_p > 0 && (!K || !V)) return fail(DSA_ERR_ARG, "K and V must be non-NULL when L_p > 0");
+    if (h->L_p > 0 && (!aligned16(K) || !aligned16(V))) return fail(DSA_ERR_ARG, "K and V must be 16-byte aligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t S = (size_t)h->S;
+    cudaError_t e;
+    if ((e = cudaMemsetAsync(h->mask, 0, S * h->MW * 4, st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(h->ticket, 0, S * 4, st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(h->status, 0, 16, st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(h->last_sel, 0xff, S * 4, st)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync");
+    if (h->dtype == DSA_BF16)
+        e = h->D == 64 ? launch_prefill<__nv_bfloat16, 64>(K, V, h->prefix, h->S, h->L_p, h->Lcap, st)
+                       : launch_prefill<__nv_bfloat16, 128>(K, V, h->prefix, h->S, h->L_p, h->Lcap, st);
+    else
+        e = h->D == 64 ? launch_prefill<float, 64>(K, V, h->prefix, h->S, h->L_p, h->Lcap, st)
+                       : launch_prefill<float, 128>(K, V, h->prefix, h->S, h->L_p, h->Lcap, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    h->t = 0;
+    h->prefilled = 1;
+    h->last_select = 0;
+    return DSA_OK;
+}
+
+int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (!out || t < 0) return fail(DSA_ERR_ARG, "out must be non-NULL and t >= 0");
+    const Plan p = make_plan(h, t);
+    out->phase = p.phase;
+    out->t_inner = p.tin;
+    out->n_prefix = p.P;
+    out->n_decode = p.a;
+    out->select = p.select;
+    out->nsplit = p.nsplit;
+    out->chunk = p.chunk;
+    out->grid = p.nsplit * h->S;
+    out->algo_bytes = p.bytes;
+    return DSA_OK;
+}
+
+int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *v_new, void *out, void *stream)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (!h->prefilled) return fail(DSA_ERR_STATE, "dsa_decode_step before dsa_prefill");
+    if (!q || !k_new || !v_new || !out) return fail(DSA_ERR_ARG, "q, k_new, v_new and out must be non-NULL");
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out))
+        return fail(DSA_ERR_ARG, "q, k_new, v_new and out must be 16-byte aligned");
+    if (h->t == INT_MAX) return fail(DSA_ERR_STATE, "decode step counter exhausted");
+    const Plan pl = make_plan(h, h->t);
+    if ((long long)pl.nsplit * h->S > INT_MAX) return fail(DSA_ERR_ARG, "grid too large");
+    int rc = ensure_partials(h, pl.nsplit);
+    if (rc != DSA_OK) return rc;
+
+    dsa::DecodeParams p;
+    p.q = q;
+    p.knew = k_new;
+    p.vnew = v_new;
+    p.out = out;
+    p.prefix = h->prefix;
+    p.ring = h->ring;
+    p.mask = h->mask;
+    p.last_sel = h->last_sel;
+    p.part_acc = h->part_acc;
+    p.part_ml = h->part_ml;
+    p.part_min = h->part_min;
+    p.ticket = h->ticket;
+    p.status = h->status;
+    p.S = h->S;
+    p.Lcap = h->Lcap;
+    p.P = pl.P;
+    p.sinkmode = pl.sinkmode;
+    p.R = h->R;
+    p.tin = pl.tin;
+    p.wlen = pl.wlen;
+    p.a = pl.a;
+    p.n = pl.n;
+    p.nsplit = pl.nsplit;
+    p.chunk = pl.chunk;
+    p.pstride = h->pstride;
+    p.select = pl.select;
+    p.MW = h->MW;
+    p.qscale = (float)(1.4426950408889634 / std::sqrt((double)h->D));
+    p.wait_limit = h->wait_limit;
+
+    cudaStream_t st = (cudaStream_t)stream;
+    const int grid = pl.nsplit * h->S;
+    cudaError_t e;
+    if (h->dtype == DSA_BF16)
+        e = h->D == 64 ? launch_decode<__nv_bfloat16, 64>(p, grid, st) : launch_decode<__nv_bfloat16, 128>(p, grid, st);
+    else
+        e = h->D == 64 ? launch_decode<float, 64>(p, grid, st) : launch_decode<float, 128>(p, grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    h->last_select = pl.select;
+    h->t += 1;
+    return DSA_OK;
+}
+
+int dsa_get_step(dsa_handle h, int *t)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (!t) return fail(DSA_ERR_ARG, "t is NULL");
+    *t = h->t;
+    return DSA_OK;
+}
+
+int dsa_get_skip_mask(dsa_handle h, uint32_t *host_dst, void *stream)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (!host_dst) return fail(DSA_ERR_ARG, "host_dst is NULL");
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(host_dst, h->mask, (size_t)h->S * h->MW * 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "skip mask copy");
+}
+
+int dsa_get_last_selection(dsa_handle h, int32_t *host_dst, void *stream)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (!host_dst) return fail(DSA_ERR_ARG, "host_dst is NULL");
+    if (!h->last_select) {
+        for (int i = 0; i < h->S; ++i) host_dst[i] = -1;
+        return DSA_OK;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(host_dst, h->last_sel, (size_t)h->S * 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "last selection copy");
+}
+
+int dsa_sync_status(dsa_handle h, void *stream)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    cudaStream_t st = (cudaStream_t)stream;
+    int word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, h->status, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "status copy");
+    if (word & dsa::ST_TIMEOUT) return fail(DSA_ERR_TIMEOUT, "a bounded wait in the decode kernel gave up");
+    if (word & dsa::ST_CHECK) return fail(DSA_ERR_DEVICE_CHECK, "device consistency check failed (skip mask count)");
+    return DSA_OK;
+}
+
+int dsa_set_splits(dsa_handle h, int nsplit)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (nsplit < 0) return fail(DSA_ERR_ARG, "nsplit must be >= 0");
+    if (nsplit > 0) {
+        int rc = ensure_partials(h, nsplit);
+        if (rc != DSA_OK) return rc;
+    }
+    h->forced_split = nsplit;
+    return DSA_OK;
+}
+
+int dsa_set_wait_limit(dsa_handle h, uint32_t limit)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    h->wait_limit = limit;
+    return DSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,237 @@
+"""Thin ctypes binding over libdsa.so (include/dsa.h).
+
+The module-level functions carry the C names and only marshal arguments:
+torch tensors become device pointers, torch streams become cudaStream_t.
+Every step of the decode path runs in the library's CUDA kernels; there is
+no fallback.  Importing this module raises if libdsa.so has not been built.
+
+Method: "Understanding and Exploiting Diagonal Attention Sparsity in
+Autoregressive Image Generation" (arXiv 2609.19702), section 4, Algorithm 1.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB
+
+if not os.path.exists(LIB):
+    raise ImportError(f"libdsa.so is not built ({LIB}); run ar_image_gen_gb300.build.build()")
+
+_L = ctypes.CDLL(LIB)
+
+DSA_OK = 0
+DSA_ERR_ARG = -1
+DSA_ERR_STATE = -2
+DSA_ERR_OOM = -3
+DSA_ERR_CUDA = -4
+DSA_ERR_TIMEOUT = -5
+DSA_ERR_DEVICE_CHECK = -6
+DSA_BF16 = 0
+DSA_F32 = 1
+
+STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_ARG", -2: "DSA_ERR_STATE", -3: "DSA_ERR_OOM", -4: "DSA_ERR_CUDA",
+                -5: "DSA_ERR_TIMEOUT", -6: "DSA_ERR_DEVICE_CHECK"}
+
+EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa_destroy", "dsa_get_step",
+           "dsa_get_skip_mask", "dsa_get_last_selection", "dsa_sync_status", "dsa_last_error",
+           "dsa_state_bytes", "dsa_plan_step", "dsa_set_splits", "dsa_set_wait_limit",
+           "dsa_debug_fail_alloc_after"]
+
+
+class dsa_step_plan(ctypes.Structure):
+    _fields_ = [("phase", ctypes.c_int), ("t_inner", ctypes.c_int), ("n_prefix", ctypes.c_int),
+                ("n_decode", ctypes.c_int), ("select", ctypes.c_int), ("nsplit", ctypes.c_int),
+                ("chunk", ctypes.c_int), ("grid", ctypes.c_int), ("algo_bytes", ctypes.c_ulonglong)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_L.dsa_create.argtypes = [_I] * 6 + [ctypes.POINTER(_P)]
+_L.dsa_create_ex.argtypes = [_I] * 7 + [ctypes.POINTER(_P)]
+_L.dsa_prefill.argtypes = [_P, _P, _P, _P]
+_L.dsa_decode_step.argtypes = [_P, _P, _P, _P, _P, _P]
+_L.dsa_destroy.argtypes = [_P]
+_L.dsa_get_step.argtypes = [_P, ctypes.POINTER(_I)]
+_L.dsa_get_skip_mask.argtypes = [_P, _P, _P]
+_L.dsa_get_last_selection.argtypes = [_P, _P, _P]
+_L.dsa_sync_status.argtypes = [_P, _P]
+_L.dsa_last_error.restype = ctypes.c_char_p
+_L.dsa_state_bytes.argtypes = [_I] * 6
+_L.dsa_state_bytes.restype = ctypes.c_size_t
+_L.dsa_plan_step.argtypes = [_P, _I, ctypes.POINTER(dsa_step_plan)]
+_L.dsa_set_splits.argtypes = [_P, _I]
+_L.dsa_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
+_L.dsa_debug_fail_alloc_after.argtypes = [_I]
+
+
+class DSAError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)}: {dsa_last_error()}")
+
+
+def _check(code: int, what: str) -> int:
+    if code != DSA_OK:
+        raise DSAError(code, what)
+    return code
+
+
+def _ptr(x) -> int | None:
+    """Device (or host) address of a tensor / ndarray / int, None for None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        try:
+            import torch
+            return torch.cuda.current_stream().cuda_stream
+        except Exception:
+            return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def library_path() -> str:
+    return LIB
+
+
+# ---- C names ---------------------------------------------------------------
+
+def dsa_last_error() -> str:
+    return (_L.dsa_last_error() or b"").decode()
+
+
+def dsa_create(heads, head_dim, L_p, N_r, N_att, sink=0):
+    h = _P()
+    return _L.dsa_create(heads, head_dim, L_p, N_r, N_att, sink, ctypes.byref(h)), h
+
+
+def dsa_create_ex(heads, head_dim, L_p, N_r, N_att, sink, dtype):
+    h = _P()
+    return _L.dsa_create_ex(heads, head_dim, L_p, N_r, N_att, sink, dtype, ctypes.byref(h)), h
+
+
+def dsa_prefill(h, K, V, stream=None) -> int:
+    return _L.dsa_prefill(h, _ptr(K), _ptr(V), _stream(stream))
+
+
+def dsa_decode_step(h, q, k_new, v_new, out, stream=None) -> int:
+    return _L.dsa_decode_step(h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out), _stream(stream))
+
+
+def dsa_destroy(h) -> int:
+    return _L.dsa_destroy(h)
+
+
+def dsa_get_step(h):
+    t = _I()
+    return _L.dsa_get_step(h, ctypes.byref(t)), t.value
+
+
+def dsa_get_skip_mask(h, host_dst: np.ndarray, stream=None) -> int:
+    assert host_dst.dtype == np.uint32 and host_dst.flags["C_CONTIGUOUS"]
+    return _L.dsa_get_skip_mask(h, host_dst.ctypes.data, _stream(stream))
+
+
+def dsa_get_last_selection(h, host_dst: np.ndarray, stream=None) -> int:
+    assert host_dst.dtype == np.int32 and host_dst.flags["C_CONTIGUOUS"]
+    return _L.dsa_get_last_selection(h, host_dst.ctypes.data, _stream(stream))
+
+
+def dsa_sync_status(h, stream=None) -> int:
+    return _L.dsa_sync_status(h, _stream(stream))
+
+
+def dsa_state_bytes(heads, head_dim, L_p, N_r, sink=0, dtype=DSA_BF16) -> int:
+    return int(_L.dsa_state_bytes(heads, head_dim, L_p, N_r, sink, dtype))
+
+
+def dsa_plan_step(h, t):
+    p = dsa_step_plan()
+    return _L.dsa_plan_step(h, t, ctypes.byref(p)), p
+
+
+def dsa_set_splits(h, nsplit) -> int:
+    return _L.dsa_set_splits(h, nsplit)
+
+
+def dsa_set_wait_limit(h, limit) -> int:
+    return _L.dsa_set_wait_limit(h, limit)
+
+
+def dsa_debug_fail_alloc_after(n) -> int:
+    return _L.dsa_debug_fail_alloc_after(n)
+
+
+# ---- convenience wrapper ---------------------------------------------------
+
+class DSA:
+    """One handle: `heads` streams of one layer stepping together."""
+
+    def __init__(self, heads, head_dim, L_p, N_r, N_att, sink=0, dtype="bf16"):
+        self.dtype_code = {"bf16": DSA_BF16, "f32": DSA_F32}[dtype]
+        code, h = dsa_create_ex(heads, head_dim, L_p, N_r, N_att, sink, self.dtype_code)
+        _check(code, "dsa_create_ex")
+        self.h = h
+        self.heads, self.head_dim, self.L_p, self.N_r, self.N_att, self.sink = heads, head_dim, L_p, N_r, N_att, sink
+        self.mask_words = (N_r - sink + 31) // 32
+
+    def close(self):
+        if getattr(self, "h", None):
+            dsa_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prefill(self, K, V, stream=None):
+        _check(dsa_prefill(self.h, K, V, stream), "dsa_prefill")
+
+    def decode_step(self, q, k_new, v_new, out, stream=None):
+        _check(dsa_decode_step(self.h, q, k_new, v_new, out, stream), "dsa_decode_step")
+
+    @property
+    def t(self) -> int:
+        code, t = dsa_get_step(self.h)
+        _check(code, "dsa_get_step")
+        return t
+
+    def skip_mask(self, stream=None) -> np.ndarray:
+        dst = np.zeros((self.heads, self.mask_words), dtype=np.uint32)
+        _check(dsa_get_skip_mask(self.h, dst, stream), "dsa_get_skip_mask")
+        return dst
+
+    def last_selection(self, stream=None) -> np.ndarray:
+        dst = np.zeros(self.heads, dtype=np.int32)
+        _check(dsa_get_last_selection(self.h, dst, stream), "dsa_get_last_selection")
+        return dst
+
+    def sync_status(self, stream=None) -> int:
+        return dsa_sync_status(self.h, stream)
+
+    def plan(self, t: int | None = None) -> dsa_step_plan:
+        code, p = dsa_plan_step(self.h, self.t if t is None else t)
+        _check(code, "dsa_plan_step")
+        return p
+
+    def set_splits(self, nsplit: int):
+        _check(dsa_set_splits(self.h, nsplit), "dsa_set_splits")
+
+    def set_wait_limit(self, limit: int):
+        _check(dsa_set_wait_limit(self.h, limit), "dsa_set_wait_limit")

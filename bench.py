@@ -1,0 +1,499 @@
+"""Throughput of diagonal-aware sparse decode attention on GB300.
+
+A bench step is one decode step of the whole hot path for every layer of the
+workload: 30 (or 32) per-layer handles, each one fused kernel launch over
+batch x heads streams (append + evict, index set from the skip bitmask,
+gather, split-K softmax.V, fused argmin).  The metric counts stream-steps
+(sequence x layer x head) per second.
+
+Default workload: the Janus-Pro-7B-shaped attention stack (30 layers x 32
+heads x head_dim 128, bf16 KV, L_p 64, 24x24 grid = 576 decode tokens,
+N_r 288, 95 % sparsity -> N_att 29) at batch 96, in the phase-3 steady state
+(t >= N_r).  Inputs are seeded synthetic traces resident in HBM; each step
+touches 30 distinct layers' KV (about 4.4 GB), far more than the 129 MB L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+sequences (weak scaling, no data-path collective); the time is the max over
+ranks and the value counts all ranks' stream-steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode attn steps/s (batch·layers·heads) and HBM GB/s vs peak @95%"
+UNIT = "stream-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["ar_image_gen_gb300/csrc/dsa_decode.cuh", "ar_image_gen_gb300/csrc/dsa_ptx.cuh",
+                  "ar_image_gen_gb300/csrc/dsa_api.cu"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, or None when the kernel changed since the capture."""
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.json")
+    try:
+        with open(path) as f:
+            prof = json.load(f)
+    except Exception:
+        return None
+    if prof.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return prof.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str | None):
+        self.proc = None
+        self.uuid = gpu_uuid
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd.insert(1, f"--id={self.uuid}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for name, flag in zip(names, f[4:8]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, ws
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def workload_config(wl, phase: str) -> dict:
+    return {
+        "workload": (f"{wl.name}: {wl.layers} layers x {wl.heads} heads x head_dim {wl.head_dim}, "
+                     f"batch {wl.batch}, {wl.dtype} KV, L_p {wl.L_p}, L_dec {wl.L_dec} "
+                     f"({wl.grid}x{wl.grid} grid), N_r {wl.N_r}, N_att {wl.N_att}, sink {wl.sink}; {phase}"),
+        "streams_per_layer": wl.streams,
+        "layers": wl.layers,
+        "l2": "no flush: each step reads every layer's KV (working set >> 129 MB L2)",
+    }
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of the same workload
+# ----------------------------------------------------------------------------
+
+def oracle_baseline(wl, n_streams: int = 48, timed_steps: int = 24, budget_s: float = 20.0,
+                    device: str = "cuda") -> dict:
+    """Times the C oracle (fp64, as it stands) on `n_streams` streams of layer
+    0 over phase-3 steps N_r .. N_r + timed_steps, after running the earlier
+    steps untimed; host threads = all cores the process may use."""
+    import numpy as np
+
+    from ar_image_gen_gb300.synth import TraceGen
+    from oracle.oracle import OracleBatch, max_threads
+
+    gen = TraceGen(wl.with_batch(max(1, (n_streams + wl.heads - 1) // wl.heads)), layer=0, device=device)
+    n = min(n_streams, gen.S)
+    threads = max_threads()
+    orc = OracleBatch(n, wl.head_dim, wl.L_p, wl.N_r, wl.N_att, wl.sink)
+    Kp, Vp = gen.prompt()
+    orc.prefill(Kp[:n].double().cpu().numpy(), Vp[:n].double().cpu().numpy())
+    t_start = wl.N_r
+    steps = []
+    for t in range(min(t_start + timed_steps, wl.L_dec)):
+        q, k, v = (x[:n].double().cpu().numpy() for x in gen.step(t))
+        steps.append((t, q, k, v))
+    for t, q, k, v in steps[:t_start]:
+        orc.step(q, k, v, threads=threads)
+    done, t0 = 0, time.perf_counter()
+    for t, q, k, v in steps[t_start:]:
+        orc.step(q, k, v, threads=threads)
+        done += n
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return {"value": done / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} streams of layer 0, phase-3 steps {t_start}..{t_start + done // n - 1} "
+                      f"({done} stream-steps, {el:.2f} s, fp64 C oracle)"}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+class Stack:
+    """Per-layer handles of one workload, prefilled and advanced to a step."""
+
+    def __init__(self, wl, pool_steps: int, device: str = "cuda"):
+        import torch
+
+        from ar_image_gen_gb300.dsa import DSA
+        from ar_image_gen_gb300.synth import TraceGen
+
+        self.wl = wl
+        self.handles = []
+        self.gens = []
+        self.outs = []
+        for layer in range(wl.layers):
+            gen = TraceGen(wl, layer=layer, device=device)
+            h = DSA(wl.streams, wl.head_dim, wl.L_p, wl.N_r, wl.N_att, wl.sink, wl.dtype)
+            Kp, Vp = gen.prompt()
+            h.prefill(Kp, Vp)
+            self.handles.append(h)
+            self.gens.append(gen)
+            self.outs.append(torch.empty((wl.streams, wl.head_dim), dtype=Kp.dtype, device=device))
+        self.pool_steps = pool_steps
+        self.pool = None
+
+    def advance(self, t_end: int, generate: bool = True):
+        """Decode steps t = current .. t_end - 1 with freshly drawn inputs."""
+        t = self.handles[0].t
+        while t < t_end:
+            for layer, h in enumerate(self.handles):
+                q, k, v = self.gens[layer].step(min(t, self.wl.L_dec - 1)) if generate else self.pool[t % self.pool_steps][layer]
+                h.decode_step(q, k, v, self.outs[layer])
+            t += 1
+
+    def make_pool(self, t0: int):
+        """Inputs of pool_steps consecutive steps from t0, resident in HBM."""
+        self.pool = []
+        for i in range(self.pool_steps):
+            t = min(t0 + i, self.wl.L_dec - 1)
+            self.pool.append([self.gens[layer].step(t) for layer in range(self.wl.layers)])
+
+    def close(self):
+        for h in self.handles:
+            h.close()
+        self.handles = []
+
+
+def time_steps(stack, steps: int, per_launch: bool):
+    """Runs `steps` bench steps from the input pool; returns (elapsed_ms,
+    mean per-launch ms or None, launches)."""
+    import torch
+
+    wl = stack.wl
+    stream = torch.cuda.current_stream()
+    launches = 0
+    evs = []
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    t = stack.handles[0].t
+    for i in range(steps):
+        inputs = stack.pool[(t + i) % stack.pool_steps]
+        for layer, h in enumerate(stack.handles):
+            q, k, v = inputs[layer]
+            if per_launch:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                h.decode_step(q, k, v, stack.outs[layer], stream)
+                e1.record(stream)
+                evs.append((e0, e1))
+            else:
+                h.decode_step(q, k, v, stack.outs[layer], stream)
+            launches += 1
+    end.record(stream)
+    torch.cuda.synchronize()
+    el = start.elapsed_time(end)
+    per = statistics.fmean(a.elapsed_time(b) for a, b in evs) if evs else None
+    return el, per, launches
+
+
+def time_e2e(stack, steps: int):
+    """Same metric through the public API with host-resident inputs: every
+    step copies q, k_new, v_new of all layers from pinned host memory to the
+    device, decodes, and copies every layer's output back to pinned host
+    memory.  Returns (elapsed_ms, h2d bytes per step, d2h bytes per step)."""
+    import torch
+
+    wl = stack.wl
+    stream = torch.cuda.current_stream()
+    host_in = [[x.to("cpu").pin_memory() for x in stack.pool[i % stack.pool_steps][0]] for i in range(2)]
+    dev_in = [torch.empty_like(x, device="cuda") for x in stack.pool[0][0]]
+    host_in = [[[x.clone().pin_memory() for x in host_in[i % 2]] for _ in range(wl.layers)] for i in range(2)]
+    host_out = [torch.empty_like(stack.outs[0], device="cpu").pin_memory() for _ in range(wl.layers)]
+    h2d = sum(x.numel() * x.element_size() for x in dev_in) * wl.layers
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    start.record(stream)
+    for i in range(steps):
+        for layer, h in enumerate(stack.handles):
+            src = host_in[i % 2][layer]
+            for d, s in zip(dev_in, src):
+                d.copy_(s, non_blocking=True)
+            h.decode_step(dev_in[0], dev_in[1], dev_in[2], stack.outs[layer], stream)
+            host_out[layer].copy_(stack.outs[layer], non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - t0) * 1e3
+    return max(start.elapsed_time(end), wall), h2d, d2h
+
+
+def run_ours(args, rank: int, ws: int) -> dict | None:
+    import torch
+
+    from __graft_entry__ import build
+    from ar_image_gen_gb300.synth import WORKLOADS
+
+    build()
+    torch.cuda.init()
+    wl = WORKLOADS[args.workload]
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        pass
+
+    # --- sparse setting, phase-3 steady state
+    stack = Stack(wl, pool_steps=args.pool)
+    t_start = wl.N_r + wl.sink
+    stack.advance(t_start)
+    stack.make_pool(t_start)
+    plan = stack.handles[0].plan(t_start)
+    _, _, _ = time_steps(stack, args.warmup, per_launch=False)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(uuid) as clk:
+        el_ms, _, launches = time_steps(stack, args.steps, per_launch=False)
+    el_ms = max_over_ranks(el_ms, ws)
+    # per-launch durations over a second timed pass (events between launches)
+    _, per_launch_ms, _ = time_steps(stack, max(4, min(args.steps, 50)), per_launch=True)
+    stream_steps = wl.streams * wl.layers * args.steps * ws
+    value = stream_steps / (el_ms / 1e3)
+    peak, peak_kind = measured_peak()
+    achieved = plan.algo_bytes / (per_launch_ms / 1e3) / 1e9
+    whole = plan.algo_bytes * wl.layers * args.steps / (el_ms / 1e3) / 1e9 * ws / ws
+    traffic = profiled_traffic(args.workload)
+
+    # --- end to end through the public API with host buffers
+    e2e_steps = max(3, min(args.steps // 4, 100))
+    e2e_ms, h2d, d2h = time_e2e(stack, e2e_steps)
+    e2e_ms = max_over_ranks(e2e_ms, ws)
+    e2e_value = wl.streams * wl.layers * e2e_steps * ws / (e2e_ms / 1e3)
+
+    # last step of the trace, sparse
+    stack.advance(wl.L_dec - 1, generate=False)
+    last_sparse_ms = _last_step_ms(stack)
+    status = max((h.sync_status() for h in stack.handles), key=abs)
+    stack.close()
+    del stack
+    torch.cuda.empty_cache()
+
+    # --- dense setting (0 % sparsity) of the same kernel: N_r = N_att = L_dec
+    dense = None
+    if not args.no_dense:
+        dwl = wl.dense()
+        dstack = Stack(dwl, pool_steps=args.pool)
+        dstack.make_pool(0)
+        d_steps = max(2, min(args.dense_steps, dwl.L_dec - 1))
+        dstack.advance(dwl.L_dec - 1 - d_steps, generate=False)
+        dplan_first = dstack.handles[0].plan()
+        d_ms, d_per, _ = time_steps(dstack, d_steps, per_launch=True)
+        d_bytes = sum(dstack.handles[0].plan(dplan_first.t_inner + i).algo_bytes for i in range(d_steps))
+        last_dense_ms = _last_step_ms(dstack)
+        dplan_last = dstack.handles[0].plan(dwl.L_dec - 1)
+        dense = {
+            "workload": f"{dwl.name}: N_r = N_att = L_dec = {dwl.L_dec}, steps {dplan_first.t_inner}.."
+                        f"{dplan_first.t_inner + d_steps - 1}",
+            "value": dwl.streams * dwl.layers * d_steps / (d_ms / 1e3), "unit": UNIT,
+            "hbm_gbs": d_bytes * dwl.layers / (d_ms / 1e3) / 1e9,
+            "frac": d_bytes * dwl.layers / (d_ms / 1e3) / 1e9 / peak,
+            "last_step_gbs": dplan_last.algo_bytes * dwl.layers / (last_dense_ms / 1e3) / 1e9,
+        }
+        dstack.close()
+        del dstack
+        torch.cuda.empty_cache()
+        dense["last_step_ms"] = last_dense_ms
+        dense["last_step_speedup_sparse_vs_dense"] = last_dense_ms / last_sparse_ms
+
+    if rank != 0:
+        return None
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": workload_config(wl, f"phase-3 steady state from t = {t_start}"),
+        "hbm_gbs": whole,
+        "roofline": {"bound": "hbm", "kernel": "dsa::decode_kernel<bf16,128>", "achieved": achieved,
+                     "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algo_bytes_per_launch": plan.algo_bytes, "launch_ms": per_launch_ms,
+                     "grid": plan.grid, "nsplit": plan.nsplit},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "last_step": {"sparse_ms": last_sparse_ms},
+        "dense": dense,
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = oracle_baseline(wl, budget_s=args.cpu_budget)
+    return res
+
+
+def _last_step_ms(stack) -> float:
+    """Duration of the final decode step of the trace (all layers)."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t = stack.handles[0].t
+    a.record(stream)
+    for layer, h in enumerate(stack.handles):
+        q, k, v = stack.pool[t % stack.pool_steps][layer]
+        h.decode_step(q, k, v, stack.outs[layer], stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
+def run_reference(args, rank: int, ws: int) -> dict | None:
+    """The reference arm: the CPU oracle, as it stands, on this workload."""
+    if rank != 0:
+        return None
+    import torch
+
+    from ar_image_gen_gb300.synth import WORKLOADS
+    from oracle.oracle import build as build_oracle
+
+    build_oracle()
+    wl = WORKLOADS[args.workload]
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    per_step = []
+    base = None
+    for _ in range(args.warmup + args.steps):
+        base = oracle_baseline(wl, n_streams=16, timed_steps=4, budget_s=5.0, device=device)
+        per_step.append(base["value"])
+    vals = per_step[args.warmup:]
+    value = statistics.fmean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.streams * wl.layers / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl, f"phase-3 steady state from t = {wl.N_r + wl.sink}"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": base["cores"], "kind": "oracle",
+                         "sample": "each step: " + base["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="janus-b96")
+    ap.add_argument("--pool", type=int, default=8, help="distinct input steps kept in HBM and cycled")
+    ap.add_argument("--dense-steps", type=int, default=16)
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, ws = dist_setup()
+    res = run_reference(args, rank, ws) if args.impl == "reference" else run_ours(args, rank, ws)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * dsa.h -- C ABI of the diagonal-aware sparse decode attention library
+ * (libdsa.so, CUDA, sm_103a).
+ *
+ * The method is from "Understanding and Exploiting Diagonal Attention
+ * Sparsity in Autoregressive Image Generation" (arXiv 2609.19702), section 4
+ * "Diagonal-Aware Sparse Attention", Algorithm 1 and Fig. 12; the sink
+ * variant is "Diagonal+sink4" of section 5.1.  Per decode step and per
+ * stream (one sequence x one head of one layer) it attends the whole prompt
+ * KV plus N_att of the N_r most recent decode KV entries, grows a per-stream
+ * skip set by the argmin of the current logits during phase 2, moves that set
+ * along the diagonal every step, and evicts the oldest entry once the window
+ * is full.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - A handle holds `heads` independent streams (e.g. batch x heads of one
+ *   layer) that all step together with one decode step counter t (0-based).
+ *   Use one handle per layer.
+ * - Device pointers are plain CUDA device addresses (e.g. a torch tensor's
+ *   data_ptr()), C-contiguous, 16-byte aligned.  `stream` is a cudaStream_t
+ *   passed as void* (NULL = the legacy default stream).  The library issues
+ *   all device work on that stream and never synchronizes it, except in the
+ *   functions documented as synchronous.
+ * - Element type: DSA_BF16 (q, k, v, out and the stored KV are bf16,
+ *   arithmetic in fp32) or DSA_F32 (all fp32).
+ * - Ownership: the library owns every state buffer of a handle (prompt
+ *   prefix, decode ring, skip bitmask, split partials) and frees them in
+ *   dsa_destroy.  The caller owns q / k_new / v_new / out / K / V and must
+ *   keep them alive until `stream` has passed the call.
+ * - Errors: every function returns DSA_OK or a negative dsa_status.  Errors
+ *   found on the host are returned at once and leave the handle unchanged;
+ *   the message is available from dsa_last_error() on the same thread.
+ *   Errors found on the device (a bounded wait that gave up, an internal
+ *   consistency check) are recorded in a sticky per-handle status word that
+ *   dsa_sync_status() reads.
+ * - A handle is not thread-safe: do not call into one handle from two host
+ *   threads at once.  Different handles are independent.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dsa_ctx *dsa_handle;
+
+enum dsa_status {
+    DSA_OK = 0,
+    DSA_ERR_ARG = -1,          /* bad argument (value, size, NULL or unaligned pointer) */
+    DSA_ERR_STATE = -2,        /* call out of order (decode before prefill, bad handle) */
+    DSA_ERR_OOM = -3,          /* device allocation failed */
+    DSA_ERR_CUDA = -4,         /* a CUDA runtime call failed (no device, launch error) */
+    DSA_ERR_TIMEOUT = -5,      /* device: a bounded wait in a kernel gave up */
+    DSA_ERR_DEVICE_CHECK = -6  /* device: an internal consistency check failed */
+};
+
+enum dsa_dtype { DSA_BF16 = 0, DSA_F32 = 1 };
+
+/*
+ * dsa_create / dsa_create_ex -- allocate the state of `heads` streams.
+ *
+ * Algorithm 1 inputs (section 4): N_r is the recent-window size (decode KV
+ * kept per stream; the page uses N_r = 0.5 L_dec), N_att the number of
+ * decode tokens attended per step (sparsity 1 - N_att / L_dec), L_p the
+ * prompt length.  `sink` > 0 selects the Diagonal+sink4 variant (section 5.1)
+ * with `sink` attention sinks: decode tokens 0..sink-1 are kept and attended
+ * at every step; the algorithm runs on the later tokens with a window of
+ * N_r - sink and a budget of N_att - sink, so at most N_r decode entries are
+ * held and at most N_att attended.  N_r = N_att = L_dec gives dense decode
+ * attention; N_att = N_r gives a sliding window (StreamingLLM with sink).
+ *
+ * Requirements: heads >= 1; head_dim in {64, 128}; L_p >= 0;
+ * 1 <= N_att <= N_r <= 65536 (+ sink); sink >= 0 and, if sink > 0,
+ * N_att > sink.  dsa_create uses DSA_BF16.  Device memory:
+ * dsa_state_bytes() plus split partials.  On success *out receives the
+ * handle; on failure *out is set to NULL and nothing stays allocated.
+ * Uses the current CUDA device.
+ */
+int dsa_create(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, dsa_handle *out);
+int dsa_create_ex(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int dtype,
+                  dsa_handle *out);
+
+/*
+ * dsa_prefill -- load the prompt KV and reset the decode state (t = 0, empty
+ * skip sets, status cleared).  Section 4, Algorithm 1 inputs K_p, V_p: the
+ * prompt KV is always attended in full ("Throughout all phases, the prompt
+ * KV is always attended in full").
+ *
+ * K, V: device, [heads, L_p, head_dim] of the handle's dtype (may be NULL
+ * when L_p = 0).  Asynchronous on `stream`.
+ */
+int dsa_prefill(dsa_handle h, const void *K, const void *V, void *stream);
+
+/*
+ * dsa_decode_step -- one decode step t for every stream, then t += 1.
+ * Section 4, Algorithm 1 (all three phases) in one kernel launch:
+ *   - append k_new, v_new as decode entry t (in the ring slot of the entry
+ *     evicted at this step once t >= N_r: "K[t - N_r] <- empty");
+ *   - attend q over the prompt rows plus the attended window entries
+ *     idx = window - skip_idx; softmax and the weighted sum of V in fp32
+ *     (split across CTAs when a stream is long);
+ *   - in phase 2 (N_att - 1 <= t <= N_r - 2, sink removed) append the
+ *     attended decode entry with the lowest logit q.k to the skip set (ties:
+ *     the oldest); the entry is skipped from step t + 1 on.  The skip set is
+ *     kept as relative offsets r = t - position, which the +1 diagonal shift
+ *     leaves unchanged.
+ * q, k_new, v_new: device, [heads, head_dim]; out: device, [heads, head_dim]
+ * receives softmax(q [K_p; K[idx]]^T / sqrt(head_dim)) [V_p; V[idx]].
+ * Asynchronous on `stream`.  Returns DSA_ERR_STATE before dsa_prefill.
+ */
+int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *v_new, void *out,
+                    void *stream);
+
+/* dsa_destroy -- free the handle and its device memory (synchronizes the
+ * device first so no launch still uses it).  NULL is accepted. */
+int dsa_destroy(dsa_handle h);
+
+/* dsa_get_step -- the next decode step t (number of steps taken). */
+int dsa_get_step(dsa_handle h, int *t);
+
+/*
+ * dsa_get_skip_mask -- copy the skip sets to host memory (synchronous on
+ * `stream`).  host_dst: [heads, ceil((N_r - sink) / 32)] uint32; bit r of
+ * stream s is set when relative offset r = t - position (of the decode
+ * entries after the sinks) is skipped.  Not on the decode path.
+ */
+int dsa_get_skip_mask(dsa_handle h, uint32_t *host_dst, void *stream);
+
+/*
+ * dsa_get_last_selection -- per stream, the relative offset r* = t - j*
+ * appended to the skip set by the last decode step, or -1 for every stream
+ * if that step made no selection.  host_dst: [heads] int32.  Synchronous on
+ * `stream`.  Not on the decode path.
+ */
+int dsa_get_last_selection(dsa_handle h, int32_t *host_dst, void *stream);
+
+/*
+ * dsa_sync_status -- synchronize `stream` and return the sticky device
+ * status: DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_CHECK (or DSA_ERR_CUDA
+ * if the synchronization itself failed).  dsa_prefill clears it.
+ */
+int dsa_sync_status(dsa_handle h, void *stream);
+
+/* dsa_last_error -- message of the last failed call on this host thread
+ * ("" if none).  The pointer stays valid until the next call on the thread. */
+const char *dsa_last_error(void);
+
+/*
+ * dsa_state_bytes -- device bytes of the persistent state of a handle:
+ * prompt prefix (L_p + sink rows) and decode ring (N_r - sink slots) of K
+ * and V, plus the skip bitmask, per stream.  This is the KV footprint bound
+ * N_r + L_p of the cost analysis (section 4).  Split partials are extra.
+ * Returns 0 for invalid arguments.
+ */
+size_t dsa_state_bytes(int heads, int head_dim, int L_p, int N_r, int sink, int dtype);
+
+/*
+ * Step plan: what dsa_decode_step does at step t (host computation only).
+ * algo_bytes counts, over all streams, the HBM bytes the step must move:
+ * the attended K and V rows read from the prefix and the ring (the current
+ * token counted once, through k_new / v_new), q, k_new and v_new read, the
+ * new entry written and out written.  The skip-bitmask read is excluded.
+ */
+typedef struct dsa_step_plan {
+    int phase;                 /* 0: sink fill, 1 / 2 / 3: Algorithm 1 phases */
+    int t_inner;               /* t - sink, or -1 during the sink fill */
+    int n_prefix;              /* always-attended rows (prompt plus sinks) */
+    int n_decode;              /* attended decode rows, current token included */
+    int select;                /* 1 if this step appends to the skip set */
+    int nsplit;                /* CTAs per stream */
+    int chunk;                 /* rows per CTA */
+    int grid;                  /* CTAs launched */
+    unsigned long long algo_bytes;
+} dsa_step_plan;
+
+int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out);
+
+/* Tuning and test knobs (not needed for normal use). */
+
+/* Force the number of CTAs per stream (>= 1), or 0 for the automatic
+ * choice.  Grows the partial buffers if needed (allocates; not on the
+ * decode path). */
+int dsa_set_splits(dsa_handle h, int nsplit);
+
+/* Iteration limit of the bounded waits inside the decode kernel (default
+ * about 2^22).  A limit of 0 makes every wait give up at once; the kernel
+ * then records DSA_ERR_TIMEOUT, lets its own copies land and returns.  Used
+ * to test the timeout path without a real hang. */
+int dsa_set_wait_limit(dsa_handle h, uint32_t limit);
+
+/* Make the n-th following device allocation of this library fail (n >= 1),
+ * or disable with n <= 0.  Host-side; tests the out-of-memory paths. */
+int dsa_debug_fail_alloc_after(int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H */

@@ -1,0 +1,80 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+include/dsa.h declares, and rejects bad arguments on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from __graft_entry__ import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    build()
+    from ar_image_gen_gb300 import dsa as mod
+    return mod
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("dsa_create", "dsa_prefill", "dsa_decode_step", "dsa_destroy"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(dsa):
+    lib = ctypes.CDLL(dsa.library_path())
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(declared_functions()) == set(dsa.EXPORTS)
+
+
+@pytest.mark.parametrize("args", [
+    (0, 128, 64, 288, 29, 0),      # no streams
+    (8, 96, 64, 288, 29, 0),       # unsupported head_dim
+    (8, 128, -1, 288, 29, 0),      # negative prompt
+    (8, 128, 64, 288, 0, 0),       # N_att < 1
+    (8, 128, 64, 288, 289, 0),     # N_att > N_r
+    (8, 128, 64, 288, 4, 4),       # N_att <= sink
+    (8, 128, 64, 288, 29, -1),     # negative sink
+    (8, 128, 64, 70000, 29, 0),    # window beyond the 16-bit offset range
+])
+def test_create_rejects_bad_arguments(dsa, args):
+    code, h = dsa.dsa_create(*args)
+    assert code == dsa.DSA_ERR_ARG
+    assert not h.value
+    assert dsa.dsa_last_error()
+
+
+def test_create_rejects_bad_dtype(dsa):
+    code, h = dsa.dsa_create_ex(8, 128, 64, 288, 29, 0, 7)
+    assert code == dsa.DSA_ERR_ARG and "dtype" in dsa.dsa_last_error()
+
+
+def test_calls_on_a_null_handle_fail_cleanly(dsa):
+    null = ctypes.c_void_p()
+    assert dsa.dsa_destroy(null) == dsa.DSA_OK
+    assert dsa.dsa_prefill(null, None, None) == dsa.DSA_ERR_STATE
+    assert dsa.dsa_decode_step(null, 16, 16, 16, 16) == dsa.DSA_ERR_STATE
+    assert dsa.dsa_get_step(null)[0] == dsa.DSA_ERR_STATE
+    assert dsa.dsa_sync_status(null) == dsa.DSA_ERR_STATE
+    assert dsa.dsa_plan_step(null, 0)[0] == dsa.DSA_ERR_STATE
+
+
+def test_state_bytes_is_the_kv_bound(dsa):
+    # prefix (L_p + sink) + ring (N_r - sink) rows of K and V, plus the mask:
+    # the N_r + L_p footprint of the cost analysis.
+    S, d, L_p, N_r = 3072, 128, 64, 288
+    row = 2 * d * 2
+    assert dsa.dsa_state_bytes(S, d, L_p, N_r, 0, dsa.DSA_BF16) == S * ((L_p + N_r) * row + 9 * 4)
+    assert dsa.dsa_state_bytes(S, d, L_p, N_r, 4, dsa.DSA_BF16) == S * ((L_p + N_r) * row + 9 * 4)
+    assert dsa.dsa_state_bytes(4, 64, 16, 32, 0, dsa.DSA_F32) == 4 * (48 * 2 * 64 * 4 + 4)
+    assert dsa.dsa_state_bytes(0, 128, 64, 288, 0, 0) == 0
