@@ -170,39 +170,57 @@ def workload_config(wl, phase: str) -> dict:
 # CPU baseline: the oracle on a bounded sample of the same workload
 # ----------------------------------------------------------------------------
 
-def oracle_baseline(wl, n_streams: int = 48, timed_steps: int = 24, budget_s: float = 20.0,
-                    device: str = "cuda") -> dict:
-    """Times the C oracle (fp64, as it stands) on `n_streams` streams of layer
-    0 over phase-3 steps N_r .. N_r + timed_steps, after running the earlier
-    steps untimed; host threads = all cores the process may use."""
-    import numpy as np
+class OracleArm:
+    """The C oracle (fp64, as it stands) on `n` streams of layer 0 of the
+    workload, brought untimed to the phase-3 steady state."""
 
-    from ar_image_gen_gb300.synth import TraceGen
-    from oracle.oracle import OracleBatch, max_threads
+    def __init__(self, wl, n: int, device: str):
+        from ar_image_gen_gb300.synth import TraceGen
+        from oracle.oracle import OracleBatch, max_threads
 
-    gen = TraceGen(wl.with_batch(max(1, (n_streams + wl.heads - 1) // wl.heads)), layer=0, device=device)
-    n = min(n_streams, gen.S)
-    threads = max_threads()
-    orc = OracleBatch(n, wl.head_dim, wl.L_p, wl.N_r, wl.N_att, wl.sink)
-    Kp, Vp = gen.prompt()
-    orc.prefill(Kp[:n].double().cpu().numpy(), Vp[:n].double().cpu().numpy())
-    t_start = wl.N_r
-    steps = []
-    for t in range(min(t_start + timed_steps, wl.L_dec)):
-        q, k, v = (x[:n].double().cpu().numpy() for x in gen.step(t))
-        steps.append((t, q, k, v))
-    for t, q, k, v in steps[:t_start]:
-        orc.step(q, k, v, threads=threads)
-    done, t0 = 0, time.perf_counter()
-    for t, q, k, v in steps[t_start:]:
-        orc.step(q, k, v, threads=threads)
-        done += n
-        if time.perf_counter() - t0 > budget_s:
-            break
-    el = time.perf_counter() - t0
-    return {"value": done / el, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{n} streams of layer 0, phase-3 steps {t_start}..{t_start + done // n - 1} "
-                      f"({done} stream-steps, {el:.2f} s, fp64 C oracle)"}
+        self.wl = wl
+        self.gen = TraceGen(wl.with_batch(max(1, (n + wl.heads - 1) // wl.heads)), layer=0, device=device)
+        self.n = min(n, self.gen.S)
+        self.threads = max_threads()
+        self.orc = OracleBatch(self.n, wl.head_dim, wl.L_p, wl.N_r, wl.N_att, wl.sink)
+        Kp, Vp = self.gen.prompt()
+        self.orc.prefill(Kp[: self.n].double().cpu().numpy(), Vp[: self.n].double().cpu().numpy())
+        self.t = 0
+
+    def inputs(self):
+        t = min(self.t, self.wl.L_dec - 1)
+        return [x[: self.n].double().cpu().numpy() for x in self.gen.step(t)]
+
+    def advance(self, t_end: int):
+        while self.t < t_end:
+            self.orc.step(*self.inputs(), threads=self.threads)
+            self.t += 1
+
+    def timed_step(self) -> float:
+        """One decode step of the sample; returns its seconds (input
+        generation excluded)."""
+        q, k, v = self.inputs()
+        t0 = time.perf_counter()
+        self.orc.step(q, k, v, threads=self.threads)
+        el = time.perf_counter() - t0
+        self.t += 1
+        return el
+
+
+def oracle_baseline(wl, n_streams: int = 0, budget_s: float = 10.0, device: str = "cuda") -> dict:
+    """Stream-steps/s of the oracle on phase-3 steps of a sample of layer 0,
+    timed until about `budget_s` seconds of oracle work have run."""
+    arm = OracleArm(wl, n_streams or wl.streams, device)
+    t0 = wl.N_r + wl.sink
+    arm.advance(t0)
+    spent, steps = 0.0, 0
+    while spent < budget_s and steps < 4 * wl.L_dec:
+        spent += arm.timed_step()
+        steps += 1
+    return {"value": arm.n * steps / spent, "unit": UNIT, "cores": arm.threads, "kind": "oracle",
+            "sample": f"{arm.n} streams of layer 0, phase-3 steps {t0}..{t0 + steps - 1} "
+                      f"({arm.n * steps} stream-steps in {spent:.1f} s of oracle time, fp64 C oracle, "
+                      f"input generation excluded)"}
 
 
 # ----------------------------------------------------------------------------
@@ -290,17 +308,17 @@ def time_steps(stack, steps: int, per_launch: bool):
 
 def time_e2e(stack, steps: int):
     """Same metric through the public API with host-resident inputs: every
-    step copies q, k_new, v_new of all layers from pinned host memory to the
+    step copies q, k_new, v_new of every layer from pinned host memory to the
     device, decodes, and copies every layer's output back to pinned host
     memory.  Returns (elapsed_ms, h2d bytes per step, d2h bytes per step)."""
     import torch
 
     wl = stack.wl
     stream = torch.cuda.current_stream()
-    host_in = [[x.to("cpu").pin_memory() for x in stack.pool[i % stack.pool_steps][0]] for i in range(2)]
-    dev_in = [torch.empty_like(x, device="cuda") for x in stack.pool[0][0]]
-    host_in = [[[x.clone().pin_memory() for x in host_in[i % 2]] for _ in range(wl.layers)] for i in range(2)]
-    host_out = [torch.empty_like(stack.outs[0], device="cpu").pin_memory() for _ in range(wl.layers)]
+    host_in = [[[x.to("cpu").pin_memory() for x in stack.pool[i][layer]] for layer in range(wl.layers)]
+               for i in range(2)]
+    dev_in = [torch.empty_like(x) for x in stack.pool[0][0]]
+    host_out = [torch.empty(tuple(o.shape), dtype=o.dtype).pin_memory() for o in stack.outs]
     h2d = sum(x.numel() * x.element_size() for x in dev_in) * wl.layers
     d2h = sum(x.numel() * x.element_size() for x in host_out)
     torch.cuda.synchronize()
@@ -309,9 +327,8 @@ def time_e2e(stack, steps: int):
     start.record(stream)
     for i in range(steps):
         for layer, h in enumerate(stack.handles):
-            src = host_in[i % 2][layer]
-            for d, s in zip(dev_in, src):
-                d.copy_(s, non_blocking=True)
+            for d, src in zip(dev_in, host_in[i % 2][layer]):
+                d.copy_(src, non_blocking=True)
             h.decode_step(dev_in[0], dev_in[1], dev_in[2], stack.outs[layer], stream)
             host_out[layer].copy_(stack.outs[layer], non_blocking=True)
     end.record(stream)
@@ -328,7 +345,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
 
     build()
     torch.cuda.init()
-    wl = WORKLOADS[args.workload]
+    wl = _workload(args)
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
@@ -353,7 +370,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     value = stream_steps / (el_ms / 1e3)
     peak, peak_kind = measured_peak()
     achieved = plan.algo_bytes / (per_launch_ms / 1e3) / 1e9
-    whole = plan.algo_bytes * wl.layers * args.steps / (el_ms / 1e3) / 1e9 * ws / ws
+    whole = plan.algo_bytes * wl.layers * args.steps * ws / (el_ms / 1e3) / 1e9
     traffic = profiled_traffic(args.workload)
 
     # --- end to end through the public API with host buffers
@@ -420,6 +437,8 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     }
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = oracle_baseline(wl, budget_s=args.cpu_budget)
+    if args.layers:
+        res["config"]["layers_override"] = args.layers
     return res
 
 
@@ -441,7 +460,8 @@ def _last_step_ms(stack) -> float:
 
 
 def run_reference(args, rank: int, ws: int) -> dict | None:
-    """The reference arm: the CPU oracle, as it stands, on this workload."""
+    """The reference arm: the CPU oracle, as it stands, on this workload.
+    Each bench step is one phase-3 decode step of a fixed sample of streams."""
     if rank != 0:
         return None
     import torch
@@ -450,30 +470,43 @@ def run_reference(args, rank: int, ws: int) -> dict | None:
     from oracle.oracle import build as build_oracle
 
     build_oracle()
-    wl = WORKLOADS[args.workload]
+    wl = _workload(args)
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    per_step = []
-    base = None
-    for _ in range(args.warmup + args.steps):
-        base = oracle_baseline(wl, n_streams=16, timed_steps=4, budget_s=5.0, device=device)
-        per_step.append(base["value"])
-    vals = per_step[args.warmup:]
-    value = statistics.fmean(vals)
+    arm = OracleArm(wl, args.ref_streams, device)
+    t0 = wl.N_r + wl.sink
+    arm.advance(t0)
+    for _ in range(args.warmup):
+        arm.timed_step()
+    spent = sum(arm.timed_step() for _ in range(args.steps))
+    value = arm.n * args.steps / spent
+    sample = (f"each step: one phase-3 decode step of {arm.n} streams of layer 0 "
+              f"(steps {t0 + args.warmup}..{t0 + args.warmup + args.steps - 1}), fp64 C oracle, "
+              f"input generation excluded")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.streams * wl.layers / value,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * spent / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(wl, f"phase-3 steady state from t = {wl.N_r + wl.sink}"),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": base["cores"], "kind": "oracle",
-                         "sample": "each step: " + base["sample"]},
+        "data": "synthetic", "config": workload_config(wl, f"phase-3 steady state from t = {t0}"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": arm.threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+def _workload(args):
+    from dataclasses import replace
+
+    from ar_image_gen_gb300.synth import WORKLOADS
+
+    wl = WORKLOADS[args.workload]
+    if args.layers:
+        wl = replace(wl, layers=args.layers)
+    return wl
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="janus-b96")
@@ -481,7 +514,9 @@ def main(argv=None):
     ap.add_argument("--dense-steps", type=int, default=16)
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-streams", type=int, default=256, help="streams per step of the reference arm")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

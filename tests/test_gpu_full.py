@@ -1,0 +1,68 @@
+"""Parity at the full workload sizes, in the launch configuration the
+benchmark uses (automatic split choice), on sampled streams.
+
+Each case runs layer 0 of a workload through every decode step of its
+trace on the GPU (all streams), and a seeded random sample of streams
+(always including the first and the last) through the oracle.
+"""
+import random
+
+import pytest
+import torch
+
+from ar_image_gen_gb300.synth import WORKLOADS
+from tests.parity import run_parity
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from __graft_entry__ import build
+    build()
+
+
+def sample_streams(S: int, n: int, seed: int = 5) -> list[int]:
+    rnd = random.Random(seed)
+    picks = {0, S - 1} | set(rnd.sample(range(S), min(n, S)))
+    return sorted(picks)[: max(n, 2)]
+
+
+FULL = {
+    # workload key: (sampled streams, mask check interval)
+    "janus-b32": (32, 8),
+    "janus-b96": (32, 8),
+    "sweep512-s50": (24, 16),      # N_att = N_r = 512: the capped 0 % and 50 % rows (sliding window)
+    "sweep512-s75": (24, 16),
+    "sweep512-s90": (24, 16),
+    "sweep512-s95": (24, 16),
+    "sweep512-sink4-s95": (24, 16),
+    "lumina-s90-b16": (16, 32),
+    "lumina-s95-b32": (16, 32),
+    "lumina-s95-b54": (16, 32),
+    "stress-s95": (12, 64),
+}
+
+
+@pytest.mark.parametrize("key", list(FULL))
+def test_full_size_parity(key):
+    wl = WORKLOADS[key]
+    n, every = FULL[key]
+    rep = run_parity(wl, sample=sample_streams(wl.streams, n), mask_every=every, threads=8)
+    assert rep.ok, rep.summary()
+    assert rep.steps == wl.L_dec
+
+
+@pytest.mark.parametrize("key", ["janus-b96", "sweep512-s95", "stress-s95"])
+def test_full_size_dense_parity(key):
+    """The 0 % sparsity setting of the same kernel: N_r = N_att = L_dec (no
+    eviction, no skip), up to 8196 attended rows per stream."""
+    wl = WORKLOADS[key].dense()
+    if key == "stress-s95":
+        wl = wl.with_batch(16)  # one layer of dense KV at this batch is 2.1 GB
+    n = 8 if key == "stress-s95" else 16
+    rep = run_parity(wl, sample=sample_streams(wl.streams, n), mask_every=256, threads=8)
+    assert rep.ok, rep.summary()
+    assert rep.selections == 0
