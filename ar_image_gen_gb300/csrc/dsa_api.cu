@@ -4,7 +4,9 @@
 // mask, split partials), the per-step plan (phase, attended counts, split
 // choice) and the kernel launches.  No CPU fallback: every step of the decode
 // path runs in the kernels of dsa_decode.cuh.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <atomic>
 #include <climits>
@@ -12,6 +14,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <new>
 #include <string>
 
 #include "../../include/dsa.h"
@@ -66,9 +69,11 @@ constexpr uint32_t kDefaultWaitLimit = 0xffffffffu;
 
 int elem_bytes(int dtype) { return dtype == DSA_F32 ? 4 : 2; }
 
-// Stage rows and rows-per-CTA limit of the kernel instantiation.
-int stage_rows(int dtype, int D) { return 16384 / (2 * D * elem_bytes(dtype)); }
-constexpr int kChunkMax = 2048;
+// Stage rows and the rows-per-item limit of the kernel (8 KB stages, at most
+// 512 decode rows listed per work item).
+int stage_rows(int dtype, int D) { return 8192 / (2 * D * elem_bytes(dtype)); }
+constexpr int kChunkMax = 512;
+constexpr int kWarpsPerCta = DSA_WARPS;
 
 }  // namespace
 
@@ -90,6 +95,7 @@ struct dsa_ctx {
     float2 *part_ml, *part_min;
     int *ticket;
     int *status;
+    CUtensorMap ring_map;  // 2-D view of the ring: [S * R rows, 2 * D], one-row box
 };
 
 namespace {
@@ -107,20 +113,25 @@ int validate(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int
     if (N_r - sink > 65536) return fail(DSA_ERR_ARG, "N_r - sink must be <= 65536 (got %d)", N_r - sink);
     if (dtype != DSA_BF16 && dtype != DSA_F32) return fail(DSA_ERR_ARG, "dtype must be DSA_BF16 or DSA_F32 (got %d)", dtype);
     if ((long long)L_p + sink > INT_MAX / 4) return fail(DSA_ERR_ARG, "L_p too large");
+    if ((long long)heads * (N_r - sink) > INT_MAX) return fail(DSA_ERR_ARG, "heads * (N_r - sink) must fit in 31 bits");
     return DSA_OK;
 }
 
 struct Plan {
-    int phase, tin, P, a, wlen, select, sinkmode, n, nsplit, chunk;
+    int phase, tin, P, a, wlen, select, sinkmode, n, nsplit, chunk, nitems, grid;
     unsigned long long bytes;
 };
 
+// Work items per stream: one item per stream while there are at least as
+// many streams as resident warps; otherwise split streams until every warp
+// has an item, keeping at least two stages of rows per split and at most
+// kChunkMax rows per item.
 int auto_splits(const dsa_ctx *h, int n)
 {
     const int rows = stage_rows(h->dtype, h->D);
     const int need = (n + kChunkMax - 1) / kChunkMax;
-    const long long slots = (long long)h->sm_count * h->ctas_per_sm;
-    const int want = (int)((4 * slots + h->S - 1) / h->S);
+    const long long warps = (long long)h->sm_count * h->ctas_per_sm * kWarpsPerCta;
+    const int want = h->S >= warps ? 1 : (int)((warps + h->S - 1) / h->S);
     const int by_rows = n / (2 * rows) > 1 ? n / (2 * rows) : 1;
     const int ns = want < by_rows ? want : by_rows;
     return ns > need ? ns : need;
@@ -158,6 +169,10 @@ Plan make_plan(const dsa_ctx *h, int t)
     if (chunk > kChunkMax) chunk = kChunkMax;
     p.chunk = chunk;
     p.nsplit = (p.n + chunk - 1) / chunk;
+    p.nitems = p.nsplit * h->S;
+    const long long ctas = (long long)h->sm_count * h->ctas_per_sm;
+    const long long need_ctas = (p.nitems + kWarpsPerCta - 1) / kWarpsPerCta;
+    p.grid = (int)(need_ctas < ctas ? need_ctas : ctas);
     const unsigned long long De = (unsigned long long)h->D * elem_bytes(h->dtype);
     // K and V rows read (current token through k_new/v_new) + q + k_new, v_new
     // read + new entry written + out written.
@@ -205,6 +220,32 @@ void free_ctx(dsa_ctx *h)
     delete h;
 }
 
+// Tensor map over the ring seen as a 2-D array of S * R rows of 2 * D
+// elements (one K|V entry per row), box one row high and one entry wide:
+// the form the TMA tile::gather4 load needs.
+int encode_ring_map(dsa_ctx *h)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void **)&encode, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !encode) {
+            encode = nullptr;
+            return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        }
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)(2 * h->D), (cuuint64_t)h->S * h->R};
+    const cuuint64_t strides[1] = {(cuuint64_t)(2 * h->D * elem_bytes(h->dtype))};
+    const cuuint32_t box[2] = {(cuuint32_t)(2 * h->D), 1};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(&h->ring_map, h->dtype == DSA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, h->ring, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return DSA_OK;
+}
+
 template <typename T, int D>
 int occupancy()
 {
@@ -228,10 +269,10 @@ int occupancy_for(int dtype, int D)
 }
 
 template <typename T, int D>
-cudaError_t launch_decode(const dsa::DecodeParams &p, int grid, cudaStream_t st)
+cudaError_t launch_decode(const dsa::DecodeParams &p, const CUtensorMap &map, int grid, cudaStream_t st)
 {
     using C = dsa::KCfg<T, D>;
-    dsa::decode_kernel<T, D><<<grid, C::THREADS, C::SMEM, st>>>(p);
+    dsa::decode_kernel<T, D><<<grid, C::THREADS, C::SMEM, st>>>(p, map);
     return cudaGetLastError();
 }
 
@@ -321,6 +362,7 @@ int dsa_create_ex(int heads, int head_dim, int L_p, int N_r, int N_att, int sink
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->ticket, S * 4, "split tickets");
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->status, 16, "status word");
     if (rc == DSA_OK) rc = ensure_partials(h, auto_splits(h, L_p + N_att));
+    if (rc == DSA_OK) rc = encode_ring_map(h);
     if (rc != DSA_OK) {
         std::string msg = g_err;
         free_ctx(h);
@@ -389,7 +431,7 @@ int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out)
     out->select = p.select;
     out->nsplit = p.nsplit;
     out->chunk = p.chunk;
-    out->grid = p.nsplit * h->S;
+    out->grid = p.grid;
     out->algo_bytes = p.bytes;
     return DSA_OK;
 }
@@ -427,24 +469,29 @@ int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *
     p.sinkmode = pl.sinkmode;
     p.R = h->R;
     p.tin = pl.tin;
+    p.tin_mod = pl.tin >= 0 ? pl.tin % h->R : 0;
     p.wlen = pl.wlen;
     p.a = pl.a;
     p.n = pl.n;
     p.nsplit = pl.nsplit;
     p.chunk = pl.chunk;
     p.pstride = h->pstride;
+    p.nitems = pl.nitems;
+    p.noskip = (h->A == h->R) ? 1 : 0;
     p.select = pl.select;
     p.MW = h->MW;
     p.qscale = (float)(1.4426950408889634 / std::sqrt((double)h->D));
     p.wait_limit = h->wait_limit;
 
     cudaStream_t st = (cudaStream_t)stream;
-    const int grid = pl.nsplit * h->S;
+    const int grid = pl.grid;
     cudaError_t e;
     if (h->dtype == DSA_BF16)
-        e = h->D == 64 ? launch_decode<__nv_bfloat16, 64>(p, grid, st) : launch_decode<__nv_bfloat16, 128>(p, grid, st);
+        e = h->D == 64 ? launch_decode<__nv_bfloat16, 64>(p, h->ring_map, grid, st)
+                       : launch_decode<__nv_bfloat16, 128>(p, h->ring_map, grid, st);
     else
-        e = h->D == 64 ? launch_decode<float, 64>(p, grid, st) : launch_decode<float, 128>(p, grid, st);
+        e = h->D == 64 ? launch_decode<float, 64>(p, h->ring_map, grid, st)
+                       : launch_decode<float, 128>(p, h->ring_map, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     h->last_select = pl.select;
     h->t += 1;

@@ -3,22 +3,29 @@
 // Autoregressive Image Generation", section 4, Algorithm 1 and Fig. 12;
 // section 5.1 for Diagonal+sink4 and the fused-kernel description).
 //
-// One launch performs, for every stream s (a sequence-head of one layer):
-//   a2  append: k_new, v_new -> ring slot t' mod R (the slot of the entry
-//       evicted at this step) or, during the sink fill, prefix row L_p + t;
+// One launch is a persistent grid whose warps each take work items
+// (stream, split) in turn; a stream is one sequence-head of one layer.  Per
+// item, one warp performs:
+//   a2  append: the current token, read into registers, is stored to ring
+//       slot t' mod R (the slot of the entry evicted at this step) or,
+//       during the sink fill, to prefix row L_p + t;
 //   a4  index set: the attended relative offsets r in [0, min(t'+1, R)) whose
-//       skip bit is clear, compacted in shared memory with a block scan;
-//   a5  gather + logits: prompt rows (one contiguous bulk copy per stage)
-//       and attended ring rows (one bulk copy per row) staged into a
-//       4-stage shared-memory ring by a producer warp; fp32 logits q.k;
-//   a6  online softmax and P.V per consumer warp, then across warps;
-//   a7  split combine: the last CTA of a stream (atomic ticket) merges the
-//       per-split (m, l, acc) partials;
+//       skip bit is clear, listed by a warp scan over the mask words;
+//   a5  gather + logits: the prompt rows (bulk copies) and the attended ring
+//       rows (TMA tile::gather4, four rows per instruction, or contiguous
+//       bulk runs when nothing can be skipped) stream through the warp's
+//       shared-memory stages; fp32 logits q.k with 8 lanes per row;
+//   a6  online softmax and P.V, combined over the warp's row groups with
+//       shuffles;
+//   a7  split combine: the last split of a stream to finish (atomic ticket)
+//       merges the per-split (m, l, acc) partials;
 //   a8  fused argmin over the attended decode logits on selection steps; the
-//       finishing CTA sets bit r* of the stream's relative-offset skip mask.
+//       finishing warp sets bit r* of the stream's relative-offset skip mask.
 // The diagonal shift (+1 per step) costs nothing: skipped entries are kept as
 // relative offsets r = t' - position, which the shift leaves unchanged, and
-// the slot of offset r is (t' - r) mod R.
+// the slot of offset r is (t' - r) mod R.  Many independent warps per SM each
+// keep their own copies in flight, so no single warp's issue rate or latency
+// bounds the HBM stream.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -41,18 +48,29 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
-// Polls the barrier phase at most `limit` times and for at most kWaitNs.
+// Waits for the barrier phase: each poll sleeps until the phase completes
+// or kPollNs pass; gives up after `limit` polls or after kWaitNs in total.
 // limit == 0 gives up without polling (the test knob).
+constexpr uint32_t kPollNs = 20000;
+
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint32_t limit)
 {
     if (limit == 0) return false;
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kPollNs)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1; i < limit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > kWaitNs) return false;
+        if (mbar_try_wait_sleep(bar, parity, kPollNs)) return true;
     }
     return false;
+}
+
+// Waits (time-capped) for copies already issued.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_sleep(bar, parity, kPollNs))
+        if (globaltimer_ns() - t0 > kWaitNs) return;
 }
 
 struct DecodeParams {
@@ -75,80 +93,145 @@ struct DecodeParams {
     int sinkmode;         // 1: the new token goes to prefix row P
     int R;                // ring slots (N_r - sink)
     int tin;              // inner step t' = t - sink (-1 in sink mode)
+    int tin_mod;          // t' mod R: ring slot of the current token (0 in sink mode)
     int wlen;             // live window length min(t' + 1, R) (1 in sink mode)
     int a;                // attended decode rows (host count)
     int n;                // P + a
-    int nsplit;           // CTAs per stream
-    int chunk;            // rows per CTA (multiple of the stage rows)
+    int nsplit;           // work items per stream
+    int chunk;            // rows per work item (multiple of the stage rows)
+    int nitems;           // S * nsplit
     int pstride;          // partial slots per stream
     int select;           // 1: selection step (fused argmin)
+    int noskip;           // 1: N_att == N_r, no offset is ever skipped
     int MW;               // mask words per stream
-    float qscale;         // log2(e) / sqrt(D)
+    float qscale;         // log2(e) / sqrt(D), applied to q.k
     uint32_t wait_limit;
 };
 
+// Packed fp32 FMA on two lanes of a register pair: (d0, d1) += (a0, a1) * (b0, b1).
+__device__ __forceinline__ void fma_f32x2(float &d0, float &d1, float a0, float a1, float b0, float b1)
+{
+    asm("{\n\t.reg .b64 A, B, C;\n\t"
+        "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\tmov.b64 C, {%0, %1};\n\t"
+        "fma.rn.f32x2 C, A, B, C;\n\tmov.b64 {%0, %1}, C;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// 2^x on the special-function unit.
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Per element type: the query fragment a lane keeps, the q.k partial dot
+// product of one 16-byte vector, and acc += p * v for one 16-byte vector.
 template <typename T>
 struct Elem;
 
 template <>
 struct Elem<float> {
     static constexpr int VEC = 4;
-    static __device__ __forceinline__ void widen(const uint4 &v, float *f)
+    struct Q { float x[4]; };
+    static __device__ __forceinline__ Q load_q(const uint4 &v)
     {
-        f[0] = __uint_as_float(v.x);
-        f[1] = __uint_as_float(v.y);
-        f[2] = __uint_as_float(v.z);
-        f[3] = __uint_as_float(v.w);
+        return Q{{__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w)}};
+    }
+    // returns two partial sums (even / odd elements)
+    static __device__ __forceinline__ void dot(const Q &q, const uint4 &k, float &s0, float &s1)
+    {
+        fma_f32x2(s0, s1, q.x[0], q.x[1], __uint_as_float(k.x), __uint_as_float(k.y));
+        fma_f32x2(s0, s1, q.x[2], q.x[3], __uint_as_float(k.z), __uint_as_float(k.w));
+    }
+    static __device__ __forceinline__ void axpy(float p, const uint4 &v, float *acc)
+    {
+        fma_f32x2(acc[0], acc[1], p, p, __uint_as_float(v.x), __uint_as_float(v.y));
+        fma_f32x2(acc[2], acc[3], p, p, __uint_as_float(v.z), __uint_as_float(v.w));
     }
     static __device__ __forceinline__ float narrow(float x) { return x; }
+    static __device__ __forceinline__ uint4 pack(const float *a, float scale)
+    {
+        return make_uint4(__float_as_uint(a[0] * scale), __float_as_uint(a[1] * scale), __float_as_uint(a[2] * scale),
+                          __float_as_uint(a[3] * scale));
+    }
 };
 
 template <>
 struct Elem<__nv_bfloat16> {
     static constexpr int VEC = 8;
-    static __device__ __forceinline__ void widen(const uint4 &v, float *f)
+    struct Q { uint4 raw; };  // q stays packed bf16: the dot uses mixed-precision FMAs
+    static __device__ __forceinline__ Q load_q(const uint4 &v) { return Q{v}; }
+    // bf16 x bf16 products accumulate in fp32 (exact products, fp32 sums).
+    static __device__ __forceinline__ void dot(const Q &q, const uint4 &k, float &s0, float &s1)
     {
-        f[0] = __uint_as_float(v.x << 16);
-        f[1] = __uint_as_float(v.x & 0xffff0000u);
-        f[2] = __uint_as_float(v.y << 16);
-        f[3] = __uint_as_float(v.y & 0xffff0000u);
-        f[4] = __uint_as_float(v.z << 16);
-        f[5] = __uint_as_float(v.z & 0xffff0000u);
-        f[6] = __uint_as_float(v.w << 16);
-        f[7] = __uint_as_float(v.w & 0xffff0000u);
+        asm("{\n\t.reg .b16 k0, k1, k2, k3, k4, k5, k6, k7, q0, q1, q2, q3, q4, q5, q6, q7;\n\t"
+            "mov.b32 {k0, k1}, %2;\n\tmov.b32 {k2, k3}, %3;\n\tmov.b32 {k4, k5}, %4;\n\tmov.b32 {k6, k7}, %5;\n\t"
+            "mov.b32 {q0, q1}, %6;\n\tmov.b32 {q2, q3}, %7;\n\tmov.b32 {q4, q5}, %8;\n\tmov.b32 {q6, q7}, %9;\n\t"
+            "fma.rn.f32.bf16 %0, k0, q0, %0;\n\tfma.rn.f32.bf16 %1, k1, q1, %1;\n\t"
+            "fma.rn.f32.bf16 %0, k2, q2, %0;\n\tfma.rn.f32.bf16 %1, k3, q3, %1;\n\t"
+            "fma.rn.f32.bf16 %0, k4, q4, %0;\n\tfma.rn.f32.bf16 %1, k5, q5, %1;\n\t"
+            "fma.rn.f32.bf16 %0, k6, q6, %0;\n\tfma.rn.f32.bf16 %1, k7, q7, %1;\n\t}"
+            : "+f"(s0), "+f"(s1)
+            : "r"(k.x), "r"(k.y), "r"(k.z), "r"(k.w), "r"(q.raw.x), "r"(q.raw.y), "r"(q.raw.z), "r"(q.raw.w));
+    }
+    static __device__ __forceinline__ void axpy(float p, const uint4 &v, float *acc)
+    {
+        fma_f32x2(acc[0], acc[1], p, p, __uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+        fma_f32x2(acc[2], acc[3], p, p, __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+        fma_f32x2(acc[4], acc[5], p, p, __uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u));
+        fma_f32x2(acc[6], acc[7], p, p, __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
     }
     static __device__ __forceinline__ __nv_bfloat16 narrow(float x) { return __float2bfloat16_rn(x); }
+    static __device__ __forceinline__ uint4 pack(const float *a, float scale)
+    {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a[2 * i] * scale, a[2 * i + 1] * scale);
+            w[i] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
 };
+
+// Pipeline shape (compile-time): independent warps per CTA and 8 KB
+// shared-memory stages per warp.
+#ifndef DSA_WARPS
+#define DSA_WARPS 4
+#endif
+#ifndef DSA_NBUF
+#define DSA_NBUF 2
+#endif
 
 template <typename T, int D>
 struct KCfg {
     static constexpr int E = sizeof(T);
     static constexpr int VEC = Elem<T>::VEC;   // elements per 16-byte vector
-    static constexpr int LPR = D / VEC;        // lanes per row
+    static constexpr int LPR = D / (2 * VEC);  // lanes per row: each lane reads 2 vectors of K and of V
     static constexpr int RPW = 32 / LPR;       // rows per warp instruction
     static constexpr int KROW = D * E;         // bytes of a K (or V) row
     static constexpr int ROW = 2 * KROW;       // bytes of a K|V entry
-    static constexpr int NCW = 4;              // consumer warps
-    static constexpr int THREADS = 32 * (NCW + 1);
-    static constexpr int STAGE_BYTES = 16384;
-    static constexpr int ROWS = STAGE_BYTES / ROW;  // entries per stage
-    static constexpr int RPC = ROWS / NCW;          // entries per consumer warp per stage
-    static constexpr int NIT = RPC / RPW;
-    static constexpr int NSTAGE = 4;
-    static constexpr int CHUNK_MAX = 2048;          // decode entries listed per CTA
-    static constexpr int OFF_BAR = NSTAGE * STAGE_BYTES;
-    static constexpr int OFF_LIST = OFF_BAR + 2 * NSTAGE * 8;
-    static constexpr int OFF_CNT = OFF_LIST + CHUNK_MAX * 2;
-    static constexpr int OFF_COMB = OFF_CNT + 32 * 4;
-    static constexpr int OFF_CML = OFF_COMB + NCW * D * 4;
-    static constexpr int OFF_FLAG = OFF_CML + NCW * 16;
-    static constexpr int SMEM = OFF_FLAG + 16;
-    static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row must span a power-of-two lane group");
-    static_assert(RPC % RPW == 0 && NIT >= 1, "stage rows must split evenly over consumer warps");
-    static_assert(ROW % 16 == 0 && OFF_COMB % 16 == 0, "alignment");
+    static constexpr int WARPS = DSA_WARPS;
+    static constexpr int THREADS = 32 * WARPS;
+    static constexpr int STAGE_BYTES = 8192;
+    static constexpr int SROWS = STAGE_BYTES / ROW;  // entries per stage
+    static constexpr int NIT = SROWS / RPW;          // warp instructions per stage
+    static constexpr int NBUF = DSA_NBUF;            // stages per warp
+    static constexpr int CHUNK_MAX = 512;            // decode ranks per work item
+    static constexpr int MAXW = 8;                   // mask words per lane kept in registers
+    static constexpr int OFF_BAR = NBUF * STAGE_BYTES;
+    static constexpr int OFF_LIST = OFF_BAR + NBUF * 8;
+    static constexpr int WARP_SMEM = (OFF_LIST + CHUNK_MAX * 2 + 127) / 128 * 128;
+    static constexpr int SMEM = WARPS * WARP_SMEM;
+    static_assert(LPR >= 2 && LPR <= 16 && 32 % LPR == 0, "row must span a power-of-two lane group");
+    static_assert(SROWS % RPW == 0 && NIT >= 1, "stage rows must fill whole warp instructions");
+    static_assert(ROW % 128 == 0 || ROW == 256, "gather destinations must stay 128-byte aligned");
 };
 
-// Bits of mask word w that are attended window offsets (clear and < wlen).
+// Bits of mask word w that are attended window offsets (clear and < wlen);
+// w must satisfy 32 * w < wlen.
 __device__ __forceinline__ uint32_t attended_bits(uint32_t word, int w, int wlen)
 {
     const int base = w * 32;
@@ -156,198 +239,263 @@ __device__ __forceinline__ uint32_t attended_bits(uint32_t word, int w, int wlen
     return ~word & valid;
 }
 
+__device__ __forceinline__ bool better(float v, int r, float bv, int br)
+{
+    return v < bv || (v == bv && r > br);  // lower logit; on a tie the older entry (larger r)
+}
+
+// Warp-per-item decode kernel: a persistent grid whose warps take work items
+// (stream, split) in turn.  A warp lists the item's attended offsets (warp
+// scan over the stream's mask words, prefetched one item ahead), streams the
+// prompt rows (bulk copies) and the attended ring rows (TMA tile::gather4
+// through `tmap`, or contiguous bulk runs when nothing can be skipped)
+// through its own NBUF shared-memory stages, reads q and the current token
+// straight into registers, and ends with a warp-shuffle combine.
 template <typename T, int D>
-__global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const DecodeParams p,
+                                                                      const __grid_constant__ CUtensorMap tmap)
 {
     using C = KCfg<T, D>;
     using EL = Elem<T>;
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint16_t *list = reinterpret_cast<uint16_t *>(smem + C::OFF_LIST);
-    int *wsum = reinterpret_cast<int *>(smem + C::OFF_CNT);
-    float *comb = reinterpret_cast<float *>(smem + C::OFF_COMB);
-    float4 *cml = reinterpret_cast<float4 *>(smem + C::OFF_CML);
-    volatile int *flag = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const int s = blockIdx.x / p.nsplit;
-    const int c = blockIdx.x - s * p.nsplit;
-    const int lo = c * p.chunk;
-    const int hi = min(lo + p.chunk, p.n);
-    const int nst = (hi - lo + C::ROWS - 1) / C::ROWS;
-    const int klo = max(lo, p.P) - p.P;  // decode ranks of this CTA: [klo, khi)
-    const int khi = max(hi, p.P) - p.P;
-
-    if (tid == 0) {
-        for (int b = 0; b < C::NSTAGE; ++b) {
-            mbar_init(smem_u32(&bars[b]), 1);
-            mbar_init(smem_u32(&bars[C::NSTAGE + b]), C::NCW);
-        }
-        flag[0] = 0;
-        flag[1] = 0;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    unsigned char *ws = smem + warp * C::WARP_SMEM;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ws + C::OFF_BAR);
+    uint16_t *list = reinterpret_cast<uint16_t *>(ws + C::OFF_LIST);
+    if (lane == 0) {
+        for (int b = 0; b < C::NBUF; ++b) mbar_init(smem_u32(&bars[b]), 1);
         fence_barrier_init();
     }
+    __syncwarp();
+    const uint32_t bar0 = smem_u32(&bars[0]);
+    const uint32_t buf0 = smem_u32(ws);
 
-    // a4: rank -> relative offset of the attended decode entries of this CTA.
-    const uint32_t *mrow = p.mask + (size_t)s * p.MW;
-    const int nwords = (p.wlen + 31) >> 5;
-    const int wpt = (nwords + C::THREADS - 1) / C::THREADS;
-    const int w0 = min(tid * wpt, nwords);
-    const int w1 = min(w0 + wpt, nwords);
-    int mine = 0;
-    for (int w = w0; w < w1; ++w) mine += __popc(attended_bits(__ldg(mrow + w), w, p.wlen));
-    int incl = mine;
+    const int g = lane / C::LPR;   // row group of the lane within a warp instruction
+    const int cl = lane % C::LPR;  // the lane handles vectors cl and cl + LPR of every row
+    const uint64_t pol = policy_evict_first();
+    const int nwords = p.noskip ? 0 : (p.wlen + 31) >> 5;
+    const int wpl = (nwords + 31) >> 5;  // contiguous mask words per lane
+    const bool inreg = wpl <= C::MAXW;
+    const int GW = gridDim.x * C::WARPS;
+    const int first_item = blockIdx.x * C::WARPS + warp;
+
+    uint32_t words[C::MAXW];
+    auto load_words = [&](int item) {
+        const uint32_t *row = p.mask + (size_t)(item / p.nsplit) * p.MW;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    int rank = incl - mine;
-    int total = 0;
-    for (int wi = 0; wi < C::NCW + 1; ++wi) {
-        const int x = wsum[wi];
-        rank += (wi < warp) ? x : 0;
-        total += x;
-    }
-    if (total != p.a) {
-        // The skip mask disagrees with the host's count: record it and keep
-        // every listed offset in range (missing entries read as offset 0).
-        if (tid == 0) atomicOr(p.status, ST_CHECK);
-        for (int i = tid; i < khi - klo; i += C::THREADS) list[i] = 0;
-        __syncthreads();
-    }
-    if (rank < khi) {
-        for (int w = w0; w < w1 && rank < khi; ++w) {
-            uint32_t bits = attended_bits(__ldg(mrow + w), w, p.wlen);
-            const int cnt = __popc(bits);
-            if (rank + cnt <= klo) {
-                rank += cnt;
-                continue;
-            }
-            while (bits) {
-                const int b = __ffs(bits) - 1;
-                if (rank >= klo && rank < khi) list[rank - klo] = (uint16_t)(w * 32 + b);
-                ++rank;
-                bits &= bits - 1;
-            }
+        for (int i = 0; i < C::MAXW; ++i) {
+            const int w = lane * wpl + i;
+            words[i] = (i < wpl && w < nwords) ? __ldcg(row + w) : 0u;
         }
+    };
+    uint4 qn0 = make_uint4(0, 0, 0, 0), qn1 = qn0;  // q vectors of the next item
+    auto load_q = [&](int item) {
+        const uint4 *qr = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + (size_t)(item / p.nsplit) * D);
+        qn0 = __ldg(qr + cl);
+        qn1 = __ldg(qr + cl + C::LPR);
+    };
+    if (first_item < p.nitems) {
+        if (inreg && nwords > 0) load_words(first_item);
+        load_q(first_item);
     }
 
-    // a2: append the new entry (split 0 of each stream).
-    if (c == 0 && warp < C::NCW) {
-        constexpr int NV = C::KROW / 16;
-        T *dst = p.sinkmode ? reinterpret_cast<T *>(p.prefix) + ((size_t)s * p.Lcap + p.P) * 2 * D
-                            : reinterpret_cast<T *>(p.ring) + ((size_t)s * p.R + (p.tin % p.R)) * 2 * D;
-        const uint4 *ks = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.knew) + (size_t)s * D);
-        const uint4 *vs = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.vnew) + (size_t)s * D);
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-        for (int i = tid; i < 2 * NV; i += 32 * C::NCW) d4[i] = (i < NV) ? __ldg(ks + i) : __ldg(vs + i - NV);
-    }
-    __syncthreads();
+    bool aborted = false;
+    int issued = 0, consumed = 0;  // stages issued / consumed by this warp over all its items
+    for (int item = first_item; item < p.nitems && !aborted; item += GW) {
+        const int s = item / p.nsplit;
+        const int c = item - s * p.nsplit;
+        const int lo = c * p.chunk;
+        const int hi = min(lo + p.chunk, p.n);
+        const int klo = max(lo, p.P) - p.P;  // attended decode ranks of the item: [klo, khi)
+        const int khi = max(hi, p.P) - p.P;
+        const uint32_t *mrow = p.mask + (size_t)s * p.MW;
 
-    const uint32_t full0 = smem_u32(&bars[0]);
-    const uint32_t empty0 = smem_u32(&bars[C::NSTAGE]);
-    int lastj[C::NSTAGE];  // producer: last stage issued into each buffer
+        // ---- a4: ranks [klo, khi) -> relative offsets (list)
+        bool self_skip = false;
+        if (nwords > 0) {
+            int mine = 0;
+            if (inreg) {
 #pragma unroll
-    for (int b = 0; b < C::NSTAGE; ++b) lastj[b] = -1;
-
-    if (warp == C::NCW) {
-        // ---------------- producer warp: a5 gather via the bulk-copy engine
-        const unsigned char *pre =
-            reinterpret_cast<const unsigned char *>(p.prefix) + (size_t)s * p.Lcap * C::ROW;
-        const unsigned char *rng = reinterpret_cast<const unsigned char *>(p.ring) + (size_t)s * p.R * C::ROW;
-        const unsigned char *kn = reinterpret_cast<const unsigned char *>(p.knew) + (size_t)s * C::KROW;
-        const unsigned char *vn = reinterpret_cast<const unsigned char *>(p.vnew) + (size_t)s * C::KROW;
-        const uint64_t pol = policy_evict_first();
-        for (int j = 0; j < nst; ++j) {
-            const int b = j % C::NSTAGE;
-            if (j >= C::NSTAGE) {
-                bool ok = true;
-                if (lane == 0) ok = wait_phase(empty0 + 8 * b, ((j / C::NSTAGE) - 1) & 1, p.wait_limit);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) {
-                    if (lane == 0) {
-                        flag[0] = 1;
-                        atomicOr(p.status, ST_TIMEOUT);
-                    }
-                    break;
+                for (int i = 0; i < C::MAXW; ++i) {
+                    const int w = lane * wpl + i;
+                    if (i < wpl && w < nwords) mine += __popc(attended_bits(words[i], w, p.wlen));
                 }
-                if (flag[0]) break;
+            } else {
+                for (int i = 0; i < wpl; ++i) {
+                    const int w = lane * wpl + i;
+                    if (w < nwords) mine += __popc(attended_bits(__ldcg(mrow + w), w, p.wlen));
+                }
             }
-            const int v0 = lo + j * C::ROWS;
-            const int v1 = min(v0 + C::ROWS, hi);
-            const uint32_t dst = smem_u32(smem + b * C::STAGE_BYTES);
-            const uint32_t fb = full0 + 8 * b;
-            if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(v1 - v0) * C::ROW);
-            __syncwarp();
-            const int pe = min(v1, p.P);
-            if (lane == 0 && pe > v0) bulk_g2s_hint(dst, pre + (size_t)v0 * C::ROW, (pe - v0) * C::ROW, fb, pol);
-            for (int i = max(v0, p.P) + lane; i < v1; i += 32) {
-                const int r = list[i - p.P - klo];
-                const uint32_t sd = dst + (i - v0) * C::ROW;
-                if (r == 0) {
-                    bulk_g2s(sd, kn, C::KROW, fb);
-                    bulk_g2s(sd + C::KROW, vn, C::KROW, fb);
+            int incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            if (total != p.a) {
+                // The skip mask disagrees with the host's count: record it and
+                // keep every listed offset in range.
+                if (lane == 0) atomicOr(p.status, ST_CHECK);
+                for (int i = lane; i < khi - klo; i += 32) list[i] = 0;
+                __syncwarp();
+            }
+            int rank = incl - mine;
+            for (int i = 0; i < wpl && rank < khi; ++i) {
+                const int w = lane * wpl + i;
+                if (w >= nwords) break;
+                uint32_t word;
+                if (inreg) {
+                    word = 0;
+#pragma unroll
+                    for (int k = 0; k < C::MAXW; ++k) word = (k == i) ? words[k] : word;
                 } else {
-                    const int slot = (p.tin - r) % p.R;
-                    bulk_g2s_hint(sd, rng + (size_t)slot * C::ROW, C::ROW, fb, pol);
+                    word = __ldcg(mrow + w);
+                }
+                uint32_t bits = attended_bits(word, w, p.wlen);
+                const int cnt = __popc(bits);
+                if (rank + cnt <= klo) {
+                    rank += cnt;
+                    continue;
+                }
+                while (bits) {
+                    const int bt = __ffs(bits) - 1;
+                    if (rank >= klo && rank < khi) list[rank - klo] = (uint16_t)(w * 32 + bt);
+                    ++rank;
+                    bits &= bits - 1;
                 }
             }
-            lastj[b] = j;
+            const uint32_t w0 = inreg ? words[0] : __ldcg(mrow);
+            self_skip = (__shfl_sync(0xffffffffu, w0, 0) & 1u) != 0;
         }
         __syncwarp();
-    } else {
-        // ---------------- consumer warps: a5 logits, a6 softmax.V, a8 argmin
-        const int g = lane / C::LPR;
-        const int cl = lane % C::LPR;
-        float qf[C::VEC];
-        {
-            const uint4 qv = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + (size_t)s * D) + cl);
-            EL::widen(qv, qf);
-#pragma unroll
-            for (int e = 0; e < C::VEC; ++e) qf[e] *= p.qscale;
+        const typename EL::Q q0 = EL::load_q(qn0), q1 = EL::load_q(qn1);
+        if (item + GW < p.nitems) {  // prefetch the next item's mask words and q
+            if (inreg && nwords > 0) load_words(item + GW);
+            load_q(item + GW);
         }
-        float acc[C::VEC];
+
+        // rank 0 is the current token (offset 0) unless it is itself skipped
+        const bool has_cur = (klo == 0 && khi > 0 && !self_skip);
+        T *const cur_dst = p.sinkmode ? reinterpret_cast<T *>(p.prefix) + ((size_t)s * p.Lcap + p.P) * 2 * D
+                                      : reinterpret_cast<T *>(p.ring) + ((size_t)s * p.R + p.tin_mod) * 2 * D;
+        uint4 kc0, kc1, vc0, vc1;
+        if (has_cur) {  // the current token goes straight to registers
+            const uint4 *kr = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.knew) + (size_t)s * D);
+            const uint4 *vr = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.vnew) + (size_t)s * D);
+            kc0 = __ldg(kr + cl);
+            kc1 = __ldg(kr + cl + C::LPR);
+            vc0 = __ldg(vr + cl);
+            vc1 = __ldg(vr + cl + C::LPR);
+        } else if (self_skip && c == 0) {
+            // a2 for a token that is not attended: it is in no stage; copy it.
+            constexpr int NV = C::KROW / 16;
+            uint4 *dst = reinterpret_cast<uint4 *>(cur_dst);
+            const uint4 *ks = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.knew) + (size_t)s * D);
+            const uint4 *vs = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.vnew) + (size_t)s * D);
+            for (int i = lane; i < 2 * NV; i += 32) dst[i] = (i < NV) ? ks[i] : vs[i - NV];
+        }
+
+        // rows staged through shared memory: prompt rows [lo, lo + npre), then
+        // the attended ring entries of ranks [kr0, khi)
+        const int npre = max(min(hi, p.P) - lo, 0);
+        const int kr0 = has_cur ? klo + 1 : klo;
+        const int nrows = npre + max(khi - kr0, 0);
+        const int nst = (nrows + C::SROWS - 1) / C::SROWS;
+        const unsigned char *pre = reinterpret_cast<const unsigned char *>(p.prefix) + ((size_t)s * p.Lcap + lo) * C::ROW;
+        const unsigned char *rng = reinterpret_cast<const unsigned char *>(p.ring) + (size_t)s * p.R * C::ROW;
+
+        auto issue = [&](int j) {  // stage j of the item into buffer issued % NBUF
+            const int b = issued % C::NBUF;
+            const uint32_t fb = bar0 + 8 * b;
+            const uint32_t dst = buf0 + b * C::STAGE_BYTES;
+            const int u0 = j * C::SROWS;
+            const int u1 = min(u0 + C::SROWS, nrows);
+            if (lane == 0) {
+                fence_proxy_async_smem();  // this warp's reads of the buffer precede the new fill
+                mbar_arrive_expect_tx(fb, (uint32_t)(u1 - u0) * C::ROW);
+                const int pb = min(u1, npre);
+                if (pb > u0) bulk_g2s_hint(dst, pre + (size_t)u0 * C::ROW, (pb - u0) * C::ROW, fb, pol);
+            }
+            const int ua = max(u0, npre);
+            const int nr = u1 - ua;  // ring entries of the stage
+            if (nr > 0) {
+                const int k0 = kr0 + (ua - npre);
+                const uint32_t rd = dst + (ua - u0) * C::ROW;
+                if (p.noskip) {
+                    // offset r = rank: descending slots, at most two contiguous runs
+                    if (lane == 0) {
+                        const int kA = min(k0 + nr, p.tin_mod + 1);
+                        const int nA = max(kA - k0, 0);
+                        if (nA > 0) bulk_g2s_hint(rd, rng + (size_t)(p.tin_mod - (kA - 1)) * C::ROW, nA * C::ROW, fb, pol);
+                        if (nr > nA)
+                            bulk_g2s_hint(rd + nA * C::ROW, rng + (size_t)(p.tin_mod - (k0 + nr - 1) + p.R) * C::ROW,
+                                          (nr - nA) * C::ROW, fb, pol);
+                    }
+                } else {
+                    const int ybase = s * p.R;
+                    const int ngrp = nr >> 2;
+                    for (int g4 = lane; g4 < ngrp; g4 += 32) {
+                        const int k = k0 + 4 * g4 - klo;
+                        int y[4];
 #pragma unroll
-        for (int e = 0; e < C::VEC; ++e) acc[e] = 0.f;
-        float m = -INFINITY, l = 0.f;
-        float minv = INFINITY;
-        int minr = -1;
-        for (int j = 0; j < nst; ++j) {
-            const int b = j % C::NSTAGE;
-            const bool ok = wait_phase(full0 + 8 * b, (j / C::NSTAGE) & 1, p.wait_limit);
-            if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0) {
-                    flag[0] = 1;
-                    atomicOr(p.status, ST_TIMEOUT);
+                        for (int m = 0; m < 4; ++m) {
+                            const int sl = p.tin_mod - (int)list[k + m];
+                            y[m] = ybase + (sl < 0 ? sl + p.R : sl);
+                        }
+                        tma_gather4(rd + 4 * g4 * C::ROW, &tmap, 0, y[0], y[1], y[2], y[3], fb);
+                    }
+                    const int tail = nr - 4 * ngrp;
+                    if (lane < tail) {
+                        int sl = p.tin_mod - (int)list[k0 + 4 * ngrp + lane - klo];
+                        sl = sl < 0 ? sl + p.R : sl;
+                        bulk_g2s_hint(rd + (4 * ngrp + lane) * C::ROW, rng + (size_t)sl * C::ROW, C::ROW, fb, pol);
+                    }
                 }
+            }
+            ++issued;
+        };
+
+        float acc[2 * C::VEC];
+#pragma unroll
+        for (int e = 0; e < 2 * C::VEC; ++e) acc[e] = 0.f;
+        float m = -INFINITY, l = 0.f, minv = INFINITY;
+        int minr = -1;
+
+        for (int j = 0; j < min(C::NBUF, nst); ++j) issue(j);
+        for (int j = 0; j < nst; ++j) {
+            const int b = consumed % C::NBUF;
+            const bool ok = wait_phase(bar0 + 8 * b, (consumed / C::NBUF) & 1, p.wait_limit);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) atomicOr(p.status, ST_TIMEOUT);
+                aborted = true;
                 break;
             }
-            const int v0 = lo + j * C::ROWS;
-            const int nr = min(C::ROWS, hi - v0);
-            const unsigned char *st = smem + b * C::STAGE_BYTES;
+            ++consumed;
+            const unsigned char *st = ws + b * C::STAGE_BYTES;
+            const int u0 = j * C::SROWS;
+            const int nv = min(C::SROWS, nrows - u0);  // valid rows of the stage
             float sc[C::NIT];
 #pragma unroll
             for (int it = 0; it < C::NIT; ++it) {
-                const int row = warp * C::RPC + it * C::RPW + g;
-                const bool valid = row < nr;
-                float x = 0.f;
+                const int row = it * C::RPW + g;
+                const bool valid = row < nv;
+                float s0 = 0.f, s1 = 0.f;
                 if (valid) {
-                    float kf[C::VEC];
-                    EL::widen(*reinterpret_cast<const uint4 *>(st + row * C::ROW + cl * 16), kf);
-#pragma unroll
-                    for (int e = 0; e < C::VEC; ++e) x = fmaf(qf[e], kf[e], x);
+                    const uint4 *kr = reinterpret_cast<const uint4 *>(st + row * C::ROW);
+                    EL::dot(q0, kr[cl], s0, s1);
+                    EL::dot(q1, kr[cl + C::LPR], s0, s1);
                 }
+                float x = s0 + s1;
 #pragma unroll
                 for (int o = C::LPR / 2; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                x *= p.qscale;
                 sc[it] = valid ? x : -INFINITY;
-                if (p.select && valid && v0 + row >= p.P) {
-                    const int r = list[v0 + row - p.P - klo];
-                    if (x < minv || (x == minv && r > minr)) {
+                if (p.select && valid && u0 + row >= npre) {
+                    const int k = kr0 + (u0 + row - npre);
+                    const int r = list[k - klo];
+                    if (better(x, r, minv, minr)) {
                         minv = x;
                         minr = r;
                     }
@@ -358,137 +506,157 @@ __global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const Decod
             for (int it = 1; it < C::NIT; ++it) mx = fmaxf(mx, sc[it]);
 #pragma unroll
             for (int o = C::LPR; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float mn = fmaxf(m, mx);
-            if (mn != -INFINITY) {
-                const float alpha = exp2f(m - mn);
+            if (mx > m) {  // warp-uniform; rescale only when the running max grows
+                const float alpha = ex2(m - mx);
                 l *= alpha;
 #pragma unroll
-                for (int e = 0; e < C::VEC; ++e) acc[e] *= alpha;
+                for (int e = 0; e < 2 * C::VEC; ++e) acc[e] *= alpha;
+                m = mx;
+            }
 #pragma unroll
-                for (int it = 0; it < C::NIT; ++it) {
-                    const int row = warp * C::RPC + it * C::RPW + g;
-                    if (row < nr) {
-                        const float pj = exp2f(sc[it] - mn);
-                        l += pj;
-                        float vf[C::VEC];
-                        EL::widen(*reinterpret_cast<const uint4 *>(st + row * C::ROW + C::KROW + cl * 16), vf);
-#pragma unroll
-                        for (int e = 0; e < C::VEC; ++e) acc[e] = fmaf(pj, vf[e], acc[e]);
-                    }
+            for (int it = 0; it < C::NIT; ++it) {
+                const int row = it * C::RPW + g;
+                if (row < nv) {
+                    const float pj = ex2(sc[it] - m);
+                    l += pj;
+                    const uint4 *vr = reinterpret_cast<const uint4 *>(st + row * C::ROW + C::KROW);
+                    EL::axpy(pj, vr[cl], acc);
+                    EL::axpy(pj, vr[cl + C::LPR], acc + C::VEC);
                 }
-                m = mn;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * b);
+            if (j + C::NBUF < nst) issue(j + C::NBUF);
         }
-        // merge the row groups of the warp (m is warp-uniform)
+        if (aborted) break;
+
+        // ---- the current token (a2 append, logit, softmax.V), from registers
+        if (has_cur) {
+            float s0 = 0.f, s1 = 0.f;
+            EL::dot(q0, kc0, s0, s1);
+            EL::dot(q1, kc1, s0, s1);
+            float x = s0 + s1;
+#pragma unroll
+            for (int o = C::LPR / 2; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            x *= p.qscale;  // identical in every row group
+            if (p.select && better(x, 0, minv, minr)) {
+                minv = x;
+                minr = 0;
+            }
+            if (x > m) {
+                const float alpha = ex2(m - x);
+                l *= alpha;
+#pragma unroll
+                for (int e = 0; e < 2 * C::VEC; ++e) acc[e] *= alpha;
+                m = x;
+            }
+            if (g == 0) {
+                const float pj = ex2(x - m);
+                l += pj;
+                EL::axpy(pj, vc0, acc);
+                EL::axpy(pj, vc1, acc + C::VEC);
+                uint4 *dst = reinterpret_cast<uint4 *>(cur_dst);
+                dst[cl] = kc0;
+                dst[cl + C::LPR] = kc1;
+                dst[2 * C::LPR + cl] = vc0;
+                dst[3 * C::LPR + cl] = vc1;
+            }
+        }
+
+        // ---- a6: combine the row groups of the warp (shuffles)
 #pragma unroll
         for (int o = C::LPR; o < 32; o <<= 1) {
             l += __shfl_xor_sync(0xffffffffu, l, o);
 #pragma unroll
-            for (int e = 0; e < C::VEC; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+            for (int e = 0; e < 2 * C::VEC; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
             const float ov = __shfl_xor_sync(0xffffffffu, minv, o);
             const int orr = __shfl_xor_sync(0xffffffffu, minr, o);
-            if (ov < minv || (ov == minv && orr > minr)) {
+            if (better(ov, orr, minv, minr)) {
                 minv = ov;
                 minr = orr;
             }
         }
-        if (lane < C::LPR) {
-#pragma unroll
-            for (int e = 0; e < C::VEC; ++e) comb[warp * D + cl * C::VEC + e] = acc[e];
-        }
-        if (lane == 0) cml[warp] = make_float4(m, l, minv, __int_as_float(minr));
-    }
-    __syncthreads();
-    // If any warp gave up, every copy still in flight must land (bounded
-    // wait) before the CTA's shared memory is released.  The flag is read
-    // after the barrier, so a late abort by a consumer is seen here.
-    if (flag[0]) {
-        if (warp == C::NCW && lane == 0) {
-#pragma unroll
-            for (int b = 0; b < C::NSTAGE; ++b)
-                if (lastj[b] >= 0) wait_phase(full0 + 8 * b, (lastj[b] / C::NSTAGE) & 1, 0xffffffffu);
-        }
-        __syncthreads();
-    }
-
-    // a6/a7: merge the consumer warps of this CTA.
-    float2 best = make_float2(INFINITY, __int_as_float(-1));
-    if (tid == 0 && p.select) {
-        for (int w = 0; w < C::NCW; ++w) {
-            const float4 x = cml[w];
-            const int rx = __float_as_int(x.w), rb = __float_as_int(best.y);
-            if (x.z < best.x || (x.z == best.x && rx > rb)) best = make_float2(x.z, x.w);
-        }
-    }
-    float O = 0.f, M = -INFINITY, L = 0.f;
-    if (tid < D) {
-        for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, cml[w].x);
-        for (int w = 0; w < C::NCW; ++w) {
-            const float4 x = cml[w];
-            if (x.x != -INFINITY) {
-                const float f = exp2f(x.x - M);
-                O = fmaf(comb[w * D + tid], f, O);
-                L = fmaf(x.y, f, L);
+        if (p.nsplit == 1) {
+            if (g == 0) {
+                const float inv = 1.f / l;
+                uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + (size_t)s * D);
+                o[cl] = EL::pack(acc, inv);
+                o[cl + C::LPR] = EL::pack(acc + C::VEC, inv);
             }
-        }
-    }
-    const size_t slot = (size_t)s * p.pstride + c;
-    if (p.nsplit == 1) {
-        if (tid < D) reinterpret_cast<T *>(p.out)[(size_t)s * D + tid] = EL::narrow(O / L);
-        if (tid == 0 && p.select && !flag[0] && __float_as_int(best.y) >= 0) {
-            const int r = __float_as_int(best.y);
-            p.last_sel[s] = r;
-            p.mask[(size_t)s * p.MW + (r >> 5)] |= 1u << (r & 31);
-        }
-        return;
-    }
-    if (tid < D) p.part_acc[slot * D + tid] = O;
-    if (tid == 0) {
-        p.part_ml[slot] = make_float2(M, L);
-        p.part_min[slot] = best;
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) flag[1] = (atomicAdd(p.ticket + s, 1) == p.nsplit - 1);
-    __syncthreads();
-    if (!flag[1]) return;
-    __threadfence();
-    const size_t base = (size_t)s * p.pstride;
-    if (tid < D) {
-        float Mx = -INFINITY;
-        for (int i = 0; i < p.nsplit; ++i) Mx = fmaxf(Mx, __ldcg(&p.part_ml[base + i].x));
-        float Ox = 0.f, Lx = 0.f;
-        for (int i = 0; i < p.nsplit; ++i) {
-            const float2 ml = __ldcg(&p.part_ml[base + i]);
-            if (ml.x != -INFINITY) {
-                const float f = exp2f(ml.x - Mx);
-                Ox = fmaf(__ldcg(&p.part_acc[(base + i) * D + tid]), f, Ox);
-                Lx = fmaf(ml.y, f, Lx);
+            if (lane == 0 && p.select && minr >= 0) {
+                p.last_sel[s] = minr;
+                p.mask[(size_t)s * p.MW + (minr >> 5)] |= 1u << (minr & 31);
             }
-        }
-        reinterpret_cast<T *>(p.out)[(size_t)s * D + tid] = EL::narrow(Ox / Lx);
-    }
-    if (tid == 0) {
-        p.ticket[s] = 0;
-        if (p.select && *reinterpret_cast<volatile int *>(p.status) == 0) {
-            float bv = INFINITY;
-            int br = -1;
-            for (int i = 0; i < p.nsplit; ++i) {
-                const float2 x = __ldcg(&p.part_min[base + i]);
-                const int rx = __float_as_int(x.y);
-                if (x.x < bv || (x.x == bv && rx > br)) {
-                    bv = x.x;
-                    br = rx;
+        } else {
+            // ---- a7: partial (m, l, acc) of this split; the last split of the
+            // stream to finish merges them
+            const size_t slot = (size_t)s * p.pstride + c;
+            if (g == 0) {
+                float4 *pa = reinterpret_cast<float4 *>(p.part_acc + slot * D);
+#pragma unroll
+                for (int e = 0; e < C::VEC / 4; ++e) {
+                    pa[cl * (C::VEC / 4) + e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+                    pa[(cl + C::LPR) * (C::VEC / 4) + e] =
+                        make_float4(acc[C::VEC + 4 * e], acc[C::VEC + 4 * e + 1], acc[C::VEC + 4 * e + 2], acc[C::VEC + 4 * e + 3]);
                 }
             }
-            if (br >= 0) {
-                p.last_sel[s] = br;
-                p.mask[(size_t)s * p.MW + (br >> 5)] |= 1u << (br & 31);
+            if (lane == 0) {
+                p.part_ml[slot] = make_float2(m, l);
+                p.part_min[slot] = make_float2(minv, __int_as_float(minr));
+            }
+            __threadfence();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) last = (atomicAdd(p.ticket + s, 1) == p.nsplit - 1);
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence();
+                const size_t base = (size_t)s * p.pstride;
+                float Mx = -INFINITY;
+                for (int i = 0; i < p.nsplit; ++i) Mx = fmaxf(Mx, __ldcg(&p.part_ml[base + i].x));
+                constexpr int DPL = D / 32;  // output elements per lane
+                float O[DPL];
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) O[e] = 0.f;
+                float Lx = 0.f;
+                for (int i = 0; i < p.nsplit; ++i) {
+                    const float2 ml = __ldcg(&p.part_ml[base + i]);
+                    if (ml.x != -INFINITY) {
+                        const float f = ex2(ml.x - Mx);
+                        Lx = fmaf(ml.y, f, Lx);
+#pragma unroll
+                        for (int e = 0; e < DPL; ++e) O[e] = fmaf(__ldcg(&p.part_acc[(base + i) * D + lane * DPL + e]), f, O[e]);
+                    }
+                }
+                T *o = reinterpret_cast<T *>(p.out) + (size_t)s * D + lane * DPL;
+                const float inv = 1.f / Lx;
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o[e] = EL::narrow(O[e] * inv);
+                if (lane == 0) {
+                    p.ticket[s] = 0;
+                    if (p.select) {
+                        float bv = INFINITY;
+                        int br = -1;
+                        for (int i = 0; i < p.nsplit; ++i) {
+                            const float2 x = __ldcg(&p.part_min[base + i]);
+                            if (better(x.x, __float_as_int(x.y), bv, br)) {
+                                bv = x.x;
+                                br = __float_as_int(x.y);
+                            }
+                        }
+                        if (br >= 0) {
+                            p.last_sel[s] = br;
+                            p.mask[(size_t)s * p.MW + (br >> 5)] |= 1u << (br & 31);
+                        }
+                    }
+                }
             }
         }
     }
+    // A warp that gave up lets its own copies in flight land before exit.
+    if (aborted && lane == 0) {
+        for (int q = consumed; q < issued; ++q) drain_phase(bar0 + 8 * (q % C::NBUF), (q / C::NBUF) & 1);
+    }
+    __syncwarp();
 }
 
 // a1: prompt K, V [S, L_p, D] -> prefix [S, Lcap, 2, D].

@@ -23,6 +23,13 @@ __device__ __forceinline__ void fence_barrier_init()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk-copy) writes to shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -47,13 +54,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
-// Waits for the phase with the given parity to complete; gives up after
-// `limit` polls (each poll suspends the thread for a hardware-chosen time).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit)
+// Potentially blocking test: the thread sleeps until the phase completes or
+// about `hint_ns` nanoseconds pass, so waiting warps leave the issue slots
+// to the warps that work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
 {
-    for (uint32_t i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
 }
 
 // One bulk copy global -> shared, completion signalled on `bar` as
@@ -75,6 +89,32 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uin
             dst),
         "l"(src), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// TMA tensor gather: four rows (y0..y3) of a 2-D tensor map whose box is one
+// row high, starting at column x (x * element size must be a multiple of 16
+// bytes), into consecutive rows at dst (128-byte aligned).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int y0, int y1, int y2, int y3,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+        : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared (LDGSTS, L1 bypassed).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrives on `bar` once all earlier cp.async copies of this thread have
+// landed; the arrival counts toward the barrier's expected count.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first()

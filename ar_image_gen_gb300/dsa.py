@@ -15,7 +15,11 @@ import os
 
 import numpy as np
 
-from .build import LIB
+from .build import LIB as _BUILT_LIB
+
+# DSA_LIB may point at another build of the same library (e.g. a variant with
+# a different pipeline shape); the default is the in-tree build.
+LIB = os.environ.get("DSA_LIB", _BUILT_LIB)
 
 if not os.path.exists(LIB):
     raise ImportError(f"libdsa.so is not built ({LIB}); run ar_image_gen_gb300.build.build()")

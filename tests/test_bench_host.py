@@ -1,0 +1,82 @@
+"""Host logic of bench.py without a GPU: the multi-rank timing reduction
+(2 gloo ranks on CPU), the workload table and the JSON contract of the
+reference arm."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+
+    r, ws = bench.dist_setup()
+    assert (r, ws) == (rank, world) and dist.get_backend() == "gloo"
+    elapsed = 10.0 + rank  # rank 1 is the slow one
+    bench.barrier(ws)
+    out_q.put((rank, bench.max_over_ranks(elapsed, ws)))
+    # the reference arm runs on rank 0 only
+    class A:
+        pass
+    if rank != 0:
+        out_q.put((rank, bench.run_reference(A(), rank, ws)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_rank_timing_takes_the_max():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = [q.get(timeout=120) for _ in range(3)]
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    maxes = sorted(v for r, v in got if isinstance(v, float))
+    assert maxes == [11.0, 11.0]
+    assert (1, None) in got
+
+
+def test_reference_arm_prints_the_contract_line():
+    res = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "3", "--warmup", "3",
+                          "--ref-streams", "32"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert "workload" in line["config"]
+
+
+def test_workload_table_matches_the_sparsity_rule():
+    from ar_image_gen_gb300.synth import WORKLOADS, n_att_for
+
+    assert WORKLOADS["janus-b96"].N_att == 29 and WORKLOADS["janus-b96"].streams == 3072
+    assert [WORKLOADS[f"sweep512-s{s}"].N_att for s in (0, 50, 75, 90, 95)] == [512, 512, 256, 102, 51]
+    assert (WORKLOADS["lumina-s90-b16"].N_att, WORKLOADS["lumina-s95-b16"].N_att) == (410, 205)
+    assert WORKLOADS["stress-s95"].N_att == 405 and WORKLOADS["stress-s95"].L_dec == 8100
+    assert n_att_for(1000, 0, 2000) == 1000
+    d = WORKLOADS["janus-b96"].dense()
+    assert d.N_r == d.N_att == d.L_dec == 576
