@@ -14,6 +14,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -563,3 +564,173 @@ int dsa_set_wait_limit(dsa_handle h, uint32_t limit)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode step.
+//
+// Some callers cannot allocate device memory when they decode: a serving
+// engine that reserves all device memory up front for its own KV arena and
+// forbids libraries from taking more, or code that must not call the
+// allocator from its decode loop (allocation can synchronize the device).
+// For them, dsa_decode_step_noalloc runs the same decode kernel on state
+// buffers the caller owns; the only scratch it needs (the per-split partial
+// results and tickets of long streams, and a status word) lives in the
+// file-scope array below, which every GPU that loads this library holds
+// until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];
+int g_noalloc_sms[kMaxDevices];
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Scratch layout for `heads` streams with `nsplit` partial slots each:
+// status word, tickets, (m, l) and argmin partials, accumulator partials.
+size_t noalloc_scratch_bytes(int heads, int nsplit, int D)
+{
+    const size_t slots = (size_t)heads * nsplit;
+    return 256 + round256((size_t)heads * 4) + round256(slots * 8) * 2 + round256(slots * D * 4);
+}
+
+// Device address of the scratch array on the current device (looked up once
+// per device) and the device's SM count.
+int noalloc_setup(void **ptr, int *sms)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(DSA_ERR_CUDA, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch");
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_noalloc_sms[dev] = n;
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    *sms = g_noalloc_sms[dev];
+    return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int dtype,
+                                       int t, void *prefix, void *ring, uint32_t *mask, int32_t *last_sel,
+                                       const void *q, const void *k_new, const void *v_new, void *out, void *stream)
+{
+    int rc = validate(heads, head_dim, L_p, N_r, N_att, sink, dtype);
+    if (rc != DSA_OK) return rc;
+    if (t < 0) return fail(DSA_ERR_ARG, "t must be >= 0 (got %d)", t);
+    if (!ring || !mask || !last_sel || !q || !k_new || !v_new || !out || (L_p + sink > 0 && !prefix))
+        return fail(DSA_ERR_ARG, "state and input/output pointers must be non-NULL");
+    if (!aligned16(prefix) || !aligned16(ring) || !aligned16(q) || !aligned16(k_new) || !aligned16(v_new) ||
+        !aligned16(out) || ((uintptr_t)mask & 3u) || ((uintptr_t)last_sel & 3u))
+        return fail(DSA_ERR_ARG, "data pointers must be 16-byte aligned (mask and last_sel 4-byte aligned)");
+
+    void *scratch = nullptr;
+    int sms = 0;
+    rc = noalloc_setup(&scratch, &sms);
+    if (rc != DSA_OK) return rc;
+    const int occ = occupancy_for(dtype, head_dim);
+    if (occ < 1) return cuda_fail(cudaGetLastError(), "kernel occupancy query (is this an sm_103 device?)");
+
+    // A handle-shaped description of the caller's state; nothing is allocated.
+    dsa_ctx h{};
+    h.magic = kMagic;
+    h.S = heads;
+    h.D = head_dim;
+    h.L_p = L_p;
+    h.N_r = N_r;
+    h.N_att = N_att;
+    h.sink = sink;
+    h.dtype = dtype;
+    h.R = N_r - sink;
+    h.A = N_att - sink;
+    h.Lcap = L_p + sink;
+    h.MW = (h.R + 31) / 32;
+    h.sm_count = sms;
+    h.ctas_per_sm = occ;
+    h.prefix = prefix;
+    h.ring = ring;
+    Plan pl = make_plan(&h, t);
+    // Fewer splits if the automatic choice does not fit the static scratch.
+    int fit = 0;
+    while (fit < pl.nsplit && noalloc_scratch_bytes(heads, fit + 1, head_dim) <= kNoAllocScratchBytes) ++fit;
+    if (fit < pl.nsplit) {
+        h.forced_split = fit > 0 ? fit : 1;
+        pl = make_plan(&h, t);
+        if (fit == 0 || noalloc_scratch_bytes(heads, pl.nsplit, head_dim) > kNoAllocScratchBytes)
+            return fail(DSA_ERR_ARG,
+                        "dsa_decode_step_noalloc: %d streams with %d splits need %zu bytes of scratch, more than the "
+                        "static %zu bytes; use the handle API (dsa_create / dsa_decode_step) for this size",
+                        heads, pl.nsplit, noalloc_scratch_bytes(heads, pl.nsplit, head_dim), kNoAllocScratchBytes);
+    }
+    rc = encode_ring_map(&h);
+    if (rc != DSA_OK) return rc;
+
+    unsigned char *base = static_cast<unsigned char *>(scratch);
+    const size_t slots = (size_t)heads * pl.nsplit;
+    int *status = reinterpret_cast<int *>(base);
+    int *ticket = reinterpret_cast<int *>(base + 256);
+    float2 *part_ml = reinterpret_cast<float2 *>(base + 256 + round256((size_t)heads * 4));
+    float2 *part_min = reinterpret_cast<float2 *>(reinterpret_cast<unsigned char *>(part_ml) + round256(slots * 8));
+    float *part_acc = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(part_min) + round256(slots * 8));
+
+    cudaStream_t st = (cudaStream_t)stream;
+    // The status word and the tickets must start at zero; the partials are
+    // fully written before they are read.
+    cudaError_t e = cudaMemsetAsync(scratch, 0, 256 + round256((size_t)heads * 4), st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync of the static scratch");
+
+    dsa::DecodeParams p;
+    p.q = q;
+    p.knew = k_new;
+    p.vnew = v_new;
+    p.out = out;
+    p.prefix = prefix;
+    p.ring = ring;
+    p.mask = mask;
+    p.last_sel = last_sel;
+    p.part_acc = part_acc;
+    p.part_ml = part_ml;
+    p.part_min = part_min;
+    p.ticket = ticket;
+    p.status = status;
+    p.S = heads;
+    p.Lcap = h.Lcap;
+    p.P = pl.P;
+    p.sinkmode = pl.sinkmode;
+    p.R = h.R;
+    p.tin = pl.tin;
+    p.tin_mod = pl.tin >= 0 ? pl.tin % h.R : 0;
+    p.wlen = pl.wlen;
+    p.a = pl.a;
+    p.n = pl.n;
+    p.nsplit = pl.nsplit;
+    p.chunk = pl.chunk;
+    p.pstride = pl.nsplit;
+    p.nitems = pl.nitems;
+    p.noskip = (h.A == h.R) ? 1 : 0;
+    p.select = pl.select;
+    p.MW = h.MW;
+    p.qscale = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+    p.wait_limit = kDefaultWaitLimit;
+    if (dtype == DSA_BF16)
+        e = head_dim == 64 ? launch_decode<__nv_bfloat16, 64>(p, h.ring_map, pl.grid, st)
+                           : launch_decode<__nv_bfloat16, 128>(p, h.ring_map, pl.grid, st);
+    else
+        e = head_dim == 64 ? launch_decode<float, 64>(p, h.ring_map, pl.grid, st)
+                           : launch_decode<float, 128>(p, h.ring_map, pl.grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return DSA_OK;
+}

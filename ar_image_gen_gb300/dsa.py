@@ -42,7 +42,7 @@ STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_ARG", -2: "DSA_ERR_STATE", -3: "DSA_ER
 EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa_destroy", "dsa_get_step",
            "dsa_get_skip_mask", "dsa_get_last_selection", "dsa_sync_status", "dsa_last_error",
            "dsa_state_bytes", "dsa_plan_step", "dsa_set_splits", "dsa_set_wait_limit",
-           "dsa_debug_fail_alloc_after"]
+           "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc"]
 
 
 class dsa_step_plan(ctypes.Structure):
@@ -69,6 +69,7 @@ _L.dsa_plan_step.argtypes = [_P, _I, ctypes.POINTER(dsa_step_plan)]
 _L.dsa_set_splits.argtypes = [_P, _I]
 _L.dsa_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
 _L.dsa_debug_fail_alloc_after.argtypes = [_I]
+_L.dsa_decode_step_noalloc.argtypes = [_I] * 8 + [_P] * 9
 
 
 class DSAError(RuntimeError):
@@ -178,6 +179,13 @@ def dsa_set_wait_limit(h, limit) -> int:
 
 def dsa_debug_fail_alloc_after(n) -> int:
     return _L.dsa_debug_fail_alloc_after(n)
+
+
+def dsa_decode_step_noalloc(heads, head_dim, L_p, N_r, N_att, sink, dtype, t, prefix, ring, mask, last_sel,
+                            q, k_new, v_new, out, stream=None) -> int:
+    return _L.dsa_decode_step_noalloc(heads, head_dim, L_p, N_r, N_att, sink, dtype, t, _ptr(prefix), _ptr(ring),
+                                      _ptr(mask), _ptr(last_sel), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                      _stream(stream))
 
 
 # ---- convenience wrapper ---------------------------------------------------

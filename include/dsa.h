@@ -180,6 +180,41 @@ typedef struct dsa_step_plan {
 
 int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out);
 
+/*
+ * dsa_decode_step_noalloc -- one decode step on state buffers the caller
+ * owns, without any device allocation.  The paper has no counterpart: it is
+ * an interface for callers that cannot allocate device memory while they
+ * decode, e.g. a serving engine that reserves all device memory for its own
+ * KV arena up front and does not let libraries take more, or a decode loop
+ * that must not call the allocator because allocation can synchronize the
+ * device.  It runs the same kernel as dsa_decode_step.
+ *
+ * The caller passes the configuration (as for dsa_create_ex), the step t
+ * (0-based; the caller counts steps) and every buffer, all device pointers:
+ *   prefix   [heads, L_p + sink, 2, head_dim]  entry i = K row i then V row i;
+ *            rows 0..L_p-1 hold the prompt (the layout dsa_prefill builds),
+ *            rows L_p.. are written by the sink fill; 16-byte aligned
+ *   ring     [heads, N_r - sink, 2, head_dim]  decode entries; no
+ *            initialisation needed; 16-byte aligned
+ *   mask     [heads, ceil((N_r - sink) / 32)] uint32, all zero before t = 0
+ *   last_sel [heads] int32, written on selection steps
+ *   q, k_new, v_new, out  as for dsa_decode_step.
+ * The split partials, split tickets and a status word live in a static
+ * 4 MiB device array of this library (every GPU that loads the library holds
+ * it until the process exits).  Workloads whose splits would need more
+ * (about 7,800 streams at head_dim 128 without splits, fewer with splits)
+ * are rejected with DSA_ERR_ARG and a message.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress): make that
+ * first call before any stream capture.  Every call shares the array and
+ * clears its tickets and status word when it starts, so calls that overlap
+ * on the GPU (other streams, other threads) race: order them on one stream.
+ * Device-side errors (a bounded wait that gave up) are not reported by this
+ * entry point.  Asynchronous on `stream`.
+ */
+int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int dtype, int t,
+                            void *prefix, void *ring, uint32_t *mask, int32_t *last_sel, const void *q,
+                            const void *k_new, const void *v_new, void *out, void *stream);
+
 /* Tuning and test knobs (not needed for normal use). */
 
 /* Force the number of CTAs per stream (>= 1), or 0 for the automatic
