@@ -205,6 +205,8 @@ int ensure_partials(dsa_ctx *h, int nsplit)
     return DSA_OK;
 }
 
+void forget_handle(const dsa_ctx *h);
+
 void free_ctx(dsa_ctx *h)
 {
     if (!h) return;
@@ -218,6 +220,7 @@ void free_ctx(dsa_ctx *h)
     cudaFree(h->ticket);
     cudaFree(h->status);
     h->magic = 0;
+    forget_handle(h);
     delete h;
 }
 
@@ -269,12 +272,56 @@ int occupancy_for(int dtype, int D)
     return D == 64 ? occupancy<float, 64>() : occupancy<float, 128>();
 }
 
+// Launches the decode kernel as a programmatic dependent launch: its CTAs
+// may start while the previous kernel in the stream finishes; the kernel
+// itself waits for that kernel before it reads inputs or writes anything.
 template <typename T, int D>
 cudaError_t launch_decode(const dsa::DecodeParams &p, const CUtensorMap &map, int grid, cudaStream_t st)
 {
     using C = dsa::KCfg<T, D>;
-    dsa::decode_kernel<T, D><<<grid, C::THREADS, C::SMEM, st>>>(p, map);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dsa::decode_kernel<T, D>, p, map);
+}
+
+// The last handle this library launched a kernel for, per stream: a decode
+// step may read its state before the grid dependency wait only when the
+// kernel just before it in the stream was not one of this handle's own.
+std::mutex g_last_mu;
+struct LastLaunch {
+    cudaStream_t stream;
+    const dsa_ctx *handle;
+};
+LastLaunch g_last[16];
+int g_last_next;
+
+bool note_launch(cudaStream_t st, const dsa_ctx *h)
+{
+    std::lock_guard<std::mutex> lock(g_last_mu);
+    for (auto &e : g_last)
+        if (e.handle && e.stream == st) {
+            const bool other = e.handle != h;
+            e.handle = h;
+            return other;
+        }
+    g_last[g_last_next] = {st, h};
+    g_last_next = (g_last_next + 1) % 16;
+    return false;  // unknown stream: be conservative
+}
+
+void forget_handle(const dsa_ctx *h)
+{
+    std::lock_guard<std::mutex> lock(g_last_mu);
+    for (auto &e : g_last)
+        if (e.handle == h) e.handle = reinterpret_cast<const dsa_ctx *>(&g_last_mu);  // a value no handle has
 }
 
 template <typename T, int D>
@@ -414,6 +461,7 @@ int dsa_prefill(dsa_handle h, const void *K, const void *V, void *stream)
         e = h->D == 64 ? launch_prefill<float, 64>(K, V, h->prefix, h->S, h->L_p, h->Lcap, st)
                        : launch_prefill<float, 128>(K, V, h->prefix, h->S, h->L_p, h->Lcap, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    note_launch(st, h);
     h->t = 0;
     h->prefilled = 1;
     h->last_select = 0;
@@ -485,6 +533,7 @@ int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *
     p.wait_limit = h->wait_limit;
 
     cudaStream_t st = (cudaStream_t)stream;
+    p.early = note_launch(st, h) ? 1 : 0;
     const int grid = pl.grid;
     cudaError_t e;
     if (h->dtype == DSA_BF16)
@@ -725,6 +774,7 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.MW = h.MW;
     p.qscale = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
     p.wait_limit = kDefaultWaitLimit;
+    p.early = 0;  // caller-owned state: the previous kernel may have written it
     if (dtype == DSA_BF16)
         e = head_dim == 64 ? launch_decode<__nv_bfloat16, 64>(p, h.ring_map, pl.grid, st)
                            : launch_decode<__nv_bfloat16, 128>(p, h.ring_map, pl.grid, st);

@@ -104,6 +104,8 @@ struct DecodeParams {
     int select;           // 1: selection step (fused argmin)
     int noskip;           // 1: N_att == N_r, no offset is ever skipped
     int MW;               // mask words per stream
+    int early;            // 1: the previous grid in the stream does not write this state, so
+                          // the mask, prefix and ring may be read before the grid dependency wait
     float qscale;         // log2(e) / sqrt(D), applied to q.k
     uint32_t wait_limit;
 };
@@ -223,7 +225,7 @@ struct KCfg {
     static constexpr int MAXW = 8;                   // mask words per lane kept in registers
     static constexpr int OFF_BAR = NBUF * STAGE_BYTES;
     static constexpr int OFF_LIST = OFF_BAR + NBUF * 8;
-    static constexpr int WARP_SMEM = (OFF_LIST + CHUNK_MAX * 2 + 127) / 128 * 128;
+    static constexpr int WARP_SMEM = (OFF_LIST + 2 * CHUNK_MAX * 2 + 127) / 128 * 128;  // two item lists
     static constexpr int SMEM = WARPS * WARP_SMEM;
     static_assert(LPR >= 2 && LPR <= 16 && 32 % LPR == 0, "row must span a power-of-two lane group");
     static_assert(SROWS % RPW == 0 && NIT >= 1, "stage rows must fill whole warp instructions");
@@ -295,23 +297,43 @@ __global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const Decod
         qn0 = __ldg(qr + cl);
         qn1 = __ldg(qr + cl + C::LPR);
     };
-    if (first_item < p.nitems) {
-        if (inreg && nwords > 0) load_words(first_item);
-        load_q(first_item);
+    // Programmatic dependent launch.  Before the grid dependency wait this
+    // grid only reads its own state (mask, prompt prefix, ring), and only when
+    // the previous grid in the stream is not a step of the same state
+    // (p.early); q, k_new, v_new and every write come after the wait.  Each
+    // CTA lets the next grid start only after its own wait, so the next
+    // grid's early reads happen after the grid before this one completed.
+    if (!p.early) {
+        pdl_wait();
+        pdl_launch_dependents();
     }
+    if (first_item < p.nitems && inreg && nwords > 0) load_words(first_item);
 
     bool aborted = false;
     int issued = 0, consumed = 0;  // stages issued / consumed by this warp over all its items
-    for (int item = first_item; item < p.nitems && !aborted; item += GW) {
+
+    // ---- issuer: a cursor over the stages of this warp's items.  Each freed
+    // buffer is refilled at once, with a stage of the next item once the
+    // current item is fully issued, so the warp's copies stay in flight
+    // across item boundaries.  Items are numbered by seq (0, 1, ... for
+    // this warp); item seq's offsets are listed in list buffer seq & 1, so
+    // the issuer may run at most one item ahead of the consumer.
+    int iss_item = first_item, iss_seq = 0, iss_j = 0;
+    bool iss_ready = false;
+    int I_s = 0, I_lo = 0, I_npre = 0, I_kr0 = 0, I_klo = 0, I_nrows = 0, I_nst = 0;
+    uint32_t self_skip_bits = 0;  // bit (seq & 1): the item's current token is itself skipped
+
+    // a4: list the attended offsets of ranks [klo, khi) of the issuer's item
+    auto setup_item = [&]() {
+        const int item = iss_item;
         const int s = item / p.nsplit;
         const int c = item - s * p.nsplit;
         const int lo = c * p.chunk;
         const int hi = min(lo + p.chunk, p.n);
-        const int klo = max(lo, p.P) - p.P;  // attended decode ranks of the item: [klo, khi)
+        const int klo = max(lo, p.P) - p.P;
         const int khi = max(hi, p.P) - p.P;
+        uint16_t *lst = list + (iss_seq & 1) * C::CHUNK_MAX;
         const uint32_t *mrow = p.mask + (size_t)s * p.MW;
-
-        // ---- a4: ranks [klo, khi) -> relative offsets (list)
         bool self_skip = false;
         if (nwords > 0) {
             int mine = 0;
@@ -338,7 +360,7 @@ __global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const Decod
                 // The skip mask disagrees with the host's count: record it and
                 // keep every listed offset in range.
                 if (lane == 0) atomicOr(p.status, ST_CHECK);
-                for (int i = lane; i < khi - klo; i += 32) list[i] = 0;
+                for (int i = lane; i < khi - klo; i += 32) lst[i] = 0;
                 __syncwarp();
             }
             int rank = incl - mine;
@@ -361,20 +383,141 @@ __global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const Decod
                 }
                 while (bits) {
                     const int bt = __ffs(bits) - 1;
-                    if (rank >= klo && rank < khi) list[rank - klo] = (uint16_t)(w * 32 + bt);
+                    if (rank >= klo && rank < khi) lst[rank - klo] = (uint16_t)(w * 32 + bt);
                     ++rank;
                     bits &= bits - 1;
                 }
             }
             const uint32_t w0 = inreg ? words[0] : __ldcg(mrow);
             self_skip = (__shfl_sync(0xffffffffu, w0, 0) & 1u) != 0;
+            if (inreg && item + GW < p.nitems) load_words(item + GW);  // prefetch for the next item
         }
         __syncwarp();
-        const typename EL::Q q0 = EL::load_q(qn0), q1 = EL::load_q(qn1);
-        if (item + GW < p.nitems) {  // prefetch the next item's mask words and q
-            if (inreg && nwords > 0) load_words(item + GW);
-            load_q(item + GW);
+        const bool has_cur = (klo == 0 && khi > 0 && !self_skip);
+        self_skip_bits = (self_skip_bits & ~(1u << (iss_seq & 1))) | ((self_skip ? 1u : 0u) << (iss_seq & 1));
+        I_s = s;
+        I_lo = lo;
+        I_klo = klo;
+        I_npre = max(min(hi, p.P) - lo, 0);
+        I_kr0 = has_cur ? klo + 1 : klo;
+        I_nrows = I_npre + max(khi - I_kr0, 0);
+        I_nst = (I_nrows + C::SROWS - 1) / C::SROWS;
+        iss_ready = true;
+    };
+
+    // a5: issue stage iss_j of the issuer's item into buffer issued % NBUF
+    auto issue_stage = [&]() {
+        const int b = issued % C::NBUF;
+        const uint32_t fb = bar0 + 8 * b;
+        const uint32_t dst = buf0 + b * C::STAGE_BYTES;
+        const int u0 = iss_j * C::SROWS;
+        const int u1 = min(u0 + C::SROWS, I_nrows);
+        const unsigned char *pre = reinterpret_cast<const unsigned char *>(p.prefix) + ((size_t)I_s * p.Lcap + I_lo) * C::ROW;
+        const unsigned char *rng = reinterpret_cast<const unsigned char *>(p.ring) + (size_t)I_s * p.R * C::ROW;
+        if (lane == 0) {
+            fence_proxy_async_smem();  // this warp's reads of the buffer precede the new fill
+            mbar_arrive_expect_tx(fb, (uint32_t)(u1 - u0) * C::ROW);
+            const int pb = min(u1, I_npre);
+            if (pb > u0) bulk_g2s_hint(dst, pre + (size_t)u0 * C::ROW, (pb - u0) * C::ROW, fb, pol);
         }
+        const int ua = max(u0, I_npre);
+        const int nr = u1 - ua;  // ring entries of the stage
+        if (nr > 0) {
+            const int k0 = I_kr0 + (ua - I_npre);
+            const uint32_t rd = dst + (ua - u0) * C::ROW;
+            if (p.noskip) {
+                // offset r = rank: descending slots, at most two contiguous runs
+                if (lane == 0) {
+                    const int kA = min(k0 + nr, p.tin_mod + 1);
+                    const int nA = max(kA - k0, 0);
+                    if (nA > 0) bulk_g2s_hint(rd, rng + (size_t)(p.tin_mod - (kA - 1)) * C::ROW, nA * C::ROW, fb, pol);
+                    if (nr > nA)
+                        bulk_g2s_hint(rd + nA * C::ROW, rng + (size_t)(p.tin_mod - (k0 + nr - 1) + p.R) * C::ROW,
+                                      (nr - nA) * C::ROW, fb, pol);
+                }
+            } else {
+                const uint16_t *lst = list + (iss_seq & 1) * C::CHUNK_MAX;
+                const int ybase = I_s * p.R;
+                const int ngrp = nr >> 2;
+                for (int g4 = lane; g4 < ngrp; g4 += 32) {
+                    const int k = k0 + 4 * g4 - I_klo;
+                    int y[4];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const int sl = p.tin_mod - (int)lst[k + m];
+                        y[m] = ybase + (sl < 0 ? sl + p.R : sl);
+                    }
+                    tma_gather4(rd + 4 * g4 * C::ROW, &tmap, 0, y[0], y[1], y[2], y[3], fb);
+                }
+                const int tail = nr - 4 * ngrp;
+                if (lane < tail) {
+                    int sl = p.tin_mod - (int)lst[k0 + 4 * ngrp + lane - I_klo];
+                    sl = sl < 0 ? sl + p.R : sl;
+                    bulk_g2s_hint(rd + (4 * ngrp + lane) * C::ROW, rng + (size_t)sl * C::ROW, C::ROW, fb, pol);
+                }
+            }
+        }
+        ++issued;
+        ++iss_j;
+    };
+
+    // Issues the next stage in the warp's stream, if any (at most one item
+    // ahead of the consumer's item con_seq).
+    auto issue_next = [&](int con_seq) {
+        while (iss_item < p.nitems) {
+            if (!iss_ready) {
+                if (iss_seq > con_seq + 1) return;
+                setup_item();
+            }
+            if (iss_j < I_nst) {
+                issue_stage();
+                return;
+            }
+            iss_item += GW;
+            ++iss_seq;
+            iss_j = 0;
+            iss_ready = false;
+        }
+    };
+
+    // Keeps NBUF stages of the warp's stream in flight (fewer at its end).
+    auto top_up = [&](int con_seq) {
+        while (issued - consumed < C::NBUF) {
+            const int before = issued;
+            issue_next(con_seq);
+            if (issued == before) return;
+        }
+    };
+    top_up(0);
+    if (p.early) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+    if (first_item < p.nitems) load_q(first_item);
+
+    // ---- consumer: the items in order
+    int con_seq = 0;
+    for (int item = first_item; item < p.nitems; item += GW, ++con_seq) {
+        // The issuer set up every earlier item; bring it to this one if items
+        // without staged rows left it behind, and list this item if needed.
+        while (iss_seq < con_seq) {
+            iss_item += GW;
+            ++iss_seq;
+            iss_j = 0;
+            iss_ready = false;
+        }
+        if (iss_seq == con_seq && !iss_ready) setup_item();
+        top_up(con_seq);
+        const int s = item / p.nsplit;
+        const int c = item - s * p.nsplit;
+        const int lo = c * p.chunk;
+        const int hi = min(lo + p.chunk, p.n);
+        const int klo = max(lo, p.P) - p.P;
+        const int khi = max(hi, p.P) - p.P;
+        const bool self_skip = (self_skip_bits >> (con_seq & 1)) & 1u;
+        const uint16_t *lst = list + (con_seq & 1) * C::CHUNK_MAX;
+        const typename EL::Q q0 = EL::load_q(qn0), q1 = EL::load_q(qn1);
+        if (item + GW < p.nitems) load_q(item + GW);  // prefetch the next item's q
 
         // rank 0 is the current token (offset 0) unless it is itself skipped
         const bool has_cur = (klo == 0 && khi > 0 && !self_skip);
@@ -396,66 +539,10 @@ __global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const Decod
             const uint4 *vs = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.vnew) + (size_t)s * D);
             for (int i = lane; i < 2 * NV; i += 32) dst[i] = (i < NV) ? ks[i] : vs[i - NV];
         }
-
-        // rows staged through shared memory: prompt rows [lo, lo + npre), then
-        // the attended ring entries of ranks [kr0, khi)
         const int npre = max(min(hi, p.P) - lo, 0);
         const int kr0 = has_cur ? klo + 1 : klo;
         const int nrows = npre + max(khi - kr0, 0);
         const int nst = (nrows + C::SROWS - 1) / C::SROWS;
-        const unsigned char *pre = reinterpret_cast<const unsigned char *>(p.prefix) + ((size_t)s * p.Lcap + lo) * C::ROW;
-        const unsigned char *rng = reinterpret_cast<const unsigned char *>(p.ring) + (size_t)s * p.R * C::ROW;
-
-        auto issue = [&](int j) {  // stage j of the item into buffer issued % NBUF
-            const int b = issued % C::NBUF;
-            const uint32_t fb = bar0 + 8 * b;
-            const uint32_t dst = buf0 + b * C::STAGE_BYTES;
-            const int u0 = j * C::SROWS;
-            const int u1 = min(u0 + C::SROWS, nrows);
-            if (lane == 0) {
-                fence_proxy_async_smem();  // this warp's reads of the buffer precede the new fill
-                mbar_arrive_expect_tx(fb, (uint32_t)(u1 - u0) * C::ROW);
-                const int pb = min(u1, npre);
-                if (pb > u0) bulk_g2s_hint(dst, pre + (size_t)u0 * C::ROW, (pb - u0) * C::ROW, fb, pol);
-            }
-            const int ua = max(u0, npre);
-            const int nr = u1 - ua;  // ring entries of the stage
-            if (nr > 0) {
-                const int k0 = kr0 + (ua - npre);
-                const uint32_t rd = dst + (ua - u0) * C::ROW;
-                if (p.noskip) {
-                    // offset r = rank: descending slots, at most two contiguous runs
-                    if (lane == 0) {
-                        const int kA = min(k0 + nr, p.tin_mod + 1);
-                        const int nA = max(kA - k0, 0);
-                        if (nA > 0) bulk_g2s_hint(rd, rng + (size_t)(p.tin_mod - (kA - 1)) * C::ROW, nA * C::ROW, fb, pol);
-                        if (nr > nA)
-                            bulk_g2s_hint(rd + nA * C::ROW, rng + (size_t)(p.tin_mod - (k0 + nr - 1) + p.R) * C::ROW,
-                                          (nr - nA) * C::ROW, fb, pol);
-                    }
-                } else {
-                    const int ybase = s * p.R;
-                    const int ngrp = nr >> 2;
-                    for (int g4 = lane; g4 < ngrp; g4 += 32) {
-                        const int k = k0 + 4 * g4 - klo;
-                        int y[4];
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const int sl = p.tin_mod - (int)list[k + m];
-                            y[m] = ybase + (sl < 0 ? sl + p.R : sl);
-                        }
-                        tma_gather4(rd + 4 * g4 * C::ROW, &tmap, 0, y[0], y[1], y[2], y[3], fb);
-                    }
-                    const int tail = nr - 4 * ngrp;
-                    if (lane < tail) {
-                        int sl = p.tin_mod - (int)list[k0 + 4 * ngrp + lane - klo];
-                        sl = sl < 0 ? sl + p.R : sl;
-                        bulk_g2s_hint(rd + (4 * ngrp + lane) * C::ROW, rng + (size_t)sl * C::ROW, C::ROW, fb, pol);
-                    }
-                }
-            }
-            ++issued;
-        };
 
         float acc[2 * C::VEC];
 #pragma unroll
@@ -463,7 +550,6 @@ __global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const Decod
         float m = -INFINITY, l = 0.f, minv = INFINITY;
         int minr = -1;
 
-        for (int j = 0; j < min(C::NBUF, nst); ++j) issue(j);
         for (int j = 0; j < nst; ++j) {
             const int b = consumed % C::NBUF;
             const bool ok = wait_phase(bar0 + 8 * b, (consumed / C::NBUF) & 1, p.wait_limit);
@@ -494,7 +580,7 @@ __global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const Decod
                 sc[it] = valid ? x : -INFINITY;
                 if (p.select && valid && u0 + row >= npre) {
                     const int k = kr0 + (u0 + row - npre);
-                    const int r = list[k - klo];
+                    const int r = lst[k - klo];
                     if (better(x, r, minv, minr)) {
                         minv = x;
                         minr = r;
@@ -525,7 +611,7 @@ __global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const Decod
                 }
             }
             __syncwarp();
-            if (j + C::NBUF < nst) issue(j + C::NBUF);
+            top_up(con_seq);  // refill the freed buffer
         }
         if (aborted) break;
 

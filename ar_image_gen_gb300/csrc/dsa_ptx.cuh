@@ -91,6 +91,12 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uin
         : "memory");
 }
 
+// Programmatic dependent launch: let the next grid in the stream start its
+// CTAs as this grid's CTAs retire, and wait for the previous grid (its
+// completion and memory) before touching what it may have produced.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // TMA tensor gather: four rows (y0..y3) of a 2-D tensor map whose box is one
 // row high, starting at column x (x * element size must be a multiple of 16
 // bytes), into consecutive rows at dst (128-byte aligned).
