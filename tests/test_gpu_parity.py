@@ -91,3 +91,47 @@ def test_split_count_does_not_change_the_result():
     for o, m in results[1:]:
         assert (m == results[0][1]).all()
         assert torch.allclose(o, results[0][0], atol=2e-2, rtol=2e-2)
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+def test_interleaved_handles_on_one_stream(splits):
+    """Several handles (layers) stepped round-robin on one stream, as a model
+    decodes: each launch may read its own state before it waits for the
+    previous launch (another handle), so every layer is checked against its
+    own oracle at every step."""
+    import numpy as np
+
+    from ar_image_gen_gb300.dsa import DSA
+    from ar_image_gen_gb300.synth import TraceGen
+    from oracle.oracle import OracleBatch
+
+    wl = small("interleave", 40, 48, 10, grid=9, heads=6)
+    S, d = wl.streams, wl.head_dim
+    layers = []
+    for layer in range(3):
+        gen = TraceGen(wl, layer=layer, device="cuda")
+        h = DSA(S, d, wl.L_p, wl.N_r, wl.N_att, 0, "bf16")
+        if splits:
+            h.set_splits(splits)
+        K, V = gen.prompt()
+        h.prefill(K, V)
+        orc = OracleBatch(S, d, wl.L_p, wl.N_r, wl.N_att, 0)
+        orc.prefill(K.double().cpu().numpy(), V.double().cpu().numpy())
+        layers.append((gen, h, orc, torch.empty((S, d), dtype=torch.bfloat16, device="cuda")))
+    for t in range(wl.L_dec):
+        steps = [gen.step(t) for gen, _, _, _ in layers]
+        for (gen, h, orc, out), (q, k, v) in zip(layers, steps):  # decode launches back to back
+            h.decode_step(q, k, v, out)
+        torch.cuda.synchronize()
+        for (gen, h, orc, out), (q, k, v) in zip(layers, steps):
+            sel = h.last_selection()
+            picks = np.array([t - r if r >= 0 else -1 for r in sel], dtype=np.int32)
+            ref, infos = orc.step(q.double().cpu().numpy(), k.double().cpu().numpy(), v.double().cpu().numpy(),
+                                  picks=picks)
+            got = out.double().cpu().numpy()
+            assert (np.abs(got - ref) <= 2e-3 + 1e-2 * np.abs(ref)).all(), f"t={t}"
+            for i, info in enumerate(infos):
+                assert not info.mismatch and info.selected == picks[i], f"t={t} stream {i}"
+    for gen, h, orc, out in layers:
+        assert h.sync_status() == 0
+        h.close()
