@@ -94,7 +94,6 @@ struct dsa_ctx {
     int32_t *last_sel;
     float *part_acc;
     float2 *part_ml, *part_min;
-    int *ticket;
     int *status;
     CUtensorMap ring_map;  // 2-D view of the ring: [S * R rows, 2 * D], one-row box
 };
@@ -123,16 +122,18 @@ struct Plan {
     unsigned long long bytes;
 };
 
-// Work items per stream: one item per stream while there are at least as
-// many streams as resident warps; otherwise split streams until every warp
-// has an item, keeping at least two stages of rows per split and at most
-// kChunkMax rows per item.
+// Work items per stream.  Splitting a stream costs a partial write and a
+// merge; it pays when the streams alone leave most warps idle (each warp
+// streams its rows through a short pipeline, so few warps cannot keep HBM
+// busy).  Streams are split into about resident-warps / streams pieces (one
+// round of items) once they fill at most half the warps, with at least two
+// stages of rows per piece; streams longer than kChunkMax rows always split.
 int auto_splits(const dsa_ctx *h, int n)
 {
     const int rows = stage_rows(h->dtype, h->D);
     const int need = (n + kChunkMax - 1) / kChunkMax;
     const long long warps = (long long)h->sm_count * h->ctas_per_sm * kWarpsPerCta;
-    const int want = h->S >= warps ? 1 : (int)((warps + h->S - 1) / h->S);
+    const int want = 2LL * h->S <= warps ? (int)(warps / h->S) : 1;
     const int by_rows = n / (2 * rows) > 1 ? n / (2 * rows) : 1;
     const int ns = want < by_rows ? want : by_rows;
     return ns > need ? ns : need;
@@ -171,9 +172,13 @@ Plan make_plan(const dsa_ctx *h, int t)
     p.chunk = chunk;
     p.nsplit = (p.n + chunk - 1) / chunk;
     p.nitems = p.nsplit * h->S;
-    const long long ctas = (long long)h->sm_count * h->ctas_per_sm;
-    const long long need_ctas = (p.nitems + kWarpsPerCta - 1) / kWarpsPerCta;
-    p.grid = (int)(need_ctas < ctas ? need_ctas : ctas);
+    // Give every warp the same number of items: with k = ceil(items / resident
+    // warps) rounds of items, use just enough warps for k items each, so no
+    // warp runs a round that most others do not.
+    const long long max_warps = (long long)h->sm_count * h->ctas_per_sm * kWarpsPerCta;
+    const long long rounds = (p.nitems + max_warps - 1) / max_warps;
+    const long long warps = (p.nitems + rounds - 1) / rounds;
+    p.grid = (int)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
     const unsigned long long De = (unsigned long long)h->D * elem_bytes(h->dtype);
     // K and V rows read (current token through k_new/v_new) + q + k_new, v_new
     // read + new entry written + out written.
@@ -217,7 +222,6 @@ void free_ctx(dsa_ctx *h)
     cudaFree(h->part_acc);
     cudaFree(h->part_ml);
     cudaFree(h->part_min);
-    cudaFree(h->ticket);
     cudaFree(h->status);
     h->magic = 0;
     forget_handle(h);
@@ -290,6 +294,36 @@ cudaError_t launch_decode(const dsa::DecodeParams &p, const CUtensorMap &map, in
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, dsa::decode_kernel<T, D>, p, map);
+}
+
+template <typename T, int D>
+cudaError_t launch_merge(const dsa::DecodeParams &p, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.S + dsa::kMergeWarps - 1) / dsa::kMergeWarps);
+    cfg.blockDim = dim3(32 * dsa::kMergeWarps);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dsa::merge_kernel<T, D>, p);
+}
+
+// Decode launch plus, when streams are split, the merge launch.
+cudaError_t launch_step(int dtype, int D, const dsa::DecodeParams &p, const CUtensorMap &map, int grid, cudaStream_t st)
+{
+    cudaError_t e;
+    if (dtype == DSA_BF16)
+        e = D == 64 ? launch_decode<__nv_bfloat16, 64>(p, map, grid, st) : launch_decode<__nv_bfloat16, 128>(p, map, grid, st);
+    else
+        e = D == 64 ? launch_decode<float, 64>(p, map, grid, st) : launch_decode<float, 128>(p, map, grid, st);
+    if (e != cudaSuccess || p.nsplit == 1) return e;
+    if (dtype == DSA_BF16)
+        return D == 64 ? launch_merge<__nv_bfloat16, 64>(p, st) : launch_merge<__nv_bfloat16, 128>(p, st);
+    return D == 64 ? launch_merge<float, 64>(p, st) : launch_merge<float, 128>(p, st);
 }
 
 // The last handle this library launched a kernel for, per stream: a decode
@@ -407,7 +441,6 @@ int dsa_create_ex(int heads, int head_dim, int L_p, int N_r, int N_att, int sink
     if (rc == DSA_OK) rc = dev_alloc(&h->ring, S * h->R * row, "decode ring");
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->mask, S * h->MW * 4, "skip mask");
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->last_sel, S * 4, "last selection");
-    if (rc == DSA_OK) rc = dev_alloc((void **)&h->ticket, S * 4, "split tickets");
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->status, 16, "status word");
     if (rc == DSA_OK) rc = ensure_partials(h, auto_splits(h, L_p + N_att));
     if (rc == DSA_OK) rc = encode_ring_map(h);
@@ -418,7 +451,7 @@ int dsa_create_ex(int heads, int head_dim, int L_p, int N_r, int N_att, int sink
         return rc;
     }
     if ((e = cudaMemset(h->mask, 0, S * h->MW * 4)) != cudaSuccess ||
-        (e = cudaMemset(h->ticket, 0, S * 4)) != cudaSuccess || (e = cudaMemset(h->status, 0, 16)) != cudaSuccess ||
+        (e = cudaMemset(h->status, 0, 16)) != cudaSuccess ||
         (e = cudaMemset(h->last_sel, 0xff, S * 4)) != cudaSuccess) {
         free_ctx(h);
         return cuda_fail(e, "cudaMemset");
@@ -450,7 +483,6 @@ int dsa_prefill(dsa_handle h, const void *K, const void *V, void *stream)
     const size_t S = (size_t)h->S;
     cudaError_t e;
     if ((e = cudaMemsetAsync(h->mask, 0, S * h->MW * 4, st)) != cudaSuccess ||
-        (e = cudaMemsetAsync(h->ticket, 0, S * 4, st)) != cudaSuccess ||
         (e = cudaMemsetAsync(h->status, 0, 16, st)) != cudaSuccess ||
         (e = cudaMemsetAsync(h->last_sel, 0xff, S * 4, st)) != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync");
@@ -510,7 +542,6 @@ int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *
     p.part_acc = h->part_acc;
     p.part_ml = h->part_ml;
     p.part_min = h->part_min;
-    p.ticket = h->ticket;
     p.status = h->status;
     p.S = h->S;
     p.Lcap = h->Lcap;
@@ -534,14 +565,7 @@ int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *
 
     cudaStream_t st = (cudaStream_t)stream;
     p.early = note_launch(st, h) ? 1 : 0;
-    const int grid = pl.grid;
-    cudaError_t e;
-    if (h->dtype == DSA_BF16)
-        e = h->D == 64 ? launch_decode<__nv_bfloat16, 64>(p, h->ring_map, grid, st)
-                       : launch_decode<__nv_bfloat16, 128>(p, h->ring_map, grid, st);
-    else
-        e = h->D == 64 ? launch_decode<float, 64>(p, h->ring_map, grid, st)
-                       : launch_decode<float, 128>(p, h->ring_map, grid, st);
+    cudaError_t e = launch_step(h->dtype, h->D, p, h->ring_map, pl.grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     h->last_select = pl.select;
     h->t += 1;
@@ -623,7 +647,7 @@ int dsa_set_wait_limit(dsa_handle h, uint32_t limit)
 // allocator from its decode loop (allocation can synchronize the device).
 // For them, dsa_decode_step_noalloc runs the same decode kernel on state
 // buffers the caller owns; the only scratch it needs (the per-split partial
-// results and tickets of long streams, and a status word) lives in the
+// results of split streams and a status word) lives in the
 // file-scope array below, which every GPU that loads this library holds
 // until the process exits.
 // ---------------------------------------------------------------------------
@@ -640,11 +664,11 @@ int g_noalloc_sms[kMaxDevices];
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Scratch layout for `heads` streams with `nsplit` partial slots each:
-// status word, tickets, (m, l) and argmin partials, accumulator partials.
+// status word, (m, l) and argmin partials, accumulator partials.
 size_t noalloc_scratch_bytes(int heads, int nsplit, int D)
 {
     const size_t slots = (size_t)heads * nsplit;
-    return 256 + round256((size_t)heads * 4) + round256(slots * 8) * 2 + round256(slots * D * 4);
+    return 256 + round256(slots * 8) * 2 + round256(slots * D * 4);
 }
 
 // Device address of the scratch array on the current device (looked up once
@@ -730,15 +754,14 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     unsigned char *base = static_cast<unsigned char *>(scratch);
     const size_t slots = (size_t)heads * pl.nsplit;
     int *status = reinterpret_cast<int *>(base);
-    int *ticket = reinterpret_cast<int *>(base + 256);
-    float2 *part_ml = reinterpret_cast<float2 *>(base + 256 + round256((size_t)heads * 4));
+    float2 *part_ml = reinterpret_cast<float2 *>(base + 256);
     float2 *part_min = reinterpret_cast<float2 *>(reinterpret_cast<unsigned char *>(part_ml) + round256(slots * 8));
     float *part_acc = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(part_min) + round256(slots * 8));
 
     cudaStream_t st = (cudaStream_t)stream;
-    // The status word and the tickets must start at zero; the partials are
-    // fully written before they are read.
-    cudaError_t e = cudaMemsetAsync(scratch, 0, 256 + round256((size_t)heads * 4), st);
+    // The status word must start at zero; the partials are fully written
+    // before they are read.
+    cudaError_t e = cudaMemsetAsync(scratch, 0, 256, st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync of the static scratch");
 
     dsa::DecodeParams p;
@@ -753,7 +776,6 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.part_acc = part_acc;
     p.part_ml = part_ml;
     p.part_min = part_min;
-    p.ticket = ticket;
     p.status = status;
     p.S = heads;
     p.Lcap = h.Lcap;
@@ -775,12 +797,7 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.qscale = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
     p.wait_limit = kDefaultWaitLimit;
     p.early = 0;  // caller-owned state: the previous kernel may have written it
-    if (dtype == DSA_BF16)
-        e = head_dim == 64 ? launch_decode<__nv_bfloat16, 64>(p, h.ring_map, pl.grid, st)
-                           : launch_decode<__nv_bfloat16, 128>(p, h.ring_map, pl.grid, st);
-    else
-        e = head_dim == 64 ? launch_decode<float, 64>(p, h.ring_map, pl.grid, st)
-                           : launch_decode<float, 128>(p, h.ring_map, pl.grid, st);
+    e = launch_step(dtype, head_dim, p, h.ring_map, pl.grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return DSA_OK;
 }

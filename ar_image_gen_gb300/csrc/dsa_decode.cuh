@@ -17,10 +17,11 @@
 //       shared-memory stages; fp32 logits q.k with 8 lanes per row;
 //   a6  online softmax and P.V, combined over the warp's row groups with
 //       shuffles;
-//   a7  split combine: the last split of a stream to finish (atomic ticket)
-//       merges the per-split (m, l, acc) partials;
+//   a7  split combine: split items write (m, l, acc, argmin) partials that
+//       merge_kernel, launched right after, combines;
 //   a8  fused argmin over the attended decode logits on selection steps; the
-//       finishing warp sets bit r* of the stream's relative-offset skip mask.
+//       warp (or merge_kernel, for split streams) sets bit r* of the stream's
+//       relative-offset skip mask.
 // The diagonal shift (+1 per step) costs nothing: skipped entries are kept as
 // relative offsets r = t' - position, which the shift leaves unchanged, and
 // the slot of offset r is (t' - r) mod R.  Many independent warps per SM each
@@ -85,7 +86,6 @@ struct DecodeParams {
     float *part_acc;      // [S, pstride, D]
     float2 *part_ml;      // [S, pstride]  (m, l)
     float2 *part_min;     // [S, pstride]  (min logit, r as int bits)
-    int *ticket;          // [S]
     int *status;          // sticky device status bits
     int S;
     int Lcap;             // prefix rows per stream (L_p + sink)
@@ -673,8 +673,8 @@ __global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const Decod
                 p.mask[(size_t)s * p.MW + (minr >> 5)] |= 1u << (minr & 31);
             }
         } else {
-            // ---- a7: partial (m, l, acc) of this split; the last split of the
-            // stream to finish merges them
+            // ---- a7: partial (m, l, acc, argmin) of this split; merge_kernel,
+            // launched right after this kernel, combines the splits
             const size_t slot = (size_t)s * p.pstride + c;
             if (g == 0) {
                 float4 *pa = reinterpret_cast<float4 *>(p.part_acc + slot * D);
@@ -689,53 +689,6 @@ __global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const Decod
                 p.part_ml[slot] = make_float2(m, l);
                 p.part_min[slot] = make_float2(minv, __int_as_float(minr));
             }
-            __threadfence();
-            __syncwarp();
-            int last = 0;
-            if (lane == 0) last = (atomicAdd(p.ticket + s, 1) == p.nsplit - 1);
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {
-                __threadfence();
-                const size_t base = (size_t)s * p.pstride;
-                float Mx = -INFINITY;
-                for (int i = 0; i < p.nsplit; ++i) Mx = fmaxf(Mx, __ldcg(&p.part_ml[base + i].x));
-                constexpr int DPL = D / 32;  // output elements per lane
-                float O[DPL];
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) O[e] = 0.f;
-                float Lx = 0.f;
-                for (int i = 0; i < p.nsplit; ++i) {
-                    const float2 ml = __ldcg(&p.part_ml[base + i]);
-                    if (ml.x != -INFINITY) {
-                        const float f = ex2(ml.x - Mx);
-                        Lx = fmaf(ml.y, f, Lx);
-#pragma unroll
-                        for (int e = 0; e < DPL; ++e) O[e] = fmaf(__ldcg(&p.part_acc[(base + i) * D + lane * DPL + e]), f, O[e]);
-                    }
-                }
-                T *o = reinterpret_cast<T *>(p.out) + (size_t)s * D + lane * DPL;
-                const float inv = 1.f / Lx;
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) o[e] = EL::narrow(O[e] * inv);
-                if (lane == 0) {
-                    p.ticket[s] = 0;
-                    if (p.select) {
-                        float bv = INFINITY;
-                        int br = -1;
-                        for (int i = 0; i < p.nsplit; ++i) {
-                            const float2 x = __ldcg(&p.part_min[base + i]);
-                            if (better(x.x, __float_as_int(x.y), bv, br)) {
-                                bv = x.x;
-                                br = __float_as_int(x.y);
-                            }
-                        }
-                        if (br >= 0) {
-                            p.last_sel[s] = br;
-                            p.mask[(size_t)s * p.MW + (br >> 5)] |= 1u << (br & 31);
-                        }
-                    }
-                }
-            }
         }
     }
     // A warp that gave up lets its own copies in flight land before exit.
@@ -743,6 +696,70 @@ __global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const Decod
         for (int q = consumed; q < issued; ++q) drain_phase(bar0 + 8 * (q % C::NBUF), (q / C::NBUF) & 1);
     }
     __syncwarp();
+}
+
+// a7: merges the per-split partials of every stream after a decode launch
+// whose streams were split: out = sum_i e^(m_i - M) acc_i / sum_i e^(m_i - M) l_i,
+// and on selection steps the argmin over the splits' (logit, offset) pairs
+// sets the stream's skip bit.  One warp per stream.
+constexpr int kMergeWarps = 4;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodeParams p)
+{
+    using EL = Elem<T>;
+    pdl_wait();  // the decode kernel's partials
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int s = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+    if (s >= p.S) return;
+    const size_t base = (size_t)s * p.pstride;
+    float Mx = -INFINITY;
+    for (int i = lane; i < p.nsplit; i += 32) Mx = fmaxf(Mx, __ldcg(&p.part_ml[base + i].x));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+    constexpr int DPL = D / 32;  // output elements per lane
+    float O[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) O[e] = 0.f;
+    float Lx = 0.f;
+    for (int i = 0; i < p.nsplit; ++i) {
+        const float2 ml = __ldcg(&p.part_ml[base + i]);
+        if (ml.x != -INFINITY) {
+            const float f = ex2(ml.x - Mx);
+            Lx = fmaf(ml.y, f, Lx);
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) O[e] = fmaf(__ldcg(&p.part_acc[(base + i) * D + lane * DPL + e]), f, O[e]);
+        }
+    }
+    T *o = reinterpret_cast<T *>(p.out) + (size_t)s * D + lane * DPL;
+    const float inv = 1.f / Lx;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) o[e] = EL::narrow(O[e] * inv);
+    if (p.select) {
+        float bv = INFINITY;
+        int br = -1;
+        for (int i = lane; i < p.nsplit; i += 32) {
+            const float2 x = __ldcg(&p.part_min[base + i]);
+            if (better(x.x, __float_as_int(x.y), bv, br)) {
+                bv = x.x;
+                br = __float_as_int(x.y);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int orr = __shfl_xor_sync(0xffffffffu, br, off);
+            if (better(ov, orr, bv, br)) {
+                bv = ov;
+                br = orr;
+            }
+        }
+        if (lane == 0 && br >= 0 && *reinterpret_cast<volatile int *>(p.status) == 0) {
+            p.last_sel[s] = br;
+            p.mask[(size_t)s * p.MW + (br >> 5)] |= 1u << (br & 31);
+        }
+    }
 }
 
 // a1: prompt K, V [S, L_p, D] -> prefix [S, Lcap, 2, D].

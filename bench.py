@@ -544,6 +544,55 @@ def _workload(args):
     return wl
 
 
+SWEEP = ["janus-b32", "janus-b96", "sweep512-s50", "sweep512-s75", "sweep512-s90", "sweep512-s95",
+         "sweep512-sink4-s95", "lumina-s90-b16", "lumina-s95-b16", "lumina-s95-b32", "lumina-s95-b54", "stress-s95"]
+
+
+def run_sweep(args) -> None:
+    """One JSON line per workload (sparse, phase-3 steady state) and per dense
+    setting (last steps of the trace): average launch time back to back over
+    `layers` distinct layers, GB/s of algorithmic bytes and the fraction of
+    the measured peak.  Not the benchmark contract's line."""
+    import torch
+    from dataclasses import replace
+
+    from __graft_entry__ import build
+    from ar_image_gen_gb300.synth import WORKLOADS
+
+    build()
+    peak, peak_kind = measured_peak()
+    layers = args.layers or 4
+    for key in (args.sweep_only.split(",") if args.sweep_only else SWEEP):
+        base = replace(WORKLOADS[key], layers=layers)
+        for dense in (False, True):
+            wl = base.dense() if dense else base
+            if dense and key == "stress-s95":
+                wl = wl.with_batch(32)  # dense KV of this size: 4.3 GB per layer at batch 32
+            steps = max(8, min(args.steps, 40))
+            st = Stack(wl, pool_steps=4)
+            if args.splits:
+                for h in st.handles:
+                    h.set_splits(args.splits)
+            t0 = (wl.L_dec - steps) if dense else wl.N_r + wl.sink
+            st.make_pool(min(t0, wl.L_dec - 1))
+            st.advance(t0, generate=False)
+            time_steps(st, 3, per_launch=False) if not dense else None
+            t_first = st.handles[0].t
+            plan = st.handles[0].plan(t_first)
+            el, _, n = time_steps(st, steps, per_launch=False)
+            nbytes = sum(st.handles[0].plan(t_first + i).algo_bytes for i in range(steps)) * wl.layers
+            gbs = nbytes / (el / 1e3) / 1e9
+            print(json.dumps({"workload": wl.name, "dense": dense, "streams": wl.streams, "layers": wl.layers,
+                              "rows_per_stream": plan.n_prefix + plan.n_decode, "nsplit": plan.nsplit,
+                              "steps": f"{t_first}..{t_first + steps - 1}", "ms_per_launch": el / n,
+                              "stream_steps_per_s": wl.streams * n / (el / 1e3), "gbs": gbs,
+                              "frac": gbs / peak, "peak": f"{peak} ({peak_kind})",
+                              "status": max((h.sync_status() for h in st.handles), key=abs)}), flush=True)
+            st.close()
+            del st
+            torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -558,9 +607,15 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-streams", type=int, default=256, help="streams per step of the reference arm")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
+    ap.add_argument("--sweep", action="store_true", help="time every workload family (one JSON line each)")
+    ap.add_argument("--sweep-only", default="", help="comma-separated workloads for --sweep")
+    ap.add_argument("--splits", type=int, default=0, help="--sweep: force this many work items per stream")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.sweep:
+        run_sweep(args)
+        return
     rank, ws = dist_setup()
     res = run_reference(args, rank, ws) if args.impl == "reference" else run_ours(args, rank, ws)
     if rank == 0 and res is not None:

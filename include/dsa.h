@@ -103,7 +103,8 @@ int dsa_prefill(dsa_handle h, const void *K, const void *V, void *stream);
  *     evicted at this step once t >= N_r: "K[t - N_r] <- empty");
  *   - attend q over the prompt rows plus the attended window entries
  *     idx = window - skip_idx; softmax and the weighted sum of V in fp32
- *     (split across CTAs when a stream is long);
+ *     (a long stream, or one of few streams, is split over several warps
+ *     whose partial results a second, small kernel merges);
  *   - in phase 2 (N_att - 1 <= t <= N_r - 2, sink removed) append the
  *     attended decode entry with the lowest logit q.k to the skip set (ties:
  *     the oldest); the entry is skipped from step t + 1 on.  The skip set is
@@ -199,15 +200,15 @@ int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out);
  *   mask     [heads, ceil((N_r - sink) / 32)] uint32, all zero before t = 0
  *   last_sel [heads] int32, written on selection steps
  *   q, k_new, v_new, out  as for dsa_decode_step.
- * The split partials, split tickets and a status word live in a static
- * 4 MiB device array of this library (every GPU that loads the library holds
- * it until the process exits).  Workloads whose splits would need more
- * (about 7,800 streams at head_dim 128 without splits, fewer with splits)
- * are rejected with DSA_ERR_ARG and a message.  The first call on a device
+ * The split partials and a status word live in a static 4 MiB device array
+ * of this library (every GPU that loads the library holds it until the
+ * process exits).  Workloads whose splits would need more (about 7,900
+ * streams at head_dim 128 without splits, fewer with splits) are rejected
+ * with DSA_ERR_ARG and a message.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress): make that
  * first call before any stream capture.  Every call shares the array and
- * clears its tickets and status word when it starts, so calls that overlap
- * on the GPU (other streams, other threads) race: order them on one stream.
+ * clears its status word when it starts, so calls that overlap on the GPU
+ * (other streams, other threads) race: order them on one stream.
  * Device-side errors (a bounded wait that gave up) are not reported by this
  * entry point.  Asynchronous on `stream`.
  */
