@@ -70,10 +70,16 @@ constexpr uint32_t kDefaultWaitLimit = 0xffffffffu;
 
 int elem_bytes(int dtype) { return dtype == DSA_F32 ? 4 : 2; }
 
-// Stage rows and the rows-per-item limit of the kernel (8 KB stages, at most
-// 512 decode rows listed per work item).
-int stage_rows(int dtype, int D) { return 8192 / (2 * D * elem_bytes(dtype)); }
-constexpr int kChunkMax = 512;
+// Stage rows and the rows-per-item limit of pipeline shape sh (a multiple of
+// the stage rows, so that items end on stage boundaries).
+int stage_bytes(int sh) { return sh == 0 ? dsa::Pipe<0>::STAGE_BYTES : dsa::Pipe<1>::STAGE_BYTES; }
+int stage_rows(int dtype, int D, int sh) { return stage_bytes(sh) / (2 * D * elem_bytes(dtype)); }
+int chunk_cap(int dtype, int D, int sh)
+{
+    const int rows = stage_rows(dtype, D, sh);
+    const int cap = sh == 0 ? dsa::Pipe<0>::CHUNK_MAX : dsa::Pipe<1>::CHUNK_MAX;
+    return cap / rows * rows;
+}
 constexpr int kWarpsPerCta = DSA_WARPS;
 
 }  // namespace
@@ -85,8 +91,10 @@ struct dsa_ctx {
     int t;
     int prefilled;
     int last_select;
-    int device, sm_count, ctas_per_sm;
+    int device, sm_count;
+    int ctas_per_sm[dsa::kPipes];  // resident CTAs per SM of each pipeline shape (0: unavailable)
     int forced_split;
+    int forced_pipe;  // 0: automatic, else pipeline shape + 1
     int pstride;
     uint32_t wait_limit;
     void *prefix, *ring;
@@ -118,27 +126,82 @@ int validate(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int
 }
 
 struct Plan {
-    int phase, tin, P, a, wlen, select, sinkmode, n, nsplit, chunk, nitems, grid;
+    int phase, tin, P, a, wlen, select, sinkmode, n, nsplit, chunk, nitems, grid, shape;
+    long long rounds, stages;
     unsigned long long bytes;
 };
 
-// Work items per stream.  Splitting a stream costs a partial write and a
-// merge; it pays when the streams alone leave most warps idle (each warp
-// streams its rows through a short pipeline, so few warps cannot keep HBM
-// busy).  Streams are split into about resident-warps / streams pieces (one
-// round of items) once they fill at most half the warps, with at least two
-// stages of rows per piece; streams longer than kChunkMax rows always split.
-int auto_splits(const dsa_ctx *h, int n)
+long long resident_warps(const dsa_ctx *h, int sh) { return (long long)h->sm_count * h->ctas_per_sm[sh] * kWarpsPerCta; }
+
+// Work items per stream under pipeline shape sh.  Splitting a stream costs a
+// partial write and a merge; it pays when the streams alone leave most warps
+// idle (each warp streams its rows through a short pipeline, so few warps
+// cannot keep HBM busy).  Streams are split into about resident-warps /
+// streams pieces (one round of items) once they fill at most half the warps,
+// with at least two stages of rows per piece; streams longer than an item's
+// row limit always split.
+int auto_splits(const dsa_ctx *h, int n, int sh)
 {
-    const int rows = stage_rows(h->dtype, h->D);
-    const int need = (n + kChunkMax - 1) / kChunkMax;
-    const long long warps = (long long)h->sm_count * h->ctas_per_sm * kWarpsPerCta;
+    const int rows = stage_rows(h->dtype, h->D, sh);
+    const int cap = chunk_cap(h->dtype, h->D, sh);
+    const int need = (n + cap - 1) / cap;
+    const long long warps = resident_warps(h, sh);
     const int want = 2LL * h->S <= warps ? (int)(warps / h->S) : 1;
     const int by_rows = n / (2 * rows) > 1 ? n / (2 * rows) : 1;
     const int ns = want < by_rows ? want : by_rows;
     return ns > need ? ns : need;
 }
 
+// Items, grid and cost of pipeline shape sh for a step of n rows per stream.
+void shape_plan(const dsa_ctx *h, int sh, Plan &p)
+{
+    const int rows = stage_rows(h->dtype, h->D, sh);
+    const int cap = chunk_cap(h->dtype, h->D, sh);
+    int ns = h->forced_split > 0 ? h->forced_split : auto_splits(h, p.n, sh);
+    const int need = (p.n + cap - 1) / cap;
+    if (ns < need) ns = need;
+    if (ns > p.n) ns = p.n;
+    int chunk = (p.n + ns - 1) / ns;
+    chunk = (chunk + rows - 1) / rows * rows;
+    if (chunk > cap) chunk = cap;
+    p.shape = sh;
+    p.chunk = chunk;
+    p.nsplit = (p.n + chunk - 1) / chunk;
+    p.nitems = p.nsplit * h->S;
+    // Give every warp the same number of items: with k = ceil(items / resident
+    // warps) rounds of items, use just enough warps for k items each, so no
+    // warp runs a round that most others do not.
+    const long long max_warps = resident_warps(h, sh);
+    p.rounds = (p.nitems + max_warps - 1) / max_warps;
+    const long long warps = (p.nitems + p.rounds - 1) / p.rounds;
+    p.grid = (int)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
+    // A warp's run time is its rounds times the stages of one item, each
+    // stage about one copy latency over the NBUF stages in flight.
+    const int item_rows = chunk < p.n ? chunk : p.n;
+    p.stages = p.rounds * ((item_rows + rows - 1) / rows);
+}
+
+// Cost model of a launch, in loaded copy latencies: a launch is bound either
+// by HBM bandwidth (its bytes over the HBM rate) or by the stages each warp
+// waits on in sequence (rounds x stages per item, one loaded copy latency
+// each).  Measured on GB300 (152 SMs): one loaded latency is about 1.6 us
+// and HBM streams about 6.7 TB/s, so a launch is bandwidth bound once it
+// moves more than about kBytesPerLatency per stage it runs in sequence; the
+// 6 KB stages of shape 1 stream about 5 % slower than shape 0 when
+// bandwidth bound (more stage waits per byte).
+constexpr double kBytesPerLatency = 10.5e6;
+constexpr double kShapeRate[dsa::kPipes] = {1.0, 0.95};
+
+double launch_cost(const Plan &p)
+{
+    const double bw = (double)p.bytes / (kBytesPerLatency * kShapeRate[p.shape]);
+    return bw > (double)p.stages ? bw : (double)p.stages;
+}
+
+// The pipeline shape of a step: the one the cost model above finishes first
+// (shape 0 on a tie).  Both shapes hold about the same bytes in flight per
+// SM; shape 1 wins where its extra warps take the streams in fewer rounds,
+// shape 0 where the launch is bandwidth bound either way.
 Plan make_plan(const dsa_ctx *h, int t)
 {
     Plan p{};
@@ -161,29 +224,33 @@ Plan make_plan(const dsa_ctx *h, int t)
         p.sinkmode = 0;
     }
     p.n = p.P + p.a;
-    const int rows = stage_rows(h->dtype, h->D);
-    int ns = h->forced_split > 0 ? h->forced_split : auto_splits(h, p.n);
-    const int need = (p.n + kChunkMax - 1) / kChunkMax;
-    if (ns < need) ns = need;
-    if (ns > p.n) ns = p.n;
-    int chunk = (p.n + ns - 1) / ns;
-    chunk = (chunk + rows - 1) / rows * rows;
-    if (chunk > kChunkMax) chunk = kChunkMax;
-    p.chunk = chunk;
-    p.nsplit = (p.n + chunk - 1) / chunk;
-    p.nitems = p.nsplit * h->S;
-    // Give every warp the same number of items: with k = ceil(items / resident
-    // warps) rounds of items, use just enough warps for k items each, so no
-    // warp runs a round that most others do not.
-    const long long max_warps = (long long)h->sm_count * h->ctas_per_sm * kWarpsPerCta;
-    const long long rounds = (p.nitems + max_warps - 1) / max_warps;
-    const long long warps = (p.nitems + rounds - 1) / rounds;
-    p.grid = (int)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
     const unsigned long long De = (unsigned long long)h->D * elem_bytes(h->dtype);
     // K and V rows read (current token through k_new/v_new) + q + k_new, v_new
     // read + new entry written + out written.
     p.bytes = (unsigned long long)h->S * (2 * De * (unsigned long long)(p.n - 1) + 6 * De);
+    if (h->forced_pipe > 0) {
+        shape_plan(h, h->forced_pipe - 1, p);
+    } else {
+        shape_plan(h, 0, p);
+        if (h->ctas_per_sm[1] > 0) {
+            Plan q = p;
+            shape_plan(h, 1, q);
+            if (launch_cost(q) < launch_cost(p)) p = q;
+        }
+    }
     return p;
+}
+
+// The most work items per stream any step takes (steps from N_att - 1 on
+// all attend the same row count), so that partials are sized once.
+int max_splits(const dsa_ctx *h)
+{
+    int m = 1;
+    for (int t = 0; t < h->N_att; ++t) {
+        const int ns = make_plan(h, t).nsplit;
+        m = ns > m ? ns : m;
+    }
+    return m;
 }
 
 int ensure_partials(dsa_ctx *h, int nsplit)
@@ -254,35 +321,50 @@ int encode_ring_map(dsa_ctx *h)
     return DSA_OK;
 }
 
-template <typename T, int D>
+template <typename T, int D, int SH>
 int occupancy()
 {
-    using C = dsa::KCfg<T, D>;
+    using C = dsa::KCfg<T, D, SH>;
     static int cached = -1;
     if (cached < 0) {
-        cudaError_t e = cudaFuncSetAttribute(dsa::decode_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaError_t e =
+            cudaFuncSetAttribute(dsa::decode_kernel<T, D, SH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return -1;
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dsa::decode_kernel<T, D>, C::THREADS, C::SMEM);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dsa::decode_kernel<T, D, SH>, C::THREADS, C::SMEM);
         if (e != cudaSuccess) return -1;
         cached = n;
     }
     return cached;
 }
 
-int occupancy_for(int dtype, int D)
+template <int SH>
+int occupancy_sh(int dtype, int D)
 {
-    if (dtype == DSA_BF16) return D == 64 ? occupancy<__nv_bfloat16, 64>() : occupancy<__nv_bfloat16, 128>();
-    return D == 64 ? occupancy<float, 64>() : occupancy<float, 128>();
+    if (dtype == DSA_BF16) return D == 64 ? occupancy<__nv_bfloat16, 64, SH>() : occupancy<__nv_bfloat16, 128, SH>();
+    return D == 64 ? occupancy<float, 64, SH>() : occupancy<float, 128, SH>();
+}
+
+// Resident CTAs per SM of both pipeline shapes; shape 0 must be launchable.
+int query_occupancy(int dtype, int D, int *ctas)
+{
+    ctas[0] = occupancy_sh<0>(dtype, D);
+    if (ctas[0] < 1) return cuda_fail(cudaGetLastError(), "kernel occupancy query (is this an sm_103 device?)");
+    ctas[1] = occupancy_sh<1>(dtype, D);
+    if (ctas[1] < 1) {
+        ctas[1] = 0;
+        cudaGetLastError();
+    }
+    return DSA_OK;
 }
 
 // Launches the decode kernel as a programmatic dependent launch: its CTAs
 // may start while the previous kernel in the stream finishes; the kernel
 // itself waits for that kernel before it reads inputs or writes anything.
-template <typename T, int D>
+template <typename T, int D, int SH>
 cudaError_t launch_decode(const dsa::DecodeParams &p, const CUtensorMap &map, int grid, cudaStream_t st)
 {
-    using C = dsa::KCfg<T, D>;
+    using C = dsa::KCfg<T, D, SH>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(C::THREADS);
@@ -293,7 +375,7 @@ cudaError_t launch_decode(const dsa::DecodeParams &p, const CUtensorMap &map, in
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dsa::decode_kernel<T, D>, p, map);
+    return cudaLaunchKernelEx(&cfg, dsa::decode_kernel<T, D, SH>, p, map);
 }
 
 template <typename T, int D>
@@ -312,14 +394,22 @@ cudaError_t launch_merge(const dsa::DecodeParams &p, cudaStream_t st)
     return cudaLaunchKernelEx(&cfg, dsa::merge_kernel<T, D>, p);
 }
 
-// Decode launch plus, when streams are split, the merge launch.
-cudaError_t launch_step(int dtype, int D, const dsa::DecodeParams &p, const CUtensorMap &map, int grid, cudaStream_t st)
+template <int SH>
+cudaError_t launch_decode_sh(int dtype, int D, const dsa::DecodeParams &p, const CUtensorMap &map, int grid,
+                             cudaStream_t st)
 {
-    cudaError_t e;
     if (dtype == DSA_BF16)
-        e = D == 64 ? launch_decode<__nv_bfloat16, 64>(p, map, grid, st) : launch_decode<__nv_bfloat16, 128>(p, map, grid, st);
-    else
-        e = D == 64 ? launch_decode<float, 64>(p, map, grid, st) : launch_decode<float, 128>(p, map, grid, st);
+        return D == 64 ? launch_decode<__nv_bfloat16, 64, SH>(p, map, grid, st)
+                       : launch_decode<__nv_bfloat16, 128, SH>(p, map, grid, st);
+    return D == 64 ? launch_decode<float, 64, SH>(p, map, grid, st) : launch_decode<float, 128, SH>(p, map, grid, st);
+}
+
+// Decode launch plus, when streams are split, the merge launch.
+cudaError_t launch_step(int dtype, int D, int shape, const dsa::DecodeParams &p, const CUtensorMap &map, int grid,
+                        cudaStream_t st)
+{
+    cudaError_t e = shape == 0 ? launch_decode_sh<0>(dtype, D, p, map, grid, st)
+                               : launch_decode_sh<1>(dtype, D, p, map, grid, st);
     if (e != cudaSuccess || p.nsplit == 1) return e;
     if (dtype == DSA_BF16)
         return D == 64 ? launch_merge<__nv_bfloat16, 64>(p, st) : launch_merge<__nv_bfloat16, 128>(p, st);
@@ -428,11 +518,12 @@ int dsa_create_ex(int heads, int head_dim, int L_p, int N_r, int N_att, int sink
         free_ctx(h);
         return cuda_fail(e, "cudaDeviceGetAttribute");
     }
-    h->ctas_per_sm = occupancy_for(dtype, head_dim);
-    if (h->ctas_per_sm < 1) {
+    rc = query_occupancy(dtype, head_dim, h->ctas_per_sm);
+    if (rc != DSA_OK) {
+        std::string msg = g_err;
         free_ctx(h);
-        e = cudaGetLastError();
-        return cuda_fail(e, "kernel occupancy query (is this an sm_103 device?)");
+        g_err = msg;
+        return rc;
     }
 
     const size_t row = 2 * (size_t)head_dim * elem_bytes(dtype);
@@ -442,7 +533,7 @@ int dsa_create_ex(int heads, int head_dim, int L_p, int N_r, int N_att, int sink
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->mask, S * h->MW * 4, "skip mask");
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->last_sel, S * 4, "last selection");
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->status, 16, "status word");
-    if (rc == DSA_OK) rc = ensure_partials(h, auto_splits(h, L_p + N_att));
+    if (rc == DSA_OK) rc = ensure_partials(h, max_splits(h));
     if (rc == DSA_OK) rc = encode_ring_map(h);
     if (rc != DSA_OK) {
         std::string msg = g_err;
@@ -513,6 +604,7 @@ int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out)
     out->nsplit = p.nsplit;
     out->chunk = p.chunk;
     out->grid = p.grid;
+    out->pipeline = p.shape + 1;
     out->algo_bytes = p.bytes;
     return DSA_OK;
 }
@@ -565,7 +657,7 @@ int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *
 
     cudaStream_t st = (cudaStream_t)stream;
     p.early = note_launch(st, h) ? 1 : 0;
-    cudaError_t e = launch_step(h->dtype, h->D, p, h->ring_map, pl.grid, st);
+    cudaError_t e = launch_step(h->dtype, h->D, pl.shape, p, h->ring_map, pl.grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     h->last_select = pl.select;
     h->t += 1;
@@ -626,6 +718,16 @@ int dsa_set_splits(dsa_handle h, int nsplit)
         if (rc != DSA_OK) return rc;
     }
     h->forced_split = nsplit;
+    return DSA_OK;
+}
+
+int dsa_set_pipeline(dsa_handle h, int pipeline)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (pipeline < 0 || pipeline > dsa::kPipes) return fail(DSA_ERR_ARG, "pipeline must be 0, 1 or 2 (got %d)", pipeline);
+    if (pipeline > 0 && h->ctas_per_sm[pipeline - 1] < 1)
+        return fail(DSA_ERR_ARG, "pipeline %d cannot be launched on this device", pipeline);
+    h->forced_pipe = pipeline;
     return DSA_OK;
 }
 
@@ -714,8 +816,9 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     int sms = 0;
     rc = noalloc_setup(&scratch, &sms);
     if (rc != DSA_OK) return rc;
-    const int occ = occupancy_for(dtype, head_dim);
-    if (occ < 1) return cuda_fail(cudaGetLastError(), "kernel occupancy query (is this an sm_103 device?)");
+    int occ[dsa::kPipes];
+    rc = query_occupancy(dtype, head_dim, occ);
+    if (rc != DSA_OK) return rc;
 
     // A handle-shaped description of the caller's state; nothing is allocated.
     dsa_ctx h{};
@@ -732,7 +835,8 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     h.Lcap = L_p + sink;
     h.MW = (h.R + 31) / 32;
     h.sm_count = sms;
-    h.ctas_per_sm = occ;
+    h.ctas_per_sm[0] = occ[0];
+    h.ctas_per_sm[1] = occ[1];
     h.prefix = prefix;
     h.ring = ring;
     Plan pl = make_plan(&h, t);
@@ -797,7 +901,7 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.qscale = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
     p.wait_limit = kDefaultWaitLimit;
     p.early = 0;  // caller-owned state: the previous kernel may have written it
-    e = launch_step(dtype, head_dim, p, h.ring_map, pl.grid, st);
+    e = launch_step(dtype, head_dim, pl.shape, p, h.ring_map, pl.grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return DSA_OK;
 }

@@ -198,8 +198,13 @@ struct Elem<__nv_bfloat16> {
     }
 };
 
-// Pipeline shape (compile-time): independent warps per CTA and 8 KB
-// shared-memory stages per warp.
+// Pipeline shapes (compile-time): independent warps per CTA, shared-memory
+// stages per warp, and the decode rows one work item may list.  Shape 0
+// (8 KB stages, 512-row items, three CTAs of 4 warps per SM) keeps the most
+// bytes in flight per warp; shape 1 (6 KB stages, 256-row items, four CTAs
+// per SM) has a third more warps, so more streams (or pieces of streams) run
+// in one round.  Both hold about the same bytes in flight per SM; the host
+// picks one per launch.
 #ifndef DSA_WARPS
 #define DSA_WARPS 4
 #endif
@@ -207,7 +212,22 @@ struct Elem<__nv_bfloat16> {
 #define DSA_NBUF 2
 #endif
 
-template <typename T, int D>
+constexpr int kPipes = 2;
+
+template <int SH>
+struct Pipe;
+template <>
+struct Pipe<0> {
+    static constexpr int STAGE_BYTES = 8192;
+    static constexpr int CHUNK_MAX = 512;
+};
+template <>
+struct Pipe<1> {
+    static constexpr int STAGE_BYTES = 6144;
+    static constexpr int CHUNK_MAX = 256;
+};
+
+template <typename T, int D, int SH>
 struct KCfg {
     static constexpr int E = sizeof(T);
     static constexpr int VEC = Elem<T>::VEC;   // elements per 16-byte vector
@@ -217,11 +237,11 @@ struct KCfg {
     static constexpr int ROW = 2 * KROW;       // bytes of a K|V entry
     static constexpr int WARPS = DSA_WARPS;
     static constexpr int THREADS = 32 * WARPS;
-    static constexpr int STAGE_BYTES = 8192;
+    static constexpr int STAGE_BYTES = Pipe<SH>::STAGE_BYTES;
     static constexpr int SROWS = STAGE_BYTES / ROW;  // entries per stage
     static constexpr int NIT = SROWS / RPW;          // warp instructions per stage
     static constexpr int NBUF = DSA_NBUF;            // stages per warp
-    static constexpr int CHUNK_MAX = 512;            // decode ranks per work item
+    static constexpr int CHUNK_MAX = Pipe<SH>::CHUNK_MAX;  // decode ranks per work item
     static constexpr int MAXW = 8;                   // mask words per lane kept in registers
     static constexpr int OFF_BAR = NBUF * STAGE_BYTES;
     static constexpr int OFF_LIST = OFF_BAR + NBUF * 8;
@@ -230,6 +250,7 @@ struct KCfg {
     static_assert(LPR >= 2 && LPR <= 16 && 32 % LPR == 0, "row must span a power-of-two lane group");
     static_assert(SROWS % RPW == 0 && NIT >= 1, "stage rows must fill whole warp instructions");
     static_assert(ROW % 128 == 0 || ROW == 256, "gather destinations must stay 128-byte aligned");
+    static_assert(STAGE_BYTES % 128 == 0 && CHUNK_MAX <= 65536, "stage buffers stay 128-byte aligned");
 };
 
 // Bits of mask word w that are attended window offsets (clear and < wlen);
@@ -251,13 +272,13 @@ __device__ __forceinline__ bool better(float v, int r, float bv, int br)
 // scan over the stream's mask words, prefetched one item ahead), streams the
 // prompt rows (bulk copies) and the attended ring rows (TMA tile::gather4
 // through `tmap`, or contiguous bulk runs when nothing can be skipped)
-// through its own NBUF shared-memory stages, reads q and the current token
+// through its own NBUF shared-memory stages (pipeline shape SH), reads q and the current token
 // straight into registers, and ends with a warp-shuffle combine.
-template <typename T, int D>
-__global__ void __launch_bounds__(KCfg<T, D>::THREADS) decode_kernel(const DecodeParams p,
-                                                                      const __grid_constant__ CUtensorMap tmap)
+template <typename T, int D, int SH>
+__global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const DecodeParams p,
+                                                                          const __grid_constant__ CUtensorMap tmap)
 {
-    using C = KCfg<T, D>;
+    using C = KCfg<T, D, SH>;
     using EL = Elem<T>;
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;

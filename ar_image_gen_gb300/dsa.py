@@ -41,14 +41,15 @@ STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_ARG", -2: "DSA_ERR_STATE", -3: "DSA_ER
 
 EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa_destroy", "dsa_get_step",
            "dsa_get_skip_mask", "dsa_get_last_selection", "dsa_sync_status", "dsa_last_error",
-           "dsa_state_bytes", "dsa_plan_step", "dsa_set_splits", "dsa_set_wait_limit",
+           "dsa_state_bytes", "dsa_plan_step", "dsa_set_splits", "dsa_set_pipeline", "dsa_set_wait_limit",
            "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc"]
 
 
 class dsa_step_plan(ctypes.Structure):
     _fields_ = [("phase", ctypes.c_int), ("t_inner", ctypes.c_int), ("n_prefix", ctypes.c_int),
                 ("n_decode", ctypes.c_int), ("select", ctypes.c_int), ("nsplit", ctypes.c_int),
-                ("chunk", ctypes.c_int), ("grid", ctypes.c_int), ("algo_bytes", ctypes.c_ulonglong)]
+                ("chunk", ctypes.c_int), ("grid", ctypes.c_int), ("pipeline", ctypes.c_int),
+                ("algo_bytes", ctypes.c_ulonglong)]
 
 
 _P = ctypes.c_void_p
@@ -67,6 +68,7 @@ _L.dsa_state_bytes.argtypes = [_I] * 6
 _L.dsa_state_bytes.restype = ctypes.c_size_t
 _L.dsa_plan_step.argtypes = [_P, _I, ctypes.POINTER(dsa_step_plan)]
 _L.dsa_set_splits.argtypes = [_P, _I]
+_L.dsa_set_pipeline.argtypes = [_P, _I]
 _L.dsa_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
 _L.dsa_debug_fail_alloc_after.argtypes = [_I]
 _L.dsa_decode_step_noalloc.argtypes = [_I] * 8 + [_P] * 9
@@ -173,6 +175,10 @@ def dsa_set_splits(h, nsplit) -> int:
     return _L.dsa_set_splits(h, nsplit)
 
 
+def dsa_set_pipeline(h, pipeline) -> int:
+    return _L.dsa_set_pipeline(h, pipeline)
+
+
 def dsa_set_wait_limit(h, limit) -> int:
     return _L.dsa_set_wait_limit(h, limit)
 
@@ -244,6 +250,9 @@ class DSA:
 
     def set_splits(self, nsplit: int):
         _check(dsa_set_splits(self.h, nsplit), "dsa_set_splits")
+
+    def set_pipeline(self, pipeline: int):
+        _check(dsa_set_pipeline(self.h, pipeline), "dsa_set_pipeline")
 
     def set_wait_limit(self, limit: int):
         _check(dsa_set_wait_limit(self.h, limit), "dsa_set_wait_limit")

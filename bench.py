@@ -462,12 +462,13 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": workload_config(wl, f"phase-3 steady state from t = {t_start}"),
         "hbm_gbs": whole,
-        "roofline": {"bound": "hbm", "kernel": "dsa::decode_kernel<bf16,128>", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": f"dsa::decode_kernel<bf16,128,{plan.pipeline - 1}>",
+                     "achieved": achieved,
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algo_bytes_per_launch": plan.algo_bytes, "launch_ms": per_launch_ms,
                      "isolated_launch_ms": isolated_ms,
-                     "grid": plan.grid, "nsplit": plan.nsplit},
+                     "grid": plan.grid, "nsplit": plan.nsplit, "pipeline": plan.pipeline},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
         "gpu_launches": launches,
@@ -570,9 +571,11 @@ def run_sweep(args) -> None:
                 wl = wl.with_batch(32)  # dense KV of this size: 4.3 GB per layer at batch 32
             steps = max(8, min(args.steps, 40))
             st = Stack(wl, pool_steps=4)
-            if args.splits:
-                for h in st.handles:
+            for h in st.handles:
+                if args.splits:
                     h.set_splits(args.splits)
+                if args.pipeline:
+                    h.set_pipeline(args.pipeline)
             t0 = (wl.L_dec - steps) if dense else wl.N_r + wl.sink
             st.make_pool(min(t0, wl.L_dec - 1))
             st.advance(t0, generate=False)
@@ -584,6 +587,7 @@ def run_sweep(args) -> None:
             gbs = nbytes / (el / 1e3) / 1e9
             print(json.dumps({"workload": wl.name, "dense": dense, "streams": wl.streams, "layers": wl.layers,
                               "rows_per_stream": plan.n_prefix + plan.n_decode, "nsplit": plan.nsplit,
+                              "pipeline": plan.pipeline, "grid": plan.grid,
                               "steps": f"{t_first}..{t_first + steps - 1}", "ms_per_launch": el / n,
                               "stream_steps_per_s": wl.streams * n / (el / 1e3), "gbs": gbs,
                               "frac": gbs / peak, "peak": f"{peak} ({peak_kind})",
@@ -610,6 +614,7 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="time every workload family (one JSON line each)")
     ap.add_argument("--sweep-only", default="", help="comma-separated workloads for --sweep")
     ap.add_argument("--splits", type=int, default=0, help="--sweep: force this many work items per stream")
+    ap.add_argument("--pipeline", type=int, default=0, help="--sweep: force this pipeline shape (1 or 2)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -173,9 +173,10 @@ typedef struct dsa_step_plan {
     int n_prefix;              /* always-attended rows (prompt plus sinks) */
     int n_decode;              /* attended decode rows, current token included */
     int select;                /* 1 if this step appends to the skip set */
-    int nsplit;                /* CTAs per stream */
-    int chunk;                 /* rows per CTA */
-    int grid;                  /* CTAs launched */
+    int nsplit;                /* work items (pieces) per stream */
+    int chunk;                 /* rows per work item */
+    int grid;                  /* CTAs of the decode launch */
+    int pipeline;              /* pipeline shape of the launch (1 or 2, see dsa_set_pipeline) */
     unsigned long long algo_bytes;
 } dsa_step_plan;
 
@@ -218,15 +219,24 @@ int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r, int N_att
 
 /* Tuning and test knobs (not needed for normal use). */
 
-/* Force the number of CTAs per stream (>= 1), or 0 for the automatic
- * choice.  Grows the partial buffers if needed (allocates; not on the
- * decode path). */
+/* Force the number of work items (pieces) per stream (>= 1), or 0 for the
+ * automatic choice.  Grows the partial buffers if needed (allocates; not on
+ * the decode path). */
 int dsa_set_splits(dsa_handle h, int nsplit);
 
-/* Iteration limit of the bounded waits inside the decode kernel (default
- * about 2^22).  A limit of 0 makes every wait give up at once; the kernel
- * then records DSA_ERR_TIMEOUT, lets its own copies land and returns.  Used
- * to test the timeout path without a real hang. */
+/* Force the pipeline shape of the decode kernel, or 0 for the automatic
+ * choice per step.  1: 8 KB shared-memory stages per warp and at most 512
+ * decode rows per work item; 2: 6 KB stages, at most 256 rows per item and
+ * a third more resident warps.  Results do not depend on the shape beyond
+ * fp32 rounding order (selections are identical).  DSA_ERR_ARG for other
+ * values or a shape the device cannot launch. */
+int dsa_set_pipeline(dsa_handle h, int pipeline);
+
+/* Poll limit of the bounded waits inside the decode kernel (default: none;
+ * every wait still gives up after about one second).  A limit of 0 makes
+ * every wait give up at once; the kernel then records DSA_ERR_TIMEOUT, lets
+ * its own copies land and returns.  Used to test the timeout path without a
+ * real hang. */
 int dsa_set_wait_limit(dsa_handle h, uint32_t limit);
 
 /* Make the n-th following device allocation of this library fail (n >= 1),

@@ -56,7 +56,7 @@ def mask_offsets(words: np.ndarray) -> set[int]:
 
 def run_parity(wl: Workload, steps: int | None = None, sample: list[int] | None = None,
                splits: int = 0, mask_every: int = 1, layer: int = 0, device: str = "cuda",
-               gen_device: str | None = None, threads: int = 1) -> ParityReport:
+               gen_device: str | None = None, threads: int = 1, pipeline: int = 0) -> ParityReport:
     """Runs `steps` decode steps of one layer of `wl` on the GPU and the
     sampled streams on the oracle; returns the report (does not raise)."""
     from ar_image_gen_gb300.dsa import DSA
@@ -71,6 +71,8 @@ def run_parity(wl: Workload, steps: int | None = None, sample: list[int] | None 
     h = DSA(S, d, wl.L_p, wl.N_r, wl.N_att, wl.sink, wl.dtype)
     if splits:
         h.set_splits(splits)
+    if pipeline:
+        h.set_pipeline(pipeline)
     orc = OracleBatch(len(sample), d, wl.L_p, wl.N_r, wl.N_att, wl.sink)
 
     Kp, Vp = gen.prompt()

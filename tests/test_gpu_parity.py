@@ -64,10 +64,52 @@ def test_small_parity(name):
     assert rep.steps == steps
 
 
-def test_split_count_does_not_change_the_result():
+# Both pipeline shapes forced on cases that reach their limits: ragged
+# splits, the sink fill, dense runs, fp32 rows of 1 KB (six-row stages in
+# shape 2) and windows longer than one item's row list (256 rows in shape 2).
+PIPE_CASES = ["ragged-split3", "sink4", "dense-split3", "f32-d128", "f32-d64-split4", "bf16-d64",
+              "window-wider-than-a-stage-list", "long-prompt-split2"]
+
+
+@pytest.mark.parametrize("pipeline", [1, 2])
+@pytest.mark.parametrize("name", PIPE_CASES)
+def test_small_parity_each_pipeline(name, pipeline):
+    wl, steps, splits = CASES[name]
+    rep = run_parity(wl, steps=steps, splits=splits, pipeline=pipeline)
+    assert rep.ok, rep.summary()
+    assert rep.steps == steps
+
+
+def test_pipeline_choice_is_reported():
+    """The automatic plan takes shape 2 where shape 1 would need a second
+    round of items (more streams than shape 1's resident warps, a launch
+    bound by copy latency) and shape 1 where both run two rounds of a short
+    stream and the launch is bandwidth bound."""
+    from ar_image_gen_gb300.dsa import DSA
+
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # one round in shape 2 (16 warps per SM), two in shape 1 (12 per SM)
+    h = DSA(14 * sms, 128, 64, 512, 51, 0, "bf16")
+    p = h.plan(600)
+    assert (p.pipeline, p.nsplit) == (2, 1), (p.pipeline, p.nsplit)
+    h.close()
+    # two rounds in either shape of a 93-row stream: fewer, larger stages win
+    h = DSA(20 * sms, 128, 64, 288, 29, 0, "bf16")
+    p = h.plan(400)
+    assert (p.pipeline, p.nsplit) == (1, 1), (p.pipeline, p.nsplit)
+    h.set_pipeline(2)
+    assert h.plan(400).pipeline == 2
+    h.set_pipeline(0)
+    assert h.plan(400).pipeline == 1
+    h.close()
+
+
+@pytest.mark.parametrize("pipeline", [1, 2])
+def test_split_count_does_not_change_the_result(pipeline):
     """The argmin is a total order on (logit, offset), and each logit is
-    computed by the same lanes whatever the split: selections are identical
-    across split counts and outputs agree to rounding."""
+    computed by the same lanes whatever the split or the pipeline shape:
+    selections are identical across split counts and shapes and outputs
+    agree to rounding."""
     from ar_image_gen_gb300.dsa import DSA
     from ar_image_gen_gb300.synth import TraceGen
 
@@ -77,6 +119,7 @@ def test_split_count_does_not_change_the_result():
     results = []
     for ns in (1, 2, 5):
         h = DSA(wl.streams, 128, wl.L_p, wl.N_r, wl.N_att, 0, "bf16")
+        h.set_pipeline(pipeline)
         h.set_splits(ns)
         h.prefill(Kp, Vp)
         out = torch.empty((wl.streams, 128), dtype=torch.bfloat16, device="cuda")
