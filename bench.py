@@ -267,6 +267,12 @@ class Stack:
             t = min(t0 + i, self.wl.L_dec - 1)
             self.pool.append([self.gens[layer].step(t) for layer in range(self.wl.layers)])
 
+    def reprefill(self):
+        """Prefills every layer again (t = 0, empty skip sets)."""
+        for layer, h in enumerate(self.handles):
+            Kp, Vp = self.gens[layer].prompt()
+            h.prefill(Kp, Vp)
+
     def close(self):
         for h in self.handles:
             h.close()
@@ -304,6 +310,38 @@ def time_steps(stack, steps: int, per_launch: bool):
     el = start.elapsed_time(end)
     per = statistics.fmean(a.elapsed_time(b) for a, b in evs) if evs else None
     return el, per, launches
+
+
+def time_trace(stack, runs: int):
+    """The whole decode trace (steps 0 .. L_dec - 1 of every layer: fill,
+    selection and eviction phases) from a fresh prefill, `runs` times, inputs
+    cycled from the pool.  Returns a summary dict: stream-steps/s and GB/s of
+    algorithmic bytes, mean with min and max over the runs."""
+    import torch
+
+    wl = stack.wl
+    stream = torch.cuda.current_stream()
+    nbytes = sum(stack.handles[0].plan(t).algo_bytes for t in range(wl.L_dec)) * wl.layers
+    times = []
+    for _ in range(runs):
+        stack.reprefill()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for t in range(wl.L_dec):
+            inputs = stack.pool[t % stack.pool_steps]
+            for layer, h in enumerate(stack.handles):
+                q, k, v = inputs[layer]
+                h.decode_step(q, k, v, stack.outs[layer], stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+        times.append(start.elapsed_time(end))
+    rates = [wl.streams * wl.layers * wl.L_dec / (ms / 1e3) for ms in times]
+    gbs = [nbytes / (ms / 1e3) / 1e9 for ms in times]
+    return {"steps": f"0..{wl.L_dec - 1}", "layers": wl.layers, "runs": runs,
+            "value": statistics.fmean(rates), "min": min(rates), "max": max(rates), "unit": UNIT,
+            "hbm_gbs": statistics.fmean(gbs), "ms_per_trace": statistics.fmean(times),
+            "algo_bytes_per_trace": nbytes}
 
 
 def time_e2e(stack, steps: int):
@@ -423,6 +461,12 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     stack.advance(wl.L_dec - 1, generate=False)
     last_sparse_ms = _last_step_ms(stack)
     status = max((h.sync_status() for h in stack.handles), key=abs)
+    # the whole trace, all phases, three runs
+    trace = None
+    if not args.no_trace:
+        trace = time_trace(stack, 3)
+        trace["frac"] = trace["hbm_gbs"] / measured_peak()[0]
+        status = max([status] + [h.sync_status() for h in stack.handles], key=abs)
     stack.close()
     del stack
     torch.cuda.empty_cache()
@@ -474,6 +518,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "last_step": {"sparse_ms": last_sparse_ms},
+        "trace": trace,
         "dense": dense,
         "device_status": status,
     }
@@ -585,13 +630,17 @@ def run_sweep(args) -> None:
             el, _, n = time_steps(st, steps, per_launch=False)
             nbytes = sum(st.handles[0].plan(t_first + i).algo_bytes for i in range(steps)) * wl.layers
             gbs = nbytes / (el / 1e3) / 1e9
-            print(json.dumps({"workload": wl.name, "dense": dense, "streams": wl.streams, "layers": wl.layers,
-                              "rows_per_stream": plan.n_prefix + plan.n_decode, "nsplit": plan.nsplit,
-                              "pipeline": plan.pipeline, "grid": plan.grid,
-                              "steps": f"{t_first}..{t_first + steps - 1}", "ms_per_launch": el / n,
-                              "stream_steps_per_s": wl.streams * n / (el / 1e3), "gbs": gbs,
-                              "frac": gbs / peak, "peak": f"{peak} ({peak_kind})",
-                              "status": max((h.sync_status() for h in st.handles), key=abs)}), flush=True)
+            line = {"workload": wl.name, "dense": dense, "streams": wl.streams, "layers": wl.layers,
+                    "rows_per_stream": plan.n_prefix + plan.n_decode, "nsplit": plan.nsplit,
+                    "pipeline": plan.pipeline, "grid": plan.grid,
+                    "steps": f"{t_first}..{t_first + steps - 1}", "ms_per_launch": el / n,
+                    "stream_steps_per_s": wl.streams * n / (el / 1e3), "gbs": gbs,
+                    "frac": gbs / peak, "peak": f"{peak} ({peak_kind})"}
+            if args.trace:
+                line["trace"] = time_trace(st, 3)
+                line["trace"]["frac"] = line["trace"]["hbm_gbs"] / peak
+            line["status"] = max((h.sync_status() for h in st.handles), key=abs)
+            print(json.dumps(line), flush=True)
             st.close()
             del st
             torch.cuda.empty_cache()
@@ -608,6 +657,7 @@ def main(argv=None):
     ap.add_argument("--dense-steps", type=int, default=16)
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-trace", action="store_true", help="skip the whole-trace timing")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-streams", type=int, default=256, help="streams per step of the reference arm")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
@@ -615,6 +665,7 @@ def main(argv=None):
     ap.add_argument("--sweep-only", default="", help="comma-separated workloads for --sweep")
     ap.add_argument("--splits", type=int, default=0, help="--sweep: force this many work items per stream")
     ap.add_argument("--pipeline", type=int, default=0, help="--sweep: force this pipeline shape (1 or 2)")
+    ap.add_argument("--trace", action="store_true", help="--sweep: also time whole traces (all phases, 3 runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
