@@ -40,6 +40,16 @@
  *     held stays <= N_r + L_p and the attended decode rows stay <= N_att.
  *     With N_att = N_r this is StreamingLLM with `sink` sinks.
  *
+ * FP8 KV storage (orc_set_kv_fp8).  The pages note that KV quantization is
+ * orthogonal to the method and stacks with it, and fix no scheme.  The
+ * reading taken: every K and V row the cache holds (prompt rows, sink rows,
+ * decode rows) is stored as OCP FP8 E4M3 codes with one fp32 scale per
+ * stream for K and one for V; the stored code of an element x is the E4M3
+ * value nearest to fp32(x) * fp32(1 / scale) (ties to the even code, beyond
+ * the largest finite value 448 the value 448: "satfinite"), and attention
+ * uses code * scale.  Everything after the store is the fp64 algorithm
+ * above, unchanged.
+ *
  * Near ties: a caller (the parity test) may pass the position its own
  * implementation selected.  If it differs from the oracle's argmin but its
  * logit is within 1e-4 * max(|a|, |b|, 1) of the minimum logit, the oracle
@@ -83,6 +93,8 @@ typedef struct orc_stream {
     int *skip, n_skip;    /* skip_idx, absolute inner positions, insertion order */
     int *idx, n_idx;      /* idx of the last step */
     int live;             /* decode rows held */
+    int fp8;              /* 1: rows are stored as E4M3 codes (see the header) */
+    float k_scale, v_scale, k_inv, v_inv;
     int mutation;         /* planted mistake for the pin tests; 0 = faithful */
 } orc_stream;
 
@@ -98,8 +110,73 @@ enum {
     MUT_SCALE = 6,           /* logits scaled by 1/d instead of 1/sqrt(d) */
     MUT_SKIP_NOW = 7,        /* the newly selected row is skipped in the same step */
     MUT_BUDGET = 8,          /* one selection too many */
-    MUT_NEWEST_TIE = 9       /* exact ties go to the newest position */
+    MUT_NEWEST_TIE = 9,      /* exact ties go to the newest position */
+    MUT_FP8_SWAP = 10,       /* K rows quantized with the V scale and V rows with the K scale */
+    MUT_FP8_SCALE = 11,      /* codes of x * scale instead of x / scale */
+    MUT_FP8_TRUNC = 12,      /* codes rounded toward zero instead of to nearest */
+    MUT_FP8_PROMPT = 13      /* prompt rows stored unquantized */
 };
+
+/* ---- OCP FP8 E4M3 ("E4M3FN"): 1 sign bit, 4 exponent bits (bias 7), 3
+ * mantissa bits; no infinities, code 0x7F / 0xFF is NaN, so the largest
+ * finite magnitude is 1.75 * 2^8 = 448; exponent field 0 holds the
+ * subnormals m * 2^-9. */
+double orc_e4m3_decode(unsigned char c)
+{
+    const int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return sgn ? -mag : mag;
+}
+
+/* Nearest finite E4M3 value to y by exhaustive search over the 127
+ * non-negative finite codes; an exact midpoint goes to the even code (the
+ * one whose mantissa ends in 0); magnitudes beyond 448 give 448. */
+unsigned char orc_e4m3_encode(float y)
+{
+    if (y != y) return 0x7F;
+    const double a = fabs((double)y);
+    if (a > 448.0) return (unsigned char)(126 | (signbit(y) ? 0x80 : 0));
+    int best = 0;
+    double berr = a;
+    for (int c = 1; c < 127; ++c) {
+        const double err = fabs(orc_e4m3_decode((unsigned char)c) - a);
+        if (err < berr || (err == berr && (c & 1) == 0)) {
+            berr = err;
+            best = c;
+        }
+    }
+    return (unsigned char)(best | (signbit(y) ? 0x80 : 0));
+}
+
+/* Largest-magnitude finite code not above |y| (planted mistake only). */
+static unsigned char e4m3_trunc(float y)
+{
+    const double a = fabs((double)y);
+    int best = 0;
+    for (int c = 1; c < 127; ++c)
+        if (orc_e4m3_decode((unsigned char)c) <= a) best = c;
+    return (unsigned char)(best | (signbit(y) ? 0x80 : 0));
+}
+
+/* A stored row: x unchanged, or code * scale with code = E4M3(fp32(x) * inv).
+ * `prompt` marks rows loaded by the prefill. */
+static void store_row(const orc_stream *st, double *dst, const double *x, int is_v, int prompt)
+{
+    const int m = st->mutation;
+    if (!st->fp8 || (prompt && m == MUT_FP8_PROMPT)) {
+        for (int i = 0; i < st->d; ++i) dst[i] = x[i];
+        return;
+    }
+    const int use_v = (m == MUT_FP8_SWAP) ? !is_v : is_v;
+    const float scale = use_v ? st->v_scale : st->k_scale;
+    const float inv = (m == MUT_FP8_SCALE) ? scale : (use_v ? st->v_inv : st->k_inv);
+    for (int i = 0; i < st->d; ++i) {
+        const float y = (float)x[i] * inv;
+        const unsigned char c = (m == MUT_FP8_TRUNC) ? e4m3_trunc(y) : orc_e4m3_encode(y);
+        dst[i] = orc_e4m3_decode(c) * (double)scale;
+    }
+}
 
 static double dot(const double *a, const double *b, int d)
 {
@@ -139,6 +216,19 @@ void orc_destroy(orc_stream *st)
 
 void orc_set_mutation(orc_stream *st, int m) { st->mutation = m; }
 
+/* Stores rows as E4M3 codes with the given per-stream scales from the next
+ * prefill on.  Returns -1 unless both scales are positive and finite. */
+int orc_set_kv_fp8(orc_stream *st, float k_scale, float v_scale)
+{
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || isinf(k_scale) || isinf(v_scale)) return -1;
+    st->fp8 = 1;
+    st->k_scale = k_scale;
+    st->v_scale = v_scale;
+    st->k_inv = 1.0f / k_scale;
+    st->v_inv = 1.0f / v_scale;
+    return 0;
+}
+
 /* Loads the prompt KV (always attended in full) and resets the decode state. */
 int orc_prefill(orc_stream *st, const double *Kp, const double *Vp)
 {
@@ -146,8 +236,10 @@ int orc_prefill(orc_stream *st, const double *Kp, const double *Vp)
         free(st->K[j]); free(st->V[j]);
         st->K[j] = st->V[j] = NULL;
     }
-    memcpy(st->Kp, Kp, sizeof(double) * (size_t)st->L_p * st->d);
-    memcpy(st->Vp, Vp, sizeof(double) * (size_t)st->L_p * st->d);
+    for (int i = 0; i < st->L_p; ++i) {
+        store_row(st, st->Kp + (size_t)i * st->d, Kp + (size_t)i * st->d, 0, 1);
+        store_row(st, st->Vp + (size_t)i * st->d, Vp + (size_t)i * st->d, 1, 1);
+    }
     st->np = st->L_p;
     st->t = 0;
     st->n_skip = 0;
@@ -236,8 +328,8 @@ int orc_step(orc_stream *st, const double *q, const double *k, const double *v,
 
     if (st->t < st->sink) {
         /* Diagonal+sink4: the first `sink` decode tokens join the prefix. */
-        memcpy(st->Kp + (size_t)st->np * d, k, sizeof(double) * d);
-        memcpy(st->Vp + (size_t)st->np * d, v, sizeof(double) * d);
+        store_row(st, st->Kp + (size_t)st->np * d, k, 0, 0);
+        store_row(st, st->Vp + (size_t)st->np * d, v, 1, 0);
         st->np += 1;
         st->n_idx = 0;
         attn(st, q, out);
@@ -250,8 +342,8 @@ int orc_step(orc_stream *st, const double *q, const double *k, const double *v,
         st->K[tt] = (double *)malloc(sizeof(double) * d);
         st->V[tt] = (double *)malloc(sizeof(double) * d);
         if (!st->K[tt] || !st->V[tt]) return -1;
-        memcpy(st->K[tt], k, sizeof(double) * d);
-        memcpy(st->V[tt], v, sizeof(double) * d);
+        store_row(st, st->K[tt], k, 0, 0);
+        store_row(st, st->V[tt], v, 1, 0);
         st->live += 1;
         inf.t_inner = tt;
 

@@ -32,6 +32,10 @@ MUTATIONS = {
     "skip_now": 7,
     "budget": 8,
     "newest_tie": 9,
+    "fp8_swap": 10,
+    "fp8_scale": 11,
+    "fp8_trunc": 12,
+    "fp8_prompt": 13,
 }
 
 
@@ -93,6 +97,11 @@ def lib() -> ctypes.CDLL:
         L.orc_step_batch.argtypes = [ctypes.POINTER(P), ctypes.c_int, dp, dp, dp, dp, ip,
                                      ctypes.POINTER(OrcInfo), ctypes.c_int]
         L.orc_max_threads.restype = ctypes.c_int
+        L.orc_set_kv_fp8.argtypes = [P, ctypes.c_float, ctypes.c_float]
+        L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        L.orc_e4m3_encode.restype = ctypes.c_ubyte
+        L.orc_e4m3_decode.argtypes = [ctypes.c_ubyte]
+        L.orc_e4m3_decode.restype = ctypes.c_double
         _lib = L
     return _lib
 
@@ -102,16 +111,32 @@ def _dptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
-class OracleStream:
-    """One (sequence, layer, head) stream of Algorithm 1."""
+def e4m3_encode(y: float) -> int:
+    """The oracle's E4M3 code of the fp32 value y (nearest, ties to even, satfinite)."""
+    return int(lib().orc_e4m3_encode(float(y)))
 
-    def __init__(self, d: int, L_p: int, N_r: int, N_att: int, sink: int = 0, mutation: str | None = None):
+
+def e4m3_decode(c: int) -> float:
+    """The value of E4M3 code c."""
+    return float(lib().orc_e4m3_decode(int(c)))
+
+
+class OracleStream:
+    """One (sequence, layer, head) stream of Algorithm 1.  With `kv_scales`
+    = (k_scale, v_scale) the stream stores its K and V rows as FP8 E4M3 codes
+    with those scales (see dsa_oracle.c)."""
+
+    def __init__(self, d: int, L_p: int, N_r: int, N_att: int, sink: int = 0, mutation: str | None = None,
+                 kv_scales: tuple[float, float] | None = None):
         self._h = lib().orc_create(d, L_p, N_r, N_att, sink)
         if not self._h:
             raise ValueError(f"oracle rejects d={d} L_p={L_p} N_r={N_r} N_att={N_att} sink={sink}")
         self.d, self.L_p, self.N_r, self.N_att, self.sink = d, L_p, N_r, N_att, sink
         if mutation:
             lib().orc_set_mutation(self._h, MUTATIONS[mutation])
+        if kv_scales is not None:
+            if lib().orc_set_kv_fp8(self._h, float(kv_scales[0]), float(kv_scales[1])) != 0:
+                raise ValueError(f"oracle rejects the scales {kv_scales}")
 
     def __del__(self):
         h, self._h = getattr(self, "_h", None), None
@@ -152,8 +177,14 @@ class OracleStream:
 class OracleBatch:
     """n independent streams stepped together (optionally on host threads)."""
 
-    def __init__(self, n: int, d: int, L_p: int, N_r: int, N_att: int, sink: int = 0):
-        self.streams = [OracleStream(d, L_p, N_r, N_att, sink) for _ in range(n)]
+    def __init__(self, n: int, d: int, L_p: int, N_r: int, N_att: int, sink: int = 0,
+                 k_scales=None, v_scales=None):
+        """k_scales, v_scales: per-stream scales of FP8 E4M3 storage, or None."""
+        if (k_scales is None) != (v_scales is None):
+            raise ValueError("give both k_scales and v_scales, or neither")
+        self.streams = [OracleStream(d, L_p, N_r, N_att, sink,
+                                     kv_scales=None if k_scales is None else (k_scales[i], v_scales[i]))
+                        for i in range(n)]
         self.n, self.d = n, d
         self._arr = (ctypes.c_void_p * n)(*[s._h for s in self.streams])
         self._infos = (OrcInfo * n)()

@@ -332,6 +332,43 @@ def pin_ties(mutation=None):
     return fails
 
 
+def _torch_e4m3_store(x: np.ndarray, scale: float) -> np.ndarray:
+    """Library model of an FP8 E4M3 stored row: PyTorch's float8_e4m3fn of
+    fp32(x) * fp32(1 / scale) (clamped to +-448, the format's largest finite
+    value: the library maps beyond 464 to NaN), times scale."""
+    inv = np.float32(1.0) / np.float32(scale)
+    y = np.clip(x.astype(np.float32) * inv, -448.0, 448.0)
+    c = torch.from_numpy(y).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return c * np.float64(np.float32(scale))
+
+
+def pin_fp8_store(mutation=None):
+    """FP8 KV storage: the oracle with E4M3 storage equals the plain oracle run
+    on rows quantized by the library model, bit for bit (outputs and skip
+    sets), with sinks, saturating and subnormal elements, and distinct K and
+    V scales."""
+    fails = []
+    for sink in (0, 4):
+        rng = np.random.default_rng(5 + sink)
+        d, L_p, L_dec, N_r, N_att = 16, 6, 40, 14, 7
+        ks, vs = 0.0123, 0.0371
+        K = rng.normal(0, 2, (L_p, d)); V = rng.normal(0, 2, (L_p, d))
+        q = rng.normal(0, 1, (L_dec, d)); k = rng.normal(0, 2, (L_dec, d)); v = rng.normal(0, 2, (L_dec, d))
+        k[3, 0] = 1e3   # saturates
+        v[5, 1] = -1e-4  # subnormal range
+        a = OracleStream(d, L_p, N_r, N_att, sink, mutation=mutation, kv_scales=(ks, vs))
+        b = OracleStream(d, L_p, N_r, N_att, sink)
+        a.prefill(K, V)
+        b.prefill(_torch_e4m3_store(K, ks), _torch_e4m3_store(V, vs))
+        for t in range(L_dec):
+            oa, ia = a.step(q[t], k[t], v[t])
+            ob, ib = b.step(q[t], _torch_e4m3_store(k[t], ks), _torch_e4m3_store(v[t], vs))
+            if not np.array_equal(oa, ob) or ia.selected != ib.selected or a.skip() != b.skip():
+                fails.append(f"fp8 store, sink {sink}, t={t}: differs from the library model")
+                break
+    return fails
+
+
 ALL_PINS = {
     "dense": pin_dense,
     "sliding": pin_sliding,
@@ -341,4 +378,5 @@ ALL_PINS = {
     "relative": pin_relative,
     "cost": pin_cost,
     "ties": pin_ties,
+    "fp8_store": pin_fp8_store,
 }
