@@ -68,7 +68,10 @@ int dev_alloc(void **p, size_t bytes, const char *what)
 constexpr uint32_t kMagic = 0x44534131u;  // "DSA1"
 constexpr uint32_t kDefaultWaitLimit = 0xffffffffu;
 
-int elem_bytes(int dtype) { return dtype == DSA_F32 ? 4 : 2; }
+// Bytes of a stored K / V element and of a q / k_new / v_new / out element.
+int elem_bytes(int dtype) { return dtype == DSA_F32 ? 4 : (dtype == DSA_FP8_E4M3 ? 1 : 2); }
+int io_bytes(int dtype) { return dtype == DSA_F32 ? 4 : 2; }
+bool valid_dtype(int dtype) { return dtype == DSA_BF16 || dtype == DSA_F32 || dtype == DSA_FP8_E4M3; }
 
 // Stage rows and the rows-per-item limit of pipeline shape sh (a multiple of
 // the stage rows, so that items end on stage boundaries).
@@ -103,6 +106,7 @@ struct dsa_ctx {
     float *part_acc;
     float2 *part_ml, *part_min;
     int *status;
+    float *scales;         // FP8 storage: [4, S] K scale, V scale, their fp32 inverses (else NULL)
     CUtensorMap ring_map;  // 2-D view of the ring: [S * R rows, 2 * D], one-row box
 };
 
@@ -119,7 +123,8 @@ int validate(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int
     if (N_att < 1 || N_att > N_r) return fail(DSA_ERR_ARG, "need 1 <= N_att <= N_r (got N_att=%d, N_r=%d)", N_att, N_r);
     if (sink > 0 && N_att <= sink) return fail(DSA_ERR_ARG, "need N_att > sink (got N_att=%d, sink=%d)", N_att, sink);
     if (N_r - sink > 65536) return fail(DSA_ERR_ARG, "N_r - sink must be <= 65536 (got %d)", N_r - sink);
-    if (dtype != DSA_BF16 && dtype != DSA_F32) return fail(DSA_ERR_ARG, "dtype must be DSA_BF16 or DSA_F32 (got %d)", dtype);
+    if (!valid_dtype(dtype))
+        return fail(DSA_ERR_ARG, "dtype must be DSA_BF16, DSA_F32 or DSA_FP8_E4M3 (got %d)", dtype);
     if ((long long)L_p + sink > INT_MAX / 4) return fail(DSA_ERR_ARG, "L_p too large");
     if ((long long)heads * (N_r - sink) > INT_MAX) return fail(DSA_ERR_ARG, "heads * (N_r - sink) must fit in 31 bits");
     return DSA_OK;
@@ -186,15 +191,19 @@ void shape_plan(const dsa_ctx *h, int sh, Plan &p)
 // waits on in sequence (rounds x stages per item, one loaded copy latency
 // each).  Measured on GB300 (152 SMs): one loaded latency is about 1.6 us
 // and HBM streams about 6.7 TB/s, so a launch is bandwidth bound once it
-// moves more than about kBytesPerLatency per stage it runs in sequence; the
-// 6 KB stages of shape 1 stream about 5 % slower than shape 0 when
-// bandwidth bound (more stage waits per byte).
+// moves more than about kBytesPerLatency per stage it runs in sequence.
+// With bf16 / fp32 rows the 6 KB stages of shape 1 stream about 5 % slower
+// than shape 0 when bandwidth bound (more stage waits per byte); with FP8
+// rows the warps are bound by their own arithmetic rather than by HBM, and
+// the third more warps of shape 1 stream about 5 % faster.
 constexpr double kBytesPerLatency = 10.5e6;
 constexpr double kShapeRate[dsa::kPipes] = {1.0, 0.95};
+constexpr double kShapeRateFp8[dsa::kPipes] = {1.0, 1.05};
 
-double launch_cost(const Plan &p)
+double launch_cost(const Plan &p, int dtype)
 {
-    const double bw = (double)p.bytes / (kBytesPerLatency * kShapeRate[p.shape]);
+    const double rate = dtype == DSA_FP8_E4M3 ? kShapeRateFp8[p.shape] : kShapeRate[p.shape];
+    const double bw = (double)p.bytes / (kBytesPerLatency * rate);
     return bw > (double)p.stages ? bw : (double)p.stages;
 }
 
@@ -225,9 +234,10 @@ Plan make_plan(const dsa_ctx *h, int t)
     }
     p.n = p.P + p.a;
     const unsigned long long De = (unsigned long long)h->D * elem_bytes(h->dtype);
-    // K and V rows read (current token through k_new/v_new) + q + k_new, v_new
+    const unsigned long long Di = (unsigned long long)h->D * io_bytes(h->dtype);
+    // K and V rows read (current token through k_new/v_new) + q, k_new, v_new
     // read + new entry written + out written.
-    p.bytes = (unsigned long long)h->S * (2 * De * (unsigned long long)(p.n - 1) + 6 * De);
+    p.bytes = (unsigned long long)h->S * (2 * De * (unsigned long long)(p.n - 1) + 4 * Di + 2 * De);
     if (h->forced_pipe > 0) {
         shape_plan(h, h->forced_pipe - 1, p);
     } else {
@@ -235,7 +245,7 @@ Plan make_plan(const dsa_ctx *h, int t)
         if (h->ctas_per_sm[1] > 0) {
             Plan q = p;
             shape_plan(h, 1, q);
-            if (launch_cost(q) < launch_cost(p)) p = q;
+            if (launch_cost(q, h->dtype) < launch_cost(p, h->dtype)) p = q;
         }
     }
     return p;
@@ -290,6 +300,7 @@ void free_ctx(dsa_ctx *h)
     cudaFree(h->part_ml);
     cudaFree(h->part_min);
     cudaFree(h->status);
+    cudaFree(h->scales);
     h->magic = 0;
     forget_handle(h);
     delete h;
@@ -314,7 +325,10 @@ int encode_ring_map(dsa_ctx *h)
     const cuuint64_t strides[1] = {(cuuint64_t)(2 * h->D * elem_bytes(h->dtype))};
     const cuuint32_t box[2] = {(cuuint32_t)(2 * h->D), 1};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&h->ring_map, h->dtype == DSA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+    const CUtensorMapDataType ty = h->dtype == DSA_F32        ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : h->dtype == DSA_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = encode(&h->ring_map, ty,
                         2, h->ring, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -342,6 +356,7 @@ template <int SH>
 int occupancy_sh(int dtype, int D)
 {
     if (dtype == DSA_BF16) return D == 64 ? occupancy<__nv_bfloat16, 64, SH>() : occupancy<__nv_bfloat16, 128, SH>();
+    if (dtype == DSA_FP8_E4M3) return D == 64 ? occupancy<__nv_fp8_e4m3, 64, SH>() : occupancy<__nv_fp8_e4m3, 128, SH>();
     return D == 64 ? occupancy<float, 64, SH>() : occupancy<float, 128, SH>();
 }
 
@@ -401,6 +416,9 @@ cudaError_t launch_decode_sh(int dtype, int D, const dsa::DecodeParams &p, const
     if (dtype == DSA_BF16)
         return D == 64 ? launch_decode<__nv_bfloat16, 64, SH>(p, map, grid, st)
                        : launch_decode<__nv_bfloat16, 128, SH>(p, map, grid, st);
+    if (dtype == DSA_FP8_E4M3)
+        return D == 64 ? launch_decode<__nv_fp8_e4m3, 64, SH>(p, map, grid, st)
+                       : launch_decode<__nv_fp8_e4m3, 128, SH>(p, map, grid, st);
     return D == 64 ? launch_decode<float, 64, SH>(p, map, grid, st) : launch_decode<float, 128, SH>(p, map, grid, st);
 }
 
@@ -413,6 +431,8 @@ cudaError_t launch_step(int dtype, int D, int shape, const dsa::DecodeParams &p,
     if (e != cudaSuccess || p.nsplit == 1) return e;
     if (dtype == DSA_BF16)
         return D == 64 ? launch_merge<__nv_bfloat16, 64>(p, st) : launch_merge<__nv_bfloat16, 128>(p, st);
+    if (dtype == DSA_FP8_E4M3)
+        return D == 64 ? launch_merge<__nv_fp8_e4m3, 64>(p, st) : launch_merge<__nv_fp8_e4m3, 128>(p, st);
     return D == 64 ? launch_merge<float, 64>(p, st) : launch_merge<float, 128>(p, st);
 }
 
@@ -449,14 +469,34 @@ void forget_handle(const dsa_ctx *h)
 }
 
 template <typename T, int D>
-cudaError_t launch_prefill(const void *K, const void *V, void *prefix, int S, int L_p, int Lcap, cudaStream_t st)
+cudaError_t launch_prefill(const void *K, const void *V, void *prefix, const float *kinv, const float *vinv, int S,
+                           int L_p, int Lcap, cudaStream_t st)
 {
-    const size_t total = (size_t)S * L_p * 2 * (D * sizeof(T) / 16);
+    using IO = typename dsa::Elem<T>::IO;
+    const size_t total = (size_t)S * L_p * 2 * (D / dsa::Elem<T>::VEC);
     if (total == 0) return cudaSuccess;
     size_t blocks = (total + 255) / 256;
     if (blocks > 65535 * 8) blocks = 65535 * 8;
-    dsa::prefill_kernel<T, D><<<(unsigned)blocks, 256, 0, st>>>((const T *)K, (const T *)V, (T *)prefix, S, L_p, Lcap);
+    dsa::prefill_kernel<T, D><<<(unsigned)blocks, 256, 0, st>>>((const IO *)K, (const IO *)V, (T *)prefix, kinv, vinv,
+                                                                S, L_p, Lcap);
     return cudaGetLastError();
+}
+
+// FP8 storage: uploads K and V scales and their fp32 inverses ([4, S]).
+int upload_scales(dsa_ctx *h, const float *k_scale, const float *v_scale)
+{
+    const size_t S = (size_t)h->S;
+    float *host = new (std::nothrow) float[4 * S];
+    if (!host) return fail(DSA_ERR_OOM, "host allocation failed");
+    for (size_t i = 0; i < S; ++i) {
+        host[i] = k_scale ? k_scale[i] : 1.0f;
+        host[S + i] = v_scale ? v_scale[i] : 1.0f;
+        host[2 * S + i] = 1.0f / host[i];
+        host[3 * S + i] = 1.0f / host[S + i];
+    }
+    cudaError_t e = cudaMemcpy(h->scales, host, sizeof(float) * 4 * S, cudaMemcpyHostToDevice);
+    delete[] host;
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "scale upload");
 }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -475,8 +515,7 @@ int dsa_debug_fail_alloc_after(int n)
 
 size_t dsa_state_bytes(int heads, int head_dim, int L_p, int N_r, int sink, int dtype)
 {
-    if (heads < 1 || (head_dim != 64 && head_dim != 128) || L_p < 0 || sink < 0 || N_r <= sink ||
-        (dtype != DSA_BF16 && dtype != DSA_F32))
+    if (heads < 1 || (head_dim != 64 && head_dim != 128) || L_p < 0 || sink < 0 || N_r <= sink || !valid_dtype(dtype))
         return 0;
     const size_t row = 2 * (size_t)head_dim * elem_bytes(dtype);
     const size_t R = (size_t)(N_r - sink);
@@ -533,6 +572,8 @@ int dsa_create_ex(int heads, int head_dim, int L_p, int N_r, int N_att, int sink
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->mask, S * h->MW * 4, "skip mask");
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->last_sel, S * 4, "last selection");
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->status, 16, "status word");
+    if (rc == DSA_OK && dtype == DSA_FP8_E4M3) rc = dev_alloc((void **)&h->scales, S * 4 * sizeof(float), "FP8 scales");
+    if (rc == DSA_OK && dtype == DSA_FP8_E4M3) rc = upload_scales(h, nullptr, nullptr);
     if (rc == DSA_OK) rc = ensure_partials(h, max_splits(h));
     if (rc == DSA_OK) rc = encode_ring_map(h);
     if (rc != DSA_OK) {
@@ -577,12 +618,17 @@ int dsa_prefill(dsa_handle h, const void *K, const void *V, void *stream)
         (e = cudaMemsetAsync(h->status, 0, 16, st)) != cudaSuccess ||
         (e = cudaMemsetAsync(h->last_sel, 0xff, S * 4, st)) != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync");
+    const float *kinv = h->scales ? h->scales + 2 * S : nullptr;
+    const float *vinv = h->scales ? h->scales + 3 * S : nullptr;
     if (h->dtype == DSA_BF16)
-        e = h->D == 64 ? launch_prefill<__nv_bfloat16, 64>(K, V, h->prefix, h->S, h->L_p, h->Lcap, st)
-                       : launch_prefill<__nv_bfloat16, 128>(K, V, h->prefix, h->S, h->L_p, h->Lcap, st);
+        e = h->D == 64 ? launch_prefill<__nv_bfloat16, 64>(K, V, h->prefix, kinv, vinv, h->S, h->L_p, h->Lcap, st)
+                       : launch_prefill<__nv_bfloat16, 128>(K, V, h->prefix, kinv, vinv, h->S, h->L_p, h->Lcap, st);
+    else if (h->dtype == DSA_FP8_E4M3)
+        e = h->D == 64 ? launch_prefill<__nv_fp8_e4m3, 64>(K, V, h->prefix, kinv, vinv, h->S, h->L_p, h->Lcap, st)
+                       : launch_prefill<__nv_fp8_e4m3, 128>(K, V, h->prefix, kinv, vinv, h->S, h->L_p, h->Lcap, st);
     else
-        e = h->D == 64 ? launch_prefill<float, 64>(K, V, h->prefix, h->S, h->L_p, h->Lcap, st)
-                       : launch_prefill<float, 128>(K, V, h->prefix, h->S, h->L_p, h->Lcap, st);
+        e = h->D == 64 ? launch_prefill<float, 64>(K, V, h->prefix, kinv, vinv, h->S, h->L_p, h->Lcap, st)
+                       : launch_prefill<float, 128>(K, V, h->prefix, kinv, vinv, h->S, h->L_p, h->Lcap, st);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     note_launch(st, h);
     h->t = 0;
@@ -653,6 +699,10 @@ int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *
     p.select = pl.select;
     p.MW = h->MW;
     p.qscale = (float)(1.4426950408889634 / std::sqrt((double)h->D));
+    p.kscale = h->scales ? h->scales : nullptr;
+    p.vscale = h->scales ? h->scales + h->S : nullptr;
+    p.kinv = h->scales ? h->scales + 2 * (size_t)h->S : nullptr;
+    p.vinv = h->scales ? h->scales + 3 * (size_t)h->S : nullptr;
     p.wait_limit = h->wait_limit;
 
     cudaStream_t st = (cudaStream_t)stream;
@@ -731,6 +781,35 @@ int dsa_set_pipeline(dsa_handle h, int pipeline)
     return DSA_OK;
 }
 
+int dsa_set_kv_scales(dsa_handle h, const float *k_scale, const float *v_scale)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (h->dtype != DSA_FP8_E4M3) return fail(DSA_ERR_ARG, "KV scales apply to DSA_FP8_E4M3 handles only");
+    if (!k_scale || !v_scale) return fail(DSA_ERR_ARG, "k_scale and v_scale must be non-NULL");
+    for (int i = 0; i < h->S; ++i)
+        if (!(k_scale[i] > 0.0f) || !(v_scale[i] > 0.0f) || std::isinf(k_scale[i]) || std::isinf(v_scale[i]))
+            return fail(DSA_ERR_ARG, "scales must be positive and finite (stream %d: %g, %g)", i, k_scale[i], v_scale[i]);
+    // Kernels of earlier steps may still read the scales.
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    int rc = upload_scales(h, k_scale, v_scale);
+    if (rc != DSA_OK) return rc;
+    h->prefilled = 0;  // rows stored with the old scales are gone: dsa_prefill must follow
+    return DSA_OK;
+}
+
+int dsa_debug_copy_state(dsa_handle h, void *host_prefix, void *host_ring)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    const size_t row = 2 * (size_t)h->D * elem_bytes(h->dtype);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess && host_prefix)
+        e = cudaMemcpy(host_prefix, h->prefix, (size_t)h->S * h->Lcap * row, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && host_ring)
+        e = cudaMemcpy(host_ring, h->ring, (size_t)h->S * h->R * row, cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? DSA_OK : cuda_fail(e, "state copy");
+}
+
 int dsa_set_wait_limit(dsa_handle h, uint32_t limit)
 {
     if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
@@ -805,6 +884,8 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
 {
     int rc = validate(heads, head_dim, L_p, N_r, N_att, sink, dtype);
     if (rc != DSA_OK) return rc;
+    if (dtype == DSA_FP8_E4M3)
+        return fail(DSA_ERR_ARG, "dsa_decode_step_noalloc: FP8 storage needs per-stream scales; use the handle API");
     if (t < 0) return fail(DSA_ERR_ARG, "t must be >= 0 (got %d)", t);
     if (!ring || !mask || !last_sel || !q || !k_new || !v_new || !out || (L_p + sink > 0 && !prefix))
         return fail(DSA_ERR_ARG, "state and input/output pointers must be non-NULL");
@@ -899,6 +980,7 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.select = pl.select;
     p.MW = h.MW;
     p.qscale = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
+    p.kscale = p.vscale = p.kinv = p.vinv = nullptr;
     p.wait_limit = kDefaultWaitLimit;
     p.early = 0;  // caller-owned state: the previous kernel may have written it
     e = launch_step(dtype, head_dim, pl.shape, p, h.ring_map, pl.grid, st);

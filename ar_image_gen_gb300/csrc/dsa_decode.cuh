@@ -30,6 +30,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include <cstdint>
 
@@ -107,6 +109,10 @@ struct DecodeParams {
     int early;            // 1: the previous grid in the stream does not write this state, so
                           // the mask, prefix and ring may be read before the grid dependency wait
     float qscale;         // log2(e) / sqrt(D), applied to q.k
+    const float *kscale;  // [S] FP8 storage: K scale, V scale and their fp32 inverses
+    const float *vscale;  //     (NULL for bf16 / fp32 storage)
+    const float *kinv;
+    const float *vinv;
     uint32_t wait_limit;
 };
 
@@ -135,7 +141,10 @@ struct Elem;
 
 template <>
 struct Elem<float> {
-    static constexpr int VEC = 4;
+    using IO = float;                   // type of q, k_new, v_new, prompt K / V and out
+    using Vec = uint4;                  // one stored vector of a K or V row
+    static constexpr bool SCALED = false;
+    static constexpr int VEC = 4;       // elements per Vec
     struct Q { float x[4]; };
     static __device__ __forceinline__ Q load_q(const uint4 &v)
     {
@@ -158,10 +167,18 @@ struct Elem<float> {
         return make_uint4(__float_as_uint(a[0] * scale), __float_as_uint(a[1] * scale), __float_as_uint(a[2] * scale),
                           __float_as_uint(a[3] * scale));
     }
+    // Stored form of vector `vec` of an input row (unchanged).
+    static __device__ __forceinline__ Vec load_kv(const IO *row, int vec, float)
+    {
+        return __ldg(reinterpret_cast<const Vec *>(row) + vec);
+    }
 };
 
 template <>
 struct Elem<__nv_bfloat16> {
+    using IO = __nv_bfloat16;
+    using Vec = uint4;
+    static constexpr bool SCALED = false;
     static constexpr int VEC = 8;
     struct Q { uint4 raw; };  // q stays packed bf16: the dot uses mixed-precision FMAs
     static __device__ __forceinline__ Q load_q(const uint4 &v) { return Q{v}; }
@@ -196,6 +213,89 @@ struct Elem<__nv_bfloat16> {
         }
         return make_uint4(w[0], w[1], w[2], w[3]);
     }
+    static __device__ __forceinline__ Vec load_kv(const IO *row, int vec, float)
+    {
+        return __ldg(reinterpret_cast<const Vec *>(row) + vec);
+    }
+};
+
+// FP8 E4M3 storage of K and V with one scale per stream for each; q, k_new,
+// v_new, the prompt K / V and out are bf16.  A stored code is the E4M3 value
+// nearest to fp32(x) * fp32(1 / scale) (satfinite); its value is code *
+// scale.  The kernel keeps the scales out of the inner loops: logits are
+// q . code (times the K scale, applied once per logit with the softmax
+// scale) and P.V accumulates p * code (times the V scale at the end).
+// Codes widen exactly to f16 (cvt), q is rounded to f16 once per item, and
+// products accumulate in fp32 (mixed-precision FMA).
+__device__ __forceinline__ uint32_t f16x2_bits(__half2 h) { return *reinterpret_cast<const uint32_t *>(&h); }
+
+// The two f16 halves (low, high) of the codes in the 16-bit value c2.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t c2)
+{
+    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(c2 & 0xffffu), __NV_E4M3);
+    return (uint32_t)r.x | ((uint32_t)r.y << 16);
+}
+
+// acc0 += lo(a) * lo(b), acc1 += hi(a) * hi(b) for f16x2 a, b in fp32.
+__device__ __forceinline__ void fma2_f16_f32(float &acc0, float &acc1, uint32_t a, uint32_t b)
+{
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %0;\n\tfma.rn.f32.f16 %1, a1, b1, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(a), "r"(b));
+}
+
+template <>
+struct Elem<__nv_fp8_e4m3> {
+    using IO = __nv_bfloat16;
+    using Vec = uint2;                  // 8 codes
+    static constexpr bool SCALED = true;
+    static constexpr int VEC = 8;
+    struct Q { uint32_t h[4]; };        // 8 q elements as f16 pairs
+    static __device__ __forceinline__ Q load_q(const uint4 &v)  // 8 bf16
+    {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        Q q;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            q.h[i] = f16x2_bits(__floats2half2_rn(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u)));
+        return q;
+    }
+    static __device__ __forceinline__ void dot(const Q &q, const uint2 &k, float &s0, float &s1)
+    {
+        fma2_f16_f32(s0, s1, e4m3x2_to_f16x2(k.x), q.h[0]);
+        fma2_f16_f32(s0, s1, e4m3x2_to_f16x2(k.x >> 16), q.h[1]);
+        fma2_f16_f32(s0, s1, e4m3x2_to_f16x2(k.y), q.h[2]);
+        fma2_f16_f32(s0, s1, e4m3x2_to_f16x2(k.y >> 16), q.h[3]);
+    }
+    // acc[0..7] += p * v (p rounded to f16, products in fp32)
+    static __device__ __forceinline__ void axpy(float p, const uint2 &v, float *acc)
+    {
+        const uint32_t pp = f16x2_bits(__float2half2_rn(p));
+        fma2_f16_f32(acc[0], acc[1], e4m3x2_to_f16x2(v.x), pp);
+        fma2_f16_f32(acc[2], acc[3], e4m3x2_to_f16x2(v.x >> 16), pp);
+        fma2_f16_f32(acc[4], acc[5], e4m3x2_to_f16x2(v.y), pp);
+        fma2_f16_f32(acc[6], acc[7], e4m3x2_to_f16x2(v.y >> 16), pp);
+    }
+    static __device__ __forceinline__ __nv_bfloat16 narrow(float x) { return __float2bfloat16_rn(x); }
+    static __device__ __forceinline__ uint4 pack(const float *a, float scale)
+    {
+        return Elem<__nv_bfloat16>::pack(a, scale);
+    }
+    // Codes of the 8 bf16 elements of vector `vec` of an input row.
+    static __device__ __forceinline__ Vec load_kv(const IO *row, int vec, float inv)
+    {
+        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(row) + vec);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = make_float2(__uint_as_float(w[i] << 16) * inv, __uint_as_float(w[i] & 0xffff0000u) * inv);
+            c[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+        }
+        return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    }
 };
 
 // Pipeline shapes (compile-time): independent warps per CTA, shared-memory
@@ -229,8 +329,8 @@ struct Pipe<1> {
 
 template <typename T, int D, int SH>
 struct KCfg {
-    static constexpr int E = sizeof(T);
-    static constexpr int VEC = Elem<T>::VEC;   // elements per 16-byte vector
+    static constexpr int E = sizeof(T);        // bytes of a stored element
+    static constexpr int VEC = Elem<T>::VEC;   // elements per stored vector (16 bytes; 8 for FP8)
     static constexpr int LPR = D / (2 * VEC);  // lanes per row: each lane reads 2 vectors of K and of V
     static constexpr int RPW = 32 / LPR;       // rows per warp instruction
     static constexpr int KROW = D * E;         // bytes of a K (or V) row
@@ -280,6 +380,8 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
 {
     using C = KCfg<T, D, SH>;
     using EL = Elem<T>;
+    using IO = typename EL::IO;
+    using Vec = typename EL::Vec;
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -314,7 +416,7 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
     };
     uint4 qn0 = make_uint4(0, 0, 0, 0), qn1 = qn0;  // q vectors of the next item
     auto load_q = [&](int item) {
-        const uint4 *qr = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.q) + (size_t)(item / p.nsplit) * D);
+        const uint4 *qr = reinterpret_cast<const uint4 *>(reinterpret_cast<const IO *>(p.q) + (size_t)(item / p.nsplit) * D);
         qn0 = __ldg(qr + cl);
         qn1 = __ldg(qr + cl + C::LPR);
     };
@@ -544,21 +646,24 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
         const bool has_cur = (klo == 0 && khi > 0 && !self_skip);
         T *const cur_dst = p.sinkmode ? reinterpret_cast<T *>(p.prefix) + ((size_t)s * p.Lcap + p.P) * 2 * D
                                       : reinterpret_cast<T *>(p.ring) + ((size_t)s * p.R + p.tin_mod) * 2 * D;
-        uint4 kc0, kc1, vc0, vc1;
-        if (has_cur) {  // the current token goes straight to registers
-            const uint4 *kr = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.knew) + (size_t)s * D);
-            const uint4 *vr = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.vnew) + (size_t)s * D);
-            kc0 = __ldg(kr + cl);
-            kc1 = __ldg(kr + cl + C::LPR);
-            vc0 = __ldg(vr + cl);
-            vc1 = __ldg(vr + cl + C::LPR);
+        // FP8 storage: per-stream scales (1 otherwise)
+        const float kinv = EL::SCALED ? __ldg(p.kinv + s) : 1.f;
+        const float vinv = EL::SCALED ? __ldg(p.vinv + s) : 1.f;
+        const float xs = EL::SCALED ? p.qscale * __ldg(p.kscale + s) : p.qscale;
+        const IO *kio = reinterpret_cast<const IO *>(p.knew) + (size_t)s * D;
+        const IO *vio = reinterpret_cast<const IO *>(p.vnew) + (size_t)s * D;
+        Vec kc0, kc1, vc0, vc1;
+        if (has_cur) {  // the current token goes straight to registers, in its stored form
+            kc0 = EL::load_kv(kio, cl, kinv);
+            kc1 = EL::load_kv(kio, cl + C::LPR, kinv);
+            vc0 = EL::load_kv(vio, cl, vinv);
+            vc1 = EL::load_kv(vio, cl + C::LPR, vinv);
         } else if (self_skip && c == 0) {
-            // a2 for a token that is not attended: it is in no stage; copy it.
-            constexpr int NV = C::KROW / 16;
-            uint4 *dst = reinterpret_cast<uint4 *>(cur_dst);
-            const uint4 *ks = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.knew) + (size_t)s * D);
-            const uint4 *vs = reinterpret_cast<const uint4 *>(reinterpret_cast<const T *>(p.vnew) + (size_t)s * D);
-            for (int i = lane; i < 2 * NV; i += 32) dst[i] = (i < NV) ? ks[i] : vs[i - NV];
+            // a2 for a token that is not attended: it is in no stage; store it.
+            constexpr int NV = D / C::VEC;
+            Vec *dst = reinterpret_cast<Vec *>(cur_dst);
+            for (int i = lane; i < 2 * NV; i += 32)
+                dst[i] = (i < NV) ? EL::load_kv(kio, i, kinv) : EL::load_kv(vio, i - NV, vinv);
         }
         const int npre = max(min(hi, p.P) - lo, 0);
         const int kr0 = has_cur ? klo + 1 : klo;
@@ -590,14 +695,14 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
                 const bool valid = row < nv;
                 float s0 = 0.f, s1 = 0.f;
                 if (valid) {
-                    const uint4 *kr = reinterpret_cast<const uint4 *>(st + row * C::ROW);
+                    const Vec *kr = reinterpret_cast<const Vec *>(st + row * C::ROW);
                     EL::dot(q0, kr[cl], s0, s1);
                     EL::dot(q1, kr[cl + C::LPR], s0, s1);
                 }
                 float x = s0 + s1;
 #pragma unroll
                 for (int o = C::LPR / 2; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-                x *= p.qscale;
+                x *= xs;
                 sc[it] = valid ? x : -INFINITY;
                 if (p.select && valid && u0 + row >= npre) {
                     const int k = kr0 + (u0 + row - npre);
@@ -626,7 +731,7 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
                 if (row < nv) {
                     const float pj = ex2(sc[it] - m);
                     l += pj;
-                    const uint4 *vr = reinterpret_cast<const uint4 *>(st + row * C::ROW + C::KROW);
+                    const Vec *vr = reinterpret_cast<const Vec *>(st + row * C::ROW + C::KROW);
                     EL::axpy(pj, vr[cl], acc);
                     EL::axpy(pj, vr[cl + C::LPR], acc + C::VEC);
                 }
@@ -644,7 +749,7 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
             float x = s0 + s1;
 #pragma unroll
             for (int o = C::LPR / 2; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-            x *= p.qscale;  // identical in every row group
+            x *= xs;  // identical in every row group
             if (p.select && better(x, 0, minv, minr)) {
                 minv = x;
                 minr = 0;
@@ -661,7 +766,7 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
                 l += pj;
                 EL::axpy(pj, vc0, acc);
                 EL::axpy(pj, vc1, acc + C::VEC);
-                uint4 *dst = reinterpret_cast<uint4 *>(cur_dst);
+                Vec *dst = reinterpret_cast<Vec *>(cur_dst);
                 dst[cl] = kc0;
                 dst[cl + C::LPR] = kc1;
                 dst[2 * C::LPR + cl] = vc0;
@@ -684,8 +789,8 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
         }
         if (p.nsplit == 1) {
             if (g == 0) {
-                const float inv = 1.f / l;
-                uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<T *>(p.out) + (size_t)s * D);
+                const float inv = (EL::SCALED ? __ldg(p.vscale + s) : 1.f) / l;
+                uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<IO *>(p.out) + (size_t)s * D);
                 o[cl] = EL::pack(acc, inv);
                 o[cl + C::LPR] = EL::pack(acc + C::VEC, inv);
             }
@@ -753,8 +858,8 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodePar
             for (int e = 0; e < DPL; ++e) O[e] = fmaf(__ldcg(&p.part_acc[(base + i) * D + lane * DPL + e]), f, O[e]);
         }
     }
-    T *o = reinterpret_cast<T *>(p.out) + (size_t)s * D + lane * DPL;
-    const float inv = 1.f / Lx;
+    typename EL::IO *o = reinterpret_cast<typename EL::IO *>(p.out) + (size_t)s * D + lane * DPL;
+    const float inv = (EL::SCALED ? __ldg(p.vscale + s) : 1.f) / Lx;
 #pragma unroll
     for (int e = 0; e < DPL; ++e) o[e] = EL::narrow(O[e] * inv);
     if (p.select) {
@@ -783,23 +888,25 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodePar
     }
 }
 
-// a1: prompt K, V [S, L_p, D] -> prefix [S, Lcap, 2, D].
+// a1: prompt K, V [S, L_p, D] -> prefix [S, Lcap, 2, D] in the stored form
+// (FP8 storage: codes with the per-stream inverse scales kinv, vinv).
 template <typename T, int D>
-__global__ void prefill_kernel(const T *__restrict__ K, const T *__restrict__ V, T *__restrict__ prefix, int S,
-                               int L_p, int Lcap)
+__global__ void prefill_kernel(const typename Elem<T>::IO *__restrict__ K, const typename Elem<T>::IO *__restrict__ V,
+                               T *__restrict__ prefix, const float *kinv, const float *vinv, int S, int L_p, int Lcap)
 {
-    constexpr int VPR = D * (int)sizeof(T) / 16;
-    const size_t total = (size_t)S * L_p * 2 * VPR;
+    using EL = Elem<T>;
+    constexpr int NV = D / EL::VEC;  // stored vectors per K (or V) row
+    const size_t total = (size_t)S * L_p * 2 * NV;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-        const int vec = (int)(i % VPR);
-        size_t rest = i / VPR;
+        const int vec = (int)(i % NV);
+        size_t rest = i / NV;
         const int kv = (int)(rest & 1);
         rest >>= 1;
         const int row = (int)(rest % L_p);
         const size_t s = rest / L_p;
-        const uint4 *src = reinterpret_cast<const uint4 *>((kv ? V : K) + (s * L_p + row) * D) + vec;
-        uint4 *dst = reinterpret_cast<uint4 *>(prefix + ((s * Lcap + row) * 2 + kv) * D) + vec;
-        *dst = __ldg(src);
+        const float inv = EL::SCALED ? __ldg((kv ? vinv : kinv) + s) : 1.f;
+        typename EL::Vec *dst = reinterpret_cast<typename EL::Vec *>(prefix + ((s * Lcap + row) * 2 + kv) * D) + vec;
+        *dst = EL::load_kv((kv ? V : K) + (s * L_p + row) * D, vec, inv);
     }
 }
 

@@ -35,13 +35,16 @@ DSA_ERR_TIMEOUT = -5
 DSA_ERR_DEVICE_CHECK = -6
 DSA_BF16 = 0
 DSA_F32 = 1
+DSA_FP8_E4M3 = 2
+DTYPES = {"bf16": DSA_BF16, "f32": DSA_F32, "fp8e4m3": DSA_FP8_E4M3}
 
 STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_ARG", -2: "DSA_ERR_STATE", -3: "DSA_ERR_OOM", -4: "DSA_ERR_CUDA",
                 -5: "DSA_ERR_TIMEOUT", -6: "DSA_ERR_DEVICE_CHECK"}
 
 EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa_destroy", "dsa_get_step",
            "dsa_get_skip_mask", "dsa_get_last_selection", "dsa_sync_status", "dsa_last_error",
-           "dsa_state_bytes", "dsa_plan_step", "dsa_set_splits", "dsa_set_pipeline", "dsa_set_wait_limit",
+           "dsa_state_bytes", "dsa_plan_step", "dsa_set_kv_scales", "dsa_set_splits", "dsa_set_pipeline",
+           "dsa_set_wait_limit", "dsa_debug_copy_state",
            "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc"]
 
 
@@ -68,6 +71,8 @@ _L.dsa_state_bytes.argtypes = [_I] * 6
 _L.dsa_state_bytes.restype = ctypes.c_size_t
 _L.dsa_plan_step.argtypes = [_P, _I, ctypes.POINTER(dsa_step_plan)]
 _L.dsa_set_splits.argtypes = [_P, _I]
+_L.dsa_set_kv_scales.argtypes = [_P, _P, _P]
+_L.dsa_debug_copy_state.argtypes = [_P, _P, _P]
 _L.dsa_set_pipeline.argtypes = [_P, _I]
 _L.dsa_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
 _L.dsa_debug_fail_alloc_after.argtypes = [_I]
@@ -171,6 +176,17 @@ def dsa_plan_step(h, t):
     return _L.dsa_plan_step(h, t, ctypes.byref(p)), p
 
 
+def dsa_set_kv_scales(h, k_scale: np.ndarray, v_scale: np.ndarray) -> int:
+    k = np.ascontiguousarray(k_scale, dtype=np.float32)
+    v = np.ascontiguousarray(v_scale, dtype=np.float32)
+    return _L.dsa_set_kv_scales(h, k.ctypes.data, v.ctypes.data)
+
+
+def dsa_debug_copy_state(h, host_prefix: np.ndarray | None, host_ring: np.ndarray | None) -> int:
+    return _L.dsa_debug_copy_state(h, None if host_prefix is None else host_prefix.ctypes.data,
+                                   None if host_ring is None else host_ring.ctypes.data)
+
+
 def dsa_set_splits(h, nsplit) -> int:
     return _L.dsa_set_splits(h, nsplit)
 
@@ -200,7 +216,7 @@ class DSA:
     """One handle: `heads` streams of one layer stepping together."""
 
     def __init__(self, heads, head_dim, L_p, N_r, N_att, sink=0, dtype="bf16"):
-        self.dtype_code = {"bf16": DSA_BF16, "f32": DSA_F32}[dtype]
+        self.dtype_code = DTYPES[dtype]
         code, h = dsa_create_ex(heads, head_dim, L_p, N_r, N_att, sink, self.dtype_code)
         _check(code, "dsa_create_ex")
         self.h = h
@@ -247,6 +263,18 @@ class DSA:
         code, p = dsa_plan_step(self.h, self.t if t is None else t)
         _check(code, "dsa_plan_step")
         return p
+
+    def set_kv_scales(self, k_scale, v_scale):
+        """Per-stream FP8 scales (host arrays of `heads` floats); a prefill must follow."""
+        _check(dsa_set_kv_scales(self.h, k_scale, v_scale), "dsa_set_kv_scales")
+
+    def copy_state(self):
+        """(prefix, ring) as uint8 arrays [heads, rows, 2, head_dim * element bytes]."""
+        eb = {DSA_BF16: 2, DSA_F32: 4, DSA_FP8_E4M3: 1}[self.dtype_code]
+        pre = np.zeros((self.heads, self.L_p + self.sink, 2, self.head_dim * eb), dtype=np.uint8)
+        ring = np.zeros((self.heads, self.N_r - self.sink, 2, self.head_dim * eb), dtype=np.uint8)
+        _check(dsa_debug_copy_state(self.h, pre, ring), "dsa_debug_copy_state")
+        return pre, ring
 
     def set_splits(self, nsplit: int):
         _check(dsa_set_splits(self.h, nsplit), "dsa_set_splits")

@@ -43,7 +43,8 @@ class Workload:
     layers: int
     heads: int
     head_dim: int
-    dtype: str          # "f32" or "bf16": element type of q, k, v, out and the KV state
+    dtype: str          # "f32" / "bf16": element type of q, k, v, out and the KV state;
+                        # "fp8e4m3": KV state in FP8 E4M3 with per-stream scales, q, k, v, out bf16
     L_p: int
     grid: int           # L_dec = grid * grid
     N_r: int
@@ -64,6 +65,10 @@ class Workload:
     def dense(self) -> "Workload":
         """The 0 % sparsity setting of the same kernel: no eviction, no skip."""
         return replace(self, name=self.name + "-dense", N_r=self.L_dec, N_att=self.L_dec, sink=0)
+
+    def fp8(self) -> "Workload":
+        """The same workload with the KV state stored as FP8 E4M3."""
+        return replace(self, name=self.name + "-fp8", dtype="fp8e4m3")
 
     def with_batch(self, batch: int) -> "Workload":
         return replace(self, name=f"{self.name.rsplit('-b', 1)[0]}-b{batch}", batch=batch)
@@ -101,7 +106,8 @@ WORKLOADS = {
 
 
 def torch_dtype(name: str) -> torch.dtype:
-    return {"f32": torch.float32, "bf16": torch.bfloat16}[name]
+    """Element type of the q, k, v, prompt and out tensors of a workload dtype."""
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "fp8e4m3": torch.bfloat16}[name]
 
 
 def _rope(x: torch.Tensor, pos: torch.Tensor) -> torch.Tensor:
@@ -145,8 +151,18 @@ class TraceGen:
         g.manual_seed(((self.seed * 1009 + self.layer) * 7 + kind) * 1_000_003 + step)
         return g
 
+    def kv_scales(self):
+        """Per-stream K and V scales of FP8 storage, float32 [S] each: 2^-5
+        times a seeded factor in [1, 1.5), so the largest E4M3 value (448)
+        maps to 14..21, above the generated magnitudes, and the smallest
+        normal one to about 5e-4."""
+        g = self._gen(3, 0)
+        u = torch.rand((2, self.S), generator=g, device=self.device, dtype=torch.float32)
+        sc = (2.0 ** -5) * (1.0 + 0.5 * u)
+        return sc[0].cpu().numpy(), sc[1].cpu().numpy()
+
     def prompt(self):
-        """Prompt K, V as [S, L_p, d] in the workload dtype."""
+        """Prompt K, V as [S, L_p, d] in the workload's input dtype."""
         wl = self.wl
         g = self._gen(1, 0)
         shape = (self.S, wl.L_p, wl.head_dim)

@@ -182,7 +182,10 @@ class OracleArm:
         self.gen = TraceGen(wl.with_batch(max(1, (n + wl.heads - 1) // wl.heads)), layer=0, device=device)
         self.n = min(n, self.gen.S)
         self.threads = max_threads()
-        self.orc = OracleBatch(self.n, wl.head_dim, wl.L_p, wl.N_r, wl.N_att, wl.sink)
+        ks = vs = None
+        if wl.dtype == "fp8e4m3":
+            ks, vs = (x[: self.n] for x in self.gen.kv_scales())
+        self.orc = OracleBatch(self.n, wl.head_dim, wl.L_p, wl.N_r, wl.N_att, wl.sink, k_scales=ks, v_scales=vs)
         Kp, Vp = self.gen.prompt()
         self.orc.prefill(Kp[: self.n].double().cpu().numpy(), Vp[: self.n].double().cpu().numpy())
         self.t = 0
@@ -243,6 +246,8 @@ class Stack:
         for layer in range(wl.layers):
             gen = TraceGen(wl, layer=layer, device=device)
             h = DSA(wl.streams, wl.head_dim, wl.L_p, wl.N_r, wl.N_att, wl.sink, wl.dtype)
+            if wl.dtype == "fp8e4m3":
+                h.set_kv_scales(*gen.kv_scales())
             Kp, Vp = gen.prompt()
             h.prefill(Kp, Vp)
             self.handles.append(h)
@@ -449,7 +454,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     peak, peak_kind = measured_peak()
     achieved = plan.algo_bytes / (per_launch_ms / 1e3) / 1e9
     whole = plan.algo_bytes * wl.layers * args.steps * ws / (el_ms / 1e3) / 1e9
-    traffic = profiled_traffic(args.workload)
+    traffic = profiled_traffic(wl.name)
 
     # --- end to end through the public API with host buffers
     e2e_steps = max(3, min(args.steps // 4, 100))
@@ -506,7 +511,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": workload_config(wl, f"phase-3 steady state from t = {t_start}"),
         "hbm_gbs": whole,
-        "roofline": {"bound": "hbm", "kernel": f"dsa::decode_kernel<bf16,128,{plan.pipeline - 1}>",
+        "roofline": {"bound": "hbm", "kernel": f"dsa::decode_kernel<{wl.dtype},{wl.head_dim},{plan.pipeline - 1}>",
                      "achieved": achieved,
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -587,6 +592,8 @@ def _workload(args):
     wl = WORKLOADS[args.workload]
     if args.layers:
         wl = replace(wl, layers=args.layers)
+    if args.kv == "fp8":
+        wl = wl.fp8()
     return wl
 
 
@@ -610,6 +617,8 @@ def run_sweep(args) -> None:
     layers = args.layers or 4
     for key in (args.sweep_only.split(",") if args.sweep_only else SWEEP):
         base = replace(WORKLOADS[key], layers=layers)
+        if args.kv == "fp8":
+            base = base.fp8()
         for dense in (False, True):
             wl = base.dense() if dense else base
             if dense and key == "stress-s95":
@@ -661,6 +670,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-streams", type=int, default=256, help="streams per step of the reference arm")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
+    ap.add_argument("--kv", choices=["native", "fp8"], default="native",
+                    help="fp8: store the KV state as FP8 E4M3 (q, k, v, out stay bf16)")
     ap.add_argument("--sweep", action="store_true", help="time every workload family (one JSON line each)")
     ap.add_argument("--sweep-only", default="", help="comma-separated workloads for --sweep")
     ap.add_argument("--splits", type=int, default=0, help="--sweep: force this many work items per stream")

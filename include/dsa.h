@@ -23,7 +23,9 @@
  *   all device work on that stream and never synchronizes it, except in the
  *   functions documented as synchronous.
  * - Element type: DSA_BF16 (q, k, v, out and the stored KV are bf16,
- *   arithmetic in fp32) or DSA_F32 (all fp32).
+ *   arithmetic in fp32), DSA_F32 (all fp32) or DSA_FP8_E4M3 (the stored KV
+ *   is FP8 E4M3 with per-stream scales, see dsa_set_kv_scales; q, k_new,
+ *   v_new, the prompt K / V and out are bf16; arithmetic in fp32).
  * - Ownership: the library owns every state buffer of a handle (prompt
  *   prefix, decode ring, skip bitmask, split partials) and frees them in
  *   dsa_destroy.  The caller owns q / k_new / v_new / out / K / V and must
@@ -59,7 +61,7 @@ enum dsa_status {
     DSA_ERR_DEVICE_CHECK = -6  /* device: an internal consistency check failed */
 };
 
-enum dsa_dtype { DSA_BF16 = 0, DSA_F32 = 1 };
+enum dsa_dtype { DSA_BF16 = 0, DSA_F32 = 1, DSA_FP8_E4M3 = 2 };
 
 /*
  * dsa_create / dsa_create_ex -- allocate the state of `heads` streams.
@@ -91,8 +93,9 @@ int dsa_create_ex(int heads, int head_dim, int L_p, int N_r, int N_att, int sink
  * prompt KV is always attended in full ("Throughout all phases, the prompt
  * KV is always attended in full").
  *
- * K, V: device, [heads, L_p, head_dim] of the handle's dtype (may be NULL
- * when L_p = 0).  Asynchronous on `stream`.
+ * K, V: device, [heads, L_p, head_dim] of the handle's dtype (bf16 for
+ * DSA_FP8_E4M3, which stores them as E4M3 codes with the handle's scales;
+ * may be NULL when L_p = 0).  Asynchronous on `stream`.
  */
 int dsa_prefill(dsa_handle h, const void *K, const void *V, void *stream);
 
@@ -154,7 +157,8 @@ const char *dsa_last_error(void);
 /*
  * dsa_state_bytes -- device bytes of the persistent state of a handle:
  * prompt prefix (L_p + sink rows) and decode ring (N_r - sink slots) of K
- * and V, plus the skip bitmask, per stream.  This is the KV footprint bound
+ * and V (1 byte per element for DSA_FP8_E4M3), plus the skip bitmask, per
+ * stream.  This is the KV footprint bound
  * N_r + L_p of the cost analysis (section 4).  Split partials are extra.
  * Returns 0 for invalid arguments.
  */
@@ -217,6 +221,22 @@ int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r, int N_att
                             void *prefix, void *ring, uint32_t *mask, int32_t *last_sel, const void *q,
                             const void *k_new, const void *v_new, void *out, void *stream);
 
+/*
+ * dsa_set_kv_scales -- per-stream scales of a DSA_FP8_E4M3 handle.  The
+ * paper treats KV quantization as orthogonal to the method and applicable
+ * on top of it (section 6, Related Works, "KV quantization for LLM") and
+ * fixes no format; this library stores every K and V row (prompt, sinks,
+ * decode entries) as OCP FP8 E4M3 codes: the code of an element x is the
+ * E4M3 value nearest to fp32(x) * fp32(1 / scale) (ties to even; magnitudes
+ * beyond 448 saturate to 448), and the attention uses code * scale.
+ * k_scale, v_scale: host, [heads] float, each positive and finite (default
+ * 1.0 for every stream).  Synchronizes the device, and discards the stored
+ * sequence (its rows were coded with the old scales): dsa_prefill must
+ * follow before the next decode step.  DSA_ERR_ARG for other dtypes or bad
+ * values.  Not on the decode path.
+ */
+int dsa_set_kv_scales(dsa_handle h, const float *k_scale, const float *v_scale);
+
 /* Tuning and test knobs (not needed for normal use). */
 
 /* Force the number of work items (pieces) per stream (>= 1), or 0 for the
@@ -231,6 +251,14 @@ int dsa_set_splits(dsa_handle h, int nsplit);
  * fp32 rounding order (selections are identical).  DSA_ERR_ARG for other
  * values or a shape the device cannot launch. */
 int dsa_set_pipeline(dsa_handle h, int pipeline);
+
+/* Copy the stored KV state to host memory (synchronizes the device): the
+ * prompt prefix [heads, L_p + sink, 2, head_dim] and the decode ring
+ * [heads, N_r - sink, 2, head_dim] (decode position p in slot (p - sink)
+ * mod (N_r - sink)), in the stored element type (E4M3 codes for
+ * DSA_FP8_E4M3).  Either pointer may be NULL.  Used by the tests to check
+ * stored values bit for bit. */
+int dsa_debug_copy_state(dsa_handle h, void *host_prefix, void *host_ring);
 
 /* Poll limit of the bounded waits inside the decode kernel (default: none;
  * every wait still gives up after about one second).  A limit of 0 makes

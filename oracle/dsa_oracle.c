@@ -40,8 +40,9 @@
  *     held stays <= N_r + L_p and the attended decode rows stay <= N_att.
  *     With N_att = N_r this is StreamingLLM with `sink` sinks.
  *
- * FP8 KV storage (orc_set_kv_fp8).  The pages note that KV quantization is
- * orthogonal to the method and stacks with it, and fix no scheme.  The
+ * FP8 KV storage (orc_set_kv_fp8).  Section 6 (Related Works, "KV
+ * quantization for LLM") calls KV quantization orthogonal to the method and
+ * applicable on top of it, and fixes no scheme.  The
  * reading taken: every K and V row the cache holds (prompt rows, sink rows,
  * decode rows) is stored as OCP FP8 E4M3 codes with one fp32 scale per
  * stream for K and one for V; the stored code of an element x is the E4M3

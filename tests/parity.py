@@ -2,7 +2,8 @@
 
 Both sides see the same seeded inputs: the device draws them, and the
 sampled streams' exact values (bf16 or fp32, widened to fp64) are copied to
-the oracle.  Per step the harness checks
+the oracle.  For FP8 storage both sides get the same per-stream scales and
+each quantizes the rows itself.  Per step the harness checks
 
 * outputs: max |out - oracle| <= 2e-3 + 1e-2 |oracle| elementwise;
 * selections: the relative offset the kernel appended equals the oracle's
@@ -56,7 +57,8 @@ def mask_offsets(words: np.ndarray) -> set[int]:
 
 def run_parity(wl: Workload, steps: int | None = None, sample: list[int] | None = None,
                splits: int = 0, mask_every: int = 1, layer: int = 0, device: str = "cuda",
-               gen_device: str | None = None, threads: int = 1, pipeline: int = 0) -> ParityReport:
+               gen_device: str | None = None, threads: int = 1, pipeline: int = 0,
+               kv_scales=None) -> ParityReport:
     """Runs `steps` decode steps of one layer of `wl` on the GPU and the
     sampled streams on the oracle; returns the report (does not raise)."""
     from ar_image_gen_gb300.dsa import DSA
@@ -73,7 +75,12 @@ def run_parity(wl: Workload, steps: int | None = None, sample: list[int] | None 
         h.set_splits(splits)
     if pipeline:
         h.set_pipeline(pipeline)
-    orc = OracleBatch(len(sample), d, wl.L_p, wl.N_r, wl.N_att, wl.sink)
+    ks = vs = None
+    if wl.dtype == "fp8e4m3":
+        ks, vs = kv_scales if kv_scales is not None else gen.kv_scales()
+        h.set_kv_scales(ks, vs)
+        ks, vs = ks[sample], vs[sample]
+    orc = OracleBatch(len(sample), d, wl.L_p, wl.N_r, wl.N_att, wl.sink, k_scales=ks, v_scales=vs)
 
     Kp, Vp = gen.prompt()
     Kp_d, Vp_d = Kp.to(device), Vp.to(device)
