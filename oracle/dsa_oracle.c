@@ -476,3 +476,80 @@ int orc_max_threads(void)
     return 1;
 #endif
 }
+
+/* ---- Diagnostics of dense decode attention over one stream's trace
+ * (section 3.3, "Skewed attention toward prompt and local tokens" with
+ * Fig. 8, and "Diagonal attention sparsity pattern" with Fig. 10).
+ *
+ * Query i (decode step i, 0-based) attends the L_p prompt keys and decode
+ * keys 0..i with weights w_i = softmax(q_i k^T / sqrt(d)).
+ *   mass[3 i + 0..2]: the weight on the prompt keys, on the local keys (the
+ *     most recent ceil(0.1 (i + 1)) decoded keys, the current one included)
+ *     and on the middle keys (the other decoded keys);
+ *   for each distance dist[k], summed over the queries i = 0 .. L_dec - 1 -
+ *     dist[k]: vsum[k] += cos(w_i[0..i], w_{i+d}[0..i]) (vertical: the same
+ *     keys) and dsum[k] += cos(w_i[0..i], w_{i+d}[d..i+d]) (diagonal: keys
+ *     shifted by d), over decode keys only.
+ * Returns 0, or -1 on bad arguments / allocation failure.
+ * orc_diag_set_mutation plants a mistake for the pin tests (0: faithful):
+ * 1 the local window is floor(0.1 (i + 1)) keys, 2 the diagonal shift is
+ * applied to query i instead of i + d, 3 the score vectors include the
+ * prompt keys. */
+static int g_diag_mutation;
+void orc_diag_set_mutation(int m) { g_diag_mutation = m; }
+
+int orc_diag_stream(int d, int L_p, int L_dec, const double *Q, const double *Kp, const double *Kd,
+                    int n_dist, const int *dist, double *mass, double *vsum, double *dsum)
+{
+    if (d < 1 || L_p < 0 || L_dec < 1 || n_dist < 0) return -1;
+    const int pw = g_diag_mutation == 3 ? L_p : 0;  /* prompt columns kept in w (planted mistake only) */
+    const int W = pw + L_dec;
+    double *w = (double *)calloc((size_t)L_dec * W, sizeof(double)); /* weights of query i, row i */
+    double *z = (double *)malloc(sizeof(double) * (size_t)(L_p + L_dec));
+    if (!w || !z) { free(w); free(z); return -1; }
+    const double scale = 1.0 / sqrt((double)d);
+    for (int i = 0; i < L_dec; ++i) {
+        const double *q = Q + (size_t)i * d;
+        const int n = L_p + i + 1;
+        double m = -INFINITY;
+        for (int j = 0; j < n; ++j) {
+            const double *k = j < L_p ? Kp + (size_t)j * d : Kd + (size_t)(j - L_p) * d;
+            z[j] = dot(q, k, d) * scale;
+            if (z[j] > m) m = z[j];
+        }
+        double total = 0.0;
+        for (int j = 0; j < n; ++j) { z[j] = exp(z[j] - m); total += z[j]; }
+        const int n_local = g_diag_mutation == 1 ? (i + 1) / 10 : (i + 1 + 9) / 10;
+        double mp = 0.0, ml = 0.0, mm = 0.0;
+        for (int j = 0; j < n; ++j) {
+            const double p = z[j] / total;
+            if (j < L_p) mp += p;
+            else if (j - L_p > i - n_local) ml += p;
+            else mm += p;
+            if (j >= L_p - pw) w[(size_t)i * W + (j - (L_p - pw))] = p;
+        }
+        mass[3 * i] = mp; mass[3 * i + 1] = ml; mass[3 * i + 2] = mm;
+    }
+    for (int k = 0; k < n_dist; ++k) {
+        const int dd = dist[k];
+        vsum[k] = dsum[k] = 0.0;
+        for (int i = 0; i + dd < L_dec; ++i) {
+            const double *a = w + (size_t)i * W, *b = w + (size_t)(i + dd) * W;
+            double aa = 0.0, bv = 0.0, bd = 0.0, ab_v = 0.0, ab_d = 0.0;
+            for (int j = 0; j <= i + pw; ++j) {
+                /* planted mistake 2: query i's keys shifted instead of query i + d's */
+                const double ad = (g_diag_mutation == 2) ? (j + dd <= i + pw ? a[j + dd] : 0.0) : a[j];
+                const double bdj = (g_diag_mutation == 2) ? b[j] : b[j + dd];
+                aa += a[j] * a[j];
+                bv += b[j] * b[j];
+                bd += bdj * bdj;
+                ab_v += a[j] * b[j];
+                ab_d += ad * bdj;
+            }
+            vsum[k] += ab_v / sqrt(aa * bv);
+            dsum[k] += ab_d / sqrt(aa * bd);
+        }
+    }
+    free(w); free(z);
+    return 0;
+}

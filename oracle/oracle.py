@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
         L.orc_e4m3_encode.restype = ctypes.c_ubyte
         L.orc_e4m3_decode.argtypes = [ctypes.c_ubyte]
         L.orc_e4m3_decode.restype = ctypes.c_double
+        L.orc_diag_stream.argtypes = [ctypes.c_int] * 3 + [dp] * 3 + [ctypes.c_int, ip, dp, dp, dp]
+        L.orc_diag_set_mutation.argtypes = [ctypes.c_int]
         _lib = L
     return _lib
 
@@ -211,3 +213,32 @@ class OracleBatch:
 
 def max_threads() -> int:
     return int(lib().orc_max_threads())
+
+
+DIAG_MUTATIONS = {"local_floor": 1, "shift_query": 2, "with_prompt": 3}
+
+
+def diag_set_mutation(name: str | None) -> None:
+    """Plants a mistake in the diagnostics (pin tests only); None restores."""
+    lib().orc_diag_set_mutation(DIAG_MUTATIONS[name] if name else 0)
+
+
+def diag_stream(Q, Kp, Kd, dists):
+    """Fig. 8 / Fig. 10 diagnostics of one stream's dense trace (see
+    orc_diag_stream): returns (mass [L_dec, 3], vertical [n], diagonal [n]),
+    the similarities averaged over the queries i = 0 .. L_dec - 1 - d."""
+    Q = np.ascontiguousarray(Q, dtype=np.float64)
+    Kd = np.ascontiguousarray(Kd, dtype=np.float64)
+    Kp = np.ascontiguousarray(Kp, dtype=np.float64).reshape(-1, Q.shape[1])
+    L_dec, d = Q.shape
+    dist = np.ascontiguousarray(dists, dtype=np.int32)
+    if (dist < 1).any() or (dist >= L_dec).any():
+        raise ValueError("distances must lie in [1, L_dec)")
+    mass = np.zeros((L_dec, 3)); vs = np.zeros(len(dist)); ds = np.zeros(len(dist))
+    r = lib().orc_diag_stream(d, Kp.shape[0], L_dec, _dptr(Q), _dptr(Kp if Kp.size else np.zeros(1)), _dptr(Kd),
+                              len(dist), dist.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), _dptr(mass), _dptr(vs),
+                              _dptr(ds))
+    if r != 0:
+        raise RuntimeError("oracle diagnostics failed")
+    cnt = L_dec - dist
+    return mass, vs / cnt, ds / cnt
