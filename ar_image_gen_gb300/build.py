@@ -10,9 +10,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libdsa.so")
-SOURCES = [os.path.join(CSRC, "dsa_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("dsa_decode.cuh", "dsa_ptx.cuh")] + [
-    os.path.join(ROOT, "include", "dsa.h")]
+SOURCES = [os.path.join(CSRC, "dsa_api.cu"), os.path.join(CSRC, "dsa_diag.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("dsa_decode.cuh", "dsa_ptx.cuh", "dsa_internal.h")] + [
+    os.path.join(ROOT, "include", h) for h in ("dsa.h", "dsa_diag.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -30,17 +30,37 @@ def build(force: bool = False, verbose: bool = False) -> str:
         newest = max(os.path.getmtime(p) for p in DEPS)
         if os.path.getmtime(LIB) >= newest:
             return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), "-O3", "-std=c++17", *ARCH, "-lineinfo", "-shared", "-Xcompiler", "-fPIC",
-           "-o", tmp, *SOURCES]
+    tag = f".tmp{os.getpid()}"
+    base = [nvcc(), "-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC"]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError(f"nvcc failed ({' '.join(cmd)}):\n{res.stderr}")
-    if verbose:
-        print(res.stderr)
-    os.replace(tmp, LIB)
+        base.insert(1, "-Xptxas=-v")
+    # one object per translation unit, compiled in parallel, then linked
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = os.path.join(LIBDIR, os.path.basename(src) + tag + ".o")
+        cmd = base + ["-c", "-o", obj, src]
+        procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)))
+        objs.append(obj)
+    errors = []
+    for cmd, p in procs:
+        out, err = p.communicate()
+        if p.returncode != 0:
+            errors.append(f"nvcc failed ({' '.join(cmd)}):\n{err}")
+        elif verbose:
+            print(err)
+    try:
+        if errors:
+            raise RuntimeError("\n".join(errors))
+        tmp = LIB + tag
+        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"nvcc link failed ({' '.join(cmd)}):\n{res.stderr}")
+        os.replace(tmp, LIB)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return LIB
 
 

@@ -20,11 +20,14 @@
 
 #include "../../include/dsa.h"
 #include "dsa_decode.cuh"
+#include "dsa_internal.h"
 
 namespace {
-
 thread_local std::string g_err;
 std::atomic<int> g_fail_after{0};
+}  // namespace
+
+namespace dsa_detail {
 
 int fail(int code, const char *fmt, ...)
 {
@@ -64,6 +67,14 @@ int dev_alloc(void **p, size_t bytes, const char *what)
     }
     return DSA_OK;
 }
+
+}  // namespace dsa_detail
+
+namespace {
+
+using dsa_detail::cuda_fail;
+using dsa_detail::dev_alloc;
+using dsa_detail::fail;
 
 constexpr uint32_t kMagic = 0x44534131u;  // "DSA1"
 constexpr uint32_t kDefaultWaitLimit = 0xffffffffu;

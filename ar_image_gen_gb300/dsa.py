@@ -45,7 +45,7 @@ EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa
            "dsa_get_skip_mask", "dsa_get_last_selection", "dsa_sync_status", "dsa_last_error",
            "dsa_state_bytes", "dsa_plan_step", "dsa_set_kv_scales", "dsa_set_splits", "dsa_set_pipeline",
            "dsa_set_wait_limit", "dsa_debug_copy_state",
-           "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc"]
+           "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc", "dsa_diag_trace"]
 
 
 class dsa_step_plan(ctypes.Structure):
@@ -77,6 +77,7 @@ _L.dsa_set_pipeline.argtypes = [_P, _I]
 _L.dsa_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
 _L.dsa_debug_fail_alloc_after.argtypes = [_I]
 _L.dsa_decode_step_noalloc.argtypes = [_I] * 8 + [_P] * 9
+_L.dsa_diag_trace.argtypes = [_I] * 5 + [_P] * 3 + [_I] + [_P] * 6
 
 
 class DSAError(RuntimeError):
@@ -208,6 +209,31 @@ def dsa_decode_step_noalloc(heads, head_dim, L_p, N_r, N_att, sink, dtype, t, pr
     return _L.dsa_decode_step_noalloc(heads, head_dim, L_p, N_r, N_att, sink, dtype, t, _ptr(prefix), _ptr(ring),
                                       _ptr(mask), _ptr(last_sel), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
                                       _stream(stream))
+
+
+def dsa_diag_trace(heads, head_dim, L_p, L_dec, dtype, Q, Kp, Kd, dist: np.ndarray, step_mass, mass_mean: np.ndarray,
+                   vertical: np.ndarray, diagonal: np.ndarray, stream=None) -> int:
+    return _L.dsa_diag_trace(heads, head_dim, L_p, L_dec, dtype, _ptr(Q), _ptr(Kp), _ptr(Kd), len(dist), _ptr(dist),
+                             _ptr(step_mass), _ptr(mass_mean), _ptr(vertical), _ptr(diagonal), _stream(stream))
+
+
+def diag_trace(Q, Kp, Kd, dists, step_mass=None, stream=None):
+    """Fig. 8 / Fig. 10 diagnostics of a dense decode trace (include/dsa_diag.h).
+    Q, Kd: [heads, L_dec, d], Kp: [heads, L_p, d] device tensors (bf16 or fp32).
+    Returns (mass_mean [3], vertical [n], diagonal [n]) as numpy arrays;
+    step_mass, if given, is a device float tensor [heads, L_dec, 3] to fill."""
+    import torch
+
+    heads, L_dec, d = Q.shape
+    L_p = Kp.shape[1] if Kp is not None else 0
+    dtype = {torch.bfloat16: DSA_BF16, torch.float32: DSA_F32}[Q.dtype]
+    dist = np.ascontiguousarray(dists, dtype=np.int32)
+    mass = np.zeros(3)
+    vert = np.zeros(len(dist))
+    diag = np.zeros(len(dist))
+    _check(dsa_diag_trace(heads, d, L_p, L_dec, dtype, Q, Kp if L_p > 0 else None, Kd, dist, step_mass, mass, vert,
+                          diag, stream), "dsa_diag_trace")
+    return mass, vert, diag
 
 
 # ---- convenience wrapper ---------------------------------------------------

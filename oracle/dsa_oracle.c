@@ -478,7 +478,8 @@ int orc_max_threads(void)
 }
 
 /* ---- Diagnostics of dense decode attention over one stream's trace
- * (section 3.3, "Skewed attention toward prompt and local tokens" with
+ * (section 3.4 "Attention Sparsity Analysis": "Skewed attention toward
+ * prompt and local tokens" with
  * Fig. 8, and "Diagonal attention sparsity pattern" with Fig. 10).
  *
  * Query i (decode step i, 0-based) attends the L_p prompt keys and decode

@@ -1,5 +1,5 @@
 """The C-ABI library without a GPU: it builds, loads, exports every symbol
-include/dsa.h declares, and rejects bad arguments on the host."""
+the headers in include/ declare, and rejects bad arguments on the host."""
 import ctypes
 import os
 import re
@@ -19,9 +19,13 @@ def dsa():
 
 
 def declared_functions():
-    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
@@ -78,3 +82,19 @@ def test_state_bytes_is_the_kv_bound(dsa):
     assert dsa.dsa_state_bytes(S, d, L_p, N_r, 4, dsa.DSA_BF16) == S * ((L_p + N_r) * row + 9 * 4)
     assert dsa.dsa_state_bytes(4, 64, 16, 32, 0, dsa.DSA_F32) == 4 * (48 * 2 * 64 * 4 + 4)
     assert dsa.dsa_state_bytes(0, 128, 64, 288, 0, 0) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(heads=0), dict(head_dim=96), dict(L_p=-1), dict(L_dec=0), dict(dtype=2), dict(dist=[0]), dict(dist=[40]),
+])
+def test_diag_rejects_bad_arguments(dsa, kw):
+    import numpy as np
+
+    a = dict(heads=2, head_dim=64, L_p=4, L_dec=40, dtype=dsa.DSA_BF16, dist=[1, 3])
+    a.update(kw)
+    dist = np.array(a["dist"], dtype=np.int32)
+    z = np.zeros(8)
+    fake = 1 << 20  # never dereferenced: every case fails validation first
+    rc = dsa.dsa_diag_trace(a["heads"], a["head_dim"], a["L_p"], a["L_dec"], a["dtype"], fake, fake, fake, dist, None,
+                            z, z, z)
+    assert rc == dsa.DSA_ERR_ARG and "dsa_diag_trace" in dsa.dsa_last_error()

@@ -1,4 +1,4 @@
-"""Pins of the oracle's attention diagnostics (section 3.3: Fig. 8 attention
+"""Pins of the oracle's attention diagnostics (section 3.4: Fig. 8 attention
 mass split, Fig. 10 vertical vs diagonal score-vector similarity), without
 a GPU.  Closed forms fix each part: uniform attention gives the masses
 exactly; logits that depend only on i - j (RoPE-rotated constant vectors)
