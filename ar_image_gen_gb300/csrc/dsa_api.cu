@@ -19,6 +19,7 @@
 #include <string>
 
 #include "../../include/dsa.h"
+#include "../../include/dsa_proj.h"
 #include "dsa_decode.cuh"
 #include "dsa_internal.h"
 
@@ -666,7 +667,12 @@ int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out)
     return DSA_OK;
 }
 
-int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *v_new, void *out, void *stream)
+}  // extern "C"
+
+namespace {
+
+// Host checks of a decode step that come before any launch.
+int check_step(dsa_handle h, const void *q, const void *k_new, const void *v_new, void *out)
 {
     if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
     if (!h->prefilled) return fail(DSA_ERR_STATE, "dsa_decode_step before dsa_prefill");
@@ -674,6 +680,16 @@ int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out))
         return fail(DSA_ERR_ARG, "q, k_new, v_new and out must be 16-byte aligned");
     if (h->t == INT_MAX) return fail(DSA_ERR_STATE, "decode step counter exhausted");
+    return DSA_OK;
+}
+
+// The decode launch(es) of one step.  after_proj: the kernel just before in
+// the stream is the projection of this step, which touches none of the
+// handle's state and lets its dependents start only after the kernel before
+// it has completed, so the state may be read before the grid dependency wait.
+int launch_decode_step(dsa_handle h, const void *q, const void *k_new, const void *v_new, void *out,
+                       cudaStream_t st, bool after_proj)
+{
     const Plan pl = make_plan(h, h->t);
     if ((long long)pl.nsplit * h->S > INT_MAX) return fail(DSA_ERR_ARG, "grid too large");
     int rc = ensure_partials(h, pl.nsplit);
@@ -716,13 +732,46 @@ int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *
     p.vinv = h->scales ? h->scales + 3 * (size_t)h->S : nullptr;
     p.wait_limit = h->wait_limit;
 
-    cudaStream_t st = (cudaStream_t)stream;
-    p.early = note_launch(st, h) ? 1 : 0;
+    const bool other = note_launch(st, h);
+    p.early = (other || after_proj) ? 1 : 0;
     cudaError_t e = launch_step(h->dtype, h->D, pl.shape, p, h->ring_map, pl.grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     h->last_select = pl.select;
     h->t += 1;
     return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dsa_decode_step(dsa_handle h, const void *q, const void *k_new, const void *v_new, void *out, void *stream)
+{
+    int rc = check_step(h, q, k_new, v_new, out);
+    if (rc != DSA_OK) return rc;
+    return launch_decode_step(h, q, k_new, v_new, out, (cudaStream_t)stream, false);
+}
+
+int dsa_decode_step_fused(dsa_handle h, dsa_proj pr, const void *x, const void *W, void *out, void *stream)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    int batch = 0, heads = 0, hd = 0;
+    int rc = dsa_detail::proj_shape(pr, &batch, &heads, &hd);
+    if (rc != DSA_OK) return rc;
+    if (h->dtype != DSA_BF16 && h->dtype != DSA_FP8_E4M3)
+        return fail(DSA_ERR_ARG, "dsa_decode_step_fused needs a DSA_BF16 or DSA_FP8_E4M3 handle");
+    if ((long long)batch * heads != h->S || hd != h->D)
+        return fail(DSA_ERR_ARG, "handle (%d streams of %d) and projection (%d x %d heads of %d) do not match", h->S,
+                    h->D, batch, heads, hd);
+    void *q = nullptr, *k = nullptr, *v = nullptr;
+    dsa_detail::proj_staging(pr, &q, &k, &v);
+    rc = check_step(h, q, k, v, out);
+    if (rc != DSA_OK) return rc;
+    if ((long long)h->L_p + h->t > INT_MAX) return fail(DSA_ERR_STATE, "position out of range");
+    cudaStream_t st = (cudaStream_t)stream;
+    rc = dsa_detail::proj_launch(pr, x, W, h->L_p + h->t, q, k, v, st);
+    if (rc != DSA_OK) return rc;
+    return launch_decode_step(h, q, k, v, out, st, true);
 }
 
 int dsa_get_step(dsa_handle h, int *t)

@@ -1,16 +1,25 @@
 // dsa_internal.h -- helpers shared by the library's translation units
 // (error messages for dsa_last_error(), device allocation with the test
-// hook of dsa_debug_fail_alloc_after()).  Not part of the C ABI.
+// hook of dsa_debug_fail_alloc_after(), the projection behind
+// dsa_decode_step_fused()).  Not part of the C ABI.
 #pragma once
 
 #include <cuda_runtime.h>
 
 #include <cstddef>
 
+struct dsa_proj_ctx;
+
 namespace dsa_detail {
 
 __attribute__((visibility("hidden"))) int fail(int code, const char *fmt, ...);
 __attribute__((visibility("hidden"))) int cuda_fail(cudaError_t e, const char *what);
 __attribute__((visibility("hidden"))) int dev_alloc(void **p, size_t bytes, const char *what);
+
+// The QKV projection (dsa_proj.cu) as the fused decode step uses it.
+__attribute__((visibility("hidden"))) int proj_shape(const dsa_proj_ctx *p, int *batch, int *heads, int *head_dim);
+__attribute__((visibility("hidden"))) void proj_staging(const dsa_proj_ctx *p, void **q, void **k, void **v);
+__attribute__((visibility("hidden"))) int proj_launch(dsa_proj_ctx *p, const void *x, const void *W, int pos, void *q,
+                                                      void *k, void *v, cudaStream_t st);
 
 }  // namespace dsa_detail

@@ -1,0 +1,614 @@
+// dsa_proj.cu -- QKV projection with rotary position embedding on the
+// tensor cores, feeding a decode step ("Understanding and Exploiting Diagonal
+// Attention Sparsity in Autoregressive Image Generation", section 2,
+// "LLM-aligned decoding behavior", and section 5.3, Fig. 16(b)).  C ABI in
+// include/dsa_proj.h.
+//
+// One launch computes Y^T = W x^T for one decode step: the 3 H d output
+// features are the MMA's M dimension (tiles of 128, each one head's q, k or v
+// at head_dim 128, two heads at 64) and the batch is its N dimension (padded
+// to a multiple of 16), so a batch of a few dozen tokens still fills the
+// 128-row tensor-core tile.  At decode batch sizes the launch streams W once
+// from HBM (2 bytes per weight against 2 B flops), so it is bound by HBM,
+// not by the tensor cores; what matters is keeping every SM's copies in
+// flight.  The work (tiles x k-blocks of 64) is divided evenly over a
+// persistent grid of one CTA per SM (stream-K): a CTA takes a contiguous run
+// of k-blocks, which may end inside one tile and begin inside another.  A
+// tile finished by one CTA is written directly; a tile shared by several
+// CTAs has each CTA write an fp32 partial, and the last to finish (a counter
+// per tile) sums the partials in segment order (deterministic) and writes
+// the tile.
+//
+// CTA of 6 warps: warp 0 issues the TMA loads of W and x tiles (128-byte
+// swizzle) into a ring of shared-memory stages, warp 1 issues tcgen05.mma
+// (M 128, N = padded batch, K 16; fp32 accumulator in tensor memory), warps
+// 2-5 drain the accumulator with tcgen05.ld (warp w reads TMEM lanes
+// 32 (w % 4) ..), apply RoPE (a head's halves exchange through shared
+// memory) and store bf16.  Every mbarrier wait is bounded; a wait that gives
+// up sets a status bit and the CTA drains its copies and MMAs and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "../../include/dsa.h"
+#include "../../include/dsa_proj.h"
+#include "dsa_decode.cuh"
+#include "dsa_internal.h"
+#include "dsa_tc.cuh"
+
+namespace dsa_proj_k {
+
+using namespace dsa;
+
+constexpr int kThreads = 192;  // producer warp, MMA warp, 4 epilogue warps
+constexpr int kBM = 128;       // output features per tile
+constexpr int kBK = 64;        // hidden elements per k-block (one 128-byte swizzled row)
+constexpr int kUK = 16;        // K of one tcgen05.mma kind::f16
+constexpr int kATile = kBM * kBK * 2;
+constexpr int kMaxBatch = 256;
+constexpr int kEpiThreads = 128;
+constexpr int kChunk = 16;     // accumulator columns per tcgen05.ld
+constexpr uint32_t kEpiBar = 1;
+
+struct ProjParams {
+    __nv_bfloat16 *q, *k, *v;  // [B, HD] each
+    float *part;               // [2 * grid][npad][128] partials of split tiles
+    int *counters;             // [tiles] finished segments per split tile
+    int *status;
+    int B, npad, HD, D, tiles, kblocks, stages, tmem_cols;
+    int pos;
+    uint32_t wait_limit;
+    double inv_freq[64];       // 10000^(-2j/D), j < D/2
+};
+
+// The CTA whose k-block run [start(c), start(c + 1)) holds work unit u,
+// with start(c) = c U / G.
+__device__ __forceinline__ int owner(long long u, long long U, int G)
+{
+    return (int)(((u + 1) * G + U - 1) / U) - 1;
+}
+__device__ __forceinline__ long long run_start(int c, long long U, int G) { return (long long)c * U / G; }
+
+struct Seg {
+    int tile, kb0, kb1;  // k-blocks [kb0, kb1) of `tile`
+    int first, nseg;     // CTAs sharing the tile: first, count
+};
+
+__device__ __forceinline__ Seg make_seg(long long u, long long u1, const ProjParams &p, long long U, int G)
+{
+    Seg s;
+    s.tile = (int)(u / p.kblocks);
+    s.kb0 = (int)(u - (long long)s.tile * p.kblocks);
+    const long long tile_end = (long long)(s.tile + 1) * p.kblocks;
+    s.kb1 = (int)((u1 < tile_end ? u1 : tile_end) - (long long)s.tile * p.kblocks);
+    s.first = owner((long long)s.tile * p.kblocks, U, G);
+    s.nseg = owner(tile_end - 1, U, G) - s.first + 1;
+    return s;
+}
+
+// Partial slot of the segment of `tile` held by CTA c: 2c if the segment is
+// the first of c's run, 2c + 1 if it is the last (a shared tile is always one
+// of the two).
+__device__ __forceinline__ int slot_of(int c, int tile, const ProjParams &p, long long U, int G)
+{
+    return 2 * c + (run_start(c, U, G) >= (long long)tile * p.kblocks ? 0 : 1);
+}
+
+__device__ __forceinline__ void set_status(int *status, int bit) { atomicOr(status, bit); }
+
+// cos and sin of pos * inv_freq: the angle in fp64, reduced by 2 pi in two
+// parts (Cody and Waite), then the fp32 functions on |r| <= pi.
+__device__ __forceinline__ void rope_cs(int pos, double inv_freq, float &c, float &s)
+{
+    const double two_pi_hi = 6.283185307179586;      // nearest double to 2 pi
+    const double two_pi_lo = 2.4492935982947064e-16;  // 2 pi - two_pi_hi
+    const double a = (double)pos * inv_freq;
+    const double n = rint(a * (1.0 / two_pi_hi));
+    double r = fma(-n, two_pi_hi, a);
+    r = fma(-n, two_pi_lo, r);
+    sincosf((float)r, &s, &c);
+}
+
+// RoPE (q and k tiles) and bf16 store of 16 accumulator columns of output
+// feature f0 + m; y holds this thread's values for batch columns
+// 16 cc .. 16 cc + 15.  All 128 epilogue threads call it together.
+__device__ __forceinline__ void finish_chunk(float (&y)[16], int cc, int m, bool rope, int half, float cs, float sn,
+                                             float *xch, __nv_bfloat16 *dst, const ProjParams &p)
+{
+    if (rope) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) xch[j * kBM + m] = y[j];
+        named_bar_sync(kEpiBar, kEpiThreads);
+        const bool low = (m & half) == 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float o = xch[j * kBM + (m ^ half)];
+            y[j] = low ? fmaf(-o, sn, y[j] * cs) : fmaf(o, sn, y[j] * cs);
+        }
+        named_bar_sync(kEpiBar, kEpiThreads);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int b = cc * kChunk + j;
+        if (b < p.B) dst[(size_t)b * p.HD + m] = __float2bfloat16_rn(y[j]);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    qkv_rope_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
+                    const ProjParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;  // 128-byte swizzled tiles need 1024-byte alignment
+    unsigned char *smem = smem_raw + (sbase - raw);
+    const uint32_t stage_bytes = kATile + (uint32_t)p.npad * kBK * 2;
+    const uint32_t off_bar = (uint32_t)p.stages * stage_bytes;
+    const uint32_t bar0 = sbase + off_bar;
+    const uint32_t acc_full = bar0 + 16u * p.stages;
+    const uint32_t acc_empty = acc_full + 8u;
+    const uint32_t drain = acc_full + 16u;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + off_bar + 8u * (2 * p.stages + 3));
+    int *flags = reinterpret_cast<int *>(tmem_slot + 1);  // [0], [1]: accumulator ready; [2]: last of a shared tile
+    float *xch = reinterpret_cast<float *>(smem + ((off_bar + 8u * (2 * p.stages + 3) + 16u + 15u) & ~15u));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, c = blockIdx.x;
+    const long long U = (long long)p.tiles * p.kblocks;
+    const long long u0 = run_start(c, U, G), u1 = run_start(c + 1, U, G);
+
+    // Nothing the previous grid in the stream may still use is read or
+    // written before it completes; then the next grid may start its CTAs.
+    pdl_wait();
+    pdl_launch_dependents();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(bar0 + 8u * s, 1);                // full[s]: one expect_tx arrival + TMA bytes
+            mbar_init(bar0 + 8u * (p.stages + s), 1);   // empty[s]: one MMA commit
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, kEpiThreads);
+        mbar_init(drain, 1);
+        fence_barrier_init();
+        prefetch_tmap(&mapW);
+        prefetch_tmap(&mapX);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    long long issued = 0;  // k-blocks whose copies warp 0 issued
+
+    if (warp == 0) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();  // W is read once per launch
+            uint32_t s = 0, ph = 0;
+            bool ok = true;
+            for (long long u = u0; u < u1 && ok;) {
+                const Seg sg = make_seg(u, u1, p, U, G);
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                    if (!wait_phase(bar0 + 8u * (p.stages + s), ph ^ 1u, p.wait_limit)) {
+                        set_status(p.status, ST_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t a = sbase + s * stage_bytes;
+                    mbar_arrive_expect_tx(bar0 + 8u * s, stage_bytes);
+                    tma_load_2d_hint(a, &mapW, kb * kBK, sg.tile * kBM, bar0 + 8u * s, pol);
+                    tma_load_2d(a + kATile, &mapX, kb * kBK, 0, bar0 + 8u * s);
+                    ++issued;
+                    if (++s == (uint32_t)p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                u += sg.kb1 - sg.kb0;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kBM, p.npad);
+            uint32_t s = 0, ph = 0, aph = 0;
+            bool ok = true;
+            for (long long u = u0; u < u1 && ok;) {
+                const Seg sg = make_seg(u, u1, p, U, G);
+                if (!wait_phase(acc_empty, aph ^ 1u, p.wait_limit)) {
+                    set_status(p.status, ST_TIMEOUT);
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                    if (!wait_phase(bar0 + 8u * s, ph, p.wait_limit)) {
+                        set_status(p.status, ST_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = sbase + s * stage_bytes;
+                    const uint64_t ad = sw128_kmajor_desc(a), bd = sw128_kmajor_desc(a + kATile);
+#pragma unroll
+                    for (int k = 0; k < kBK / kUK; ++k)
+                        umma_bf16(tmem, ad + 2u * k, bd + 2u * k, idesc, (kb > sg.kb0 || k > 0) ? 1u : 0u);
+                    umma_commit(bar0 + 8u * (p.stages + s));  // stage s free once these MMAs are done
+                    if (++s == (uint32_t)p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(acc_full);
+                aph ^= 1u;
+                u += sg.kb1 - sg.kb0;
+            }
+        }
+        __syncwarp();
+    } else {
+        const int et = threadIdx.x - 64;  // 0..127
+        const int qw = warp & 3;          // the TMEM lane quarter this warp may read
+        const int m = qw * 32 + lane;     // output feature within the tile = accumulator row
+        const uint32_t trow = tmem + ((uint32_t)(qw * 32) << 16);
+        const int half = p.D / 2;
+        const int nchunks = p.npad / kChunk;
+        uint32_t aph = 0;
+        int nseen = 0;
+        for (long long u = u0; u < u1; ++nseen) {
+            const Seg sg = make_seg(u, u1, p, U, G);
+            u += sg.kb1 - sg.kb0;
+            const int part = sg.tile * kBM / p.HD;
+            const int f0 = sg.tile * kBM - part * p.HD;
+            const bool rope = part < 2;
+            __nv_bfloat16 *dst = (part == 0 ? p.q : (part == 1 ? p.k : p.v)) + f0;
+            float cs = 1.f, sn = 0.f;
+            if (rope) rope_cs(p.pos, p.inv_freq[(m % p.D) % half], cs, sn);
+            // One thread waits for the accumulator; the others learn the
+            // outcome at the barrier, so every epilogue thread takes the same
+            // path through the named barriers below.
+            if (et == 0) flags[nseen & 1] = wait_phase(acc_full, aph, p.wait_limit) ? 1 : 0;
+            named_bar_sync(kEpiBar, kEpiThreads);
+            if (!flags[nseen & 1]) {
+                if (et == 0) set_status(p.status, ST_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            aph ^= 1u;
+            if (sg.nseg == 1) {
+                for (int cc = 0; cc < nchunks; ++cc) {
+                    float y[16];
+                    tmem_ld16(trow + (uint32_t)(cc * kChunk), y);
+                    if (cc == nchunks - 1) {
+                        tc_fence_before();
+                        mbar_arrive(acc_empty);
+                    }
+                    finish_chunk(y, cc, m, rope, half, cs, sn, xch, dst, p);
+                }
+            } else {
+                float *mine = p.part + (size_t)slot_of(c, sg.tile, p, U, G) * p.npad * kBM;
+                for (int cc = 0; cc < nchunks; ++cc) {
+                    float y[16];
+                    tmem_ld16(trow + (uint32_t)(cc * kChunk), y);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) __stcg(mine + (size_t)(cc * kChunk + j) * kBM + m, y[j]);
+                }
+                tc_fence_before();
+                mbar_arrive(acc_empty);
+                __threadfence();
+                named_bar_sync(kEpiBar, kEpiThreads);
+                if (et == 0) flags[2] = atomicAdd(p.counters + sg.tile, 1) == sg.nseg - 1 ? 1 : 0;
+                named_bar_sync(kEpiBar, kEpiThreads);
+                if (flags[2]) {
+                    // Last of the tile's CTAs: sum the partials in segment order.
+                    __threadfence();
+                    for (int cc = 0; cc < nchunks; ++cc) {
+                        float y[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) y[j] = 0.f;
+                        for (int jj = 0; jj < sg.nseg; ++jj) {
+                            const float *src =
+                                p.part + (size_t)slot_of(sg.first + jj, sg.tile, p, U, G) * p.npad * kBM;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) y[j] += __ldcg(src + (size_t)(cc * kChunk + j) * kBM + m);
+                        }
+                        finish_chunk(y, cc, m, rope, half, cs, sn, xch, dst, p);
+                    }
+                    if (et == 0) atomicExch(p.counters + sg.tile, 0);
+                }
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+        // Every copy issued has landed before the CTA's shared memory goes.
+        for (int s = 0; s < p.stages && s < issued; ++s) {
+            const long long armed = (issued - 1 - s) / p.stages + 1;
+            drain_phase(bar0 + 8u * s, (uint32_t)((armed - 1) & 1));
+        }
+    }
+    if (warp == 1 && lane == 0) {
+        // Every MMA issued has completed before the tensor memory is freed.
+        umma_commit(drain);
+        drain_phase(drain, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+    }
+}
+
+}  // namespace dsa_proj_k
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+using dsa_detail::cuda_fail;
+using dsa_detail::dev_alloc;
+using dsa_detail::fail;
+
+namespace {
+
+constexpr uint32_t kProjMagic = 0x44535051u;  // "DSPQ"
+constexpr size_t kSmemLimit = 227 * 1024;     // dynamic shared memory per CTA on sm_103
+constexpr int kMaxStages = 8;
+
+// Shared-memory bytes of the kernel's layout (see qkv_rope_kernel) for
+// `stages` stages of `stage_bytes`, plus 1024 bytes of alignment slack.
+size_t proj_smem(int stages, size_t stage_bytes)
+{
+    const size_t off_bar = (size_t)stages * stage_bytes;
+    const size_t off_xch = (off_bar + 8 * (2 * (size_t)stages + 3) + 16 + 15) & ~(size_t)15;
+    return 1024 + off_xch + sizeof(float) * dsa_proj_k::kChunk * dsa_proj_k::kBM;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void **)&encode, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess) encode = nullptr;
+    }
+    return encode;
+}
+
+// Row-major bf16 matrix [rows, cols] seen by TMA in boxes of 64 columns x
+// box_rows rows with 128-byte swizzling (the operand layout of the MMA
+// descriptors).  Rows past the end read as zero.
+int encode_operand(CUtensorMap *map, const void *base, int rows, int cols, int box_rows, bool stream_once)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+    if (!encode) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)dsa_proj_k::kBK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        stream_once ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return DSA_OK;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+struct dsa_proj_ctx {
+    uint32_t magic;
+    int B, H, D, hidden, HD, npad, tiles, kblocks, grid, stages, tmem_cols;
+    size_t smem;
+    float *part;
+    int *counters;
+    int *status;
+    __nv_bfloat16 *staging;  // [3][B * HD]: q, k, v of dsa_decode_step_fused
+    uint32_t wait_limit;
+    double inv_freq[64];
+};
+
+namespace {
+
+bool valid(const dsa_proj_ctx *p) { return p != nullptr && p->magic == kProjMagic; }
+
+void free_proj(dsa_proj_ctx *p)
+{
+    if (!p) return;
+    cudaFree(p->part);
+    cudaFree(p->counters);
+    cudaFree(p->status);
+    cudaFree(p->staging);
+    p->magic = 0;
+    delete p;
+}
+
+}  // namespace
+
+namespace dsa_detail {
+
+int proj_shape(const dsa_proj_ctx *p, int *batch, int *heads, int *head_dim)
+{
+    if (!valid(p)) return fail(DSA_ERR_STATE, "invalid projection context");
+    *batch = p->B;
+    *heads = p->H;
+    *head_dim = p->D;
+    return DSA_OK;
+}
+
+void proj_staging(const dsa_proj_ctx *p, void **q, void **k, void **v)
+{
+    const size_t n = (size_t)p->B * p->HD;
+    *q = p->staging;
+    *k = p->staging + n;
+    *v = p->staging + 2 * n;
+}
+
+int proj_launch(dsa_proj_ctx *pr, const void *x, const void *W, int pos, void *q, void *k, void *v, cudaStream_t st)
+{
+    if (!valid(pr)) return fail(DSA_ERR_STATE, "invalid projection context");
+    if (!x || !W || !q || !k || !v) return fail(DSA_ERR_ARG, "x, W, q, k and v must be non-NULL");
+    if (!aligned16(x) || !aligned16(W) || !aligned16(q) || !aligned16(k) || !aligned16(v))
+        return fail(DSA_ERR_ARG, "x, W, q, k and v must be 16-byte aligned");
+    if (pos < 0) return fail(DSA_ERR_ARG, "pos must be >= 0 (got %d)", pos);
+    CUtensorMap mapW, mapX;
+    int rc = encode_operand(&mapW, W, 3 * pr->HD, pr->hidden, dsa_proj_k::kBM, true);
+    if (rc == DSA_OK) rc = encode_operand(&mapX, x, pr->B, pr->hidden, pr->npad, false);
+    if (rc != DSA_OK) return rc;
+
+    dsa_proj_k::ProjParams p;
+    p.q = static_cast<__nv_bfloat16 *>(q);
+    p.k = static_cast<__nv_bfloat16 *>(k);
+    p.v = static_cast<__nv_bfloat16 *>(v);
+    p.part = pr->part;
+    p.counters = pr->counters;
+    p.status = pr->status;
+    p.B = pr->B;
+    p.npad = pr->npad;
+    p.HD = pr->HD;
+    p.D = pr->D;
+    p.tiles = pr->tiles;
+    p.kblocks = pr->kblocks;
+    p.stages = pr->stages;
+    p.tmem_cols = pr->tmem_cols;
+    p.pos = pos;
+    p.wait_limit = pr->wait_limit;
+    std::memcpy(p.inv_freq, pr->inv_freq, sizeof p.inv_freq);
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pr->grid);
+    cfg.blockDim = dim3(dsa_proj_k::kThreads);
+    cfg.dynamicSmemBytes = pr->smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, dsa_proj_k::qkv_rope_kernel, mapW, mapX, p);
+    if (e != cudaSuccess) return cuda_fail(e, "projection launch");
+    return DSA_OK;
+}
+
+}  // namespace dsa_detail
+
+extern "C" {
+
+int dsa_proj_create(int batch, int heads, int head_dim, int hidden, dsa_proj *out)
+{
+    if (!out) return fail(DSA_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    if (batch < 1 || batch > dsa_proj_k::kMaxBatch)
+        return fail(DSA_ERR_ARG, "batch must be in [1, %d] (got %d)", dsa_proj_k::kMaxBatch, batch);
+    if (heads < 1) return fail(DSA_ERR_ARG, "heads must be >= 1 (got %d)", heads);
+    if (head_dim != 64 && head_dim != 128) return fail(DSA_ERR_ARG, "head_dim must be 64 or 128 (got %d)", head_dim);
+    if ((long long)heads * head_dim % dsa_proj_k::kBM != 0)
+        return fail(DSA_ERR_ARG, "heads * head_dim must be a multiple of 128 (got %d x %d)", heads, head_dim);
+    if ((long long)3 * heads * head_dim > INT_MAX / 2) return fail(DSA_ERR_ARG, "heads * head_dim too large");
+    if (hidden < dsa_proj_k::kBK || hidden % dsa_proj_k::kBK != 0)
+        return fail(DSA_ERR_ARG, "hidden must be a positive multiple of 64 (got %d)", hidden);
+
+    dsa_proj_ctx *p = new (std::nothrow) dsa_proj_ctx();
+    if (!p) return fail(DSA_ERR_OOM, "host allocation failed");
+    p->magic = kProjMagic;
+    p->B = batch;
+    p->H = heads;
+    p->D = head_dim;
+    p->hidden = hidden;
+    p->HD = heads * head_dim;
+    p->npad = (batch + 15) / 16 * 16;
+    p->tiles = 3 * p->HD / dsa_proj_k::kBM;
+    p->kblocks = hidden / dsa_proj_k::kBK;
+    p->tmem_cols = p->npad <= 32 ? 32 : (p->npad <= 64 ? 64 : (p->npad <= 128 ? 128 : 256));
+    p->wait_limit = 0xffffffffu;
+    for (int j = 0; j < head_dim / 2; ++j) p->inv_freq[j] = std::pow(10000.0, -2.0 * j / head_dim);
+
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+        free_proj(p);
+        return cuda_fail(e, "device query");
+    }
+    const size_t stage_bytes = (size_t)dsa_proj_k::kATile + (size_t)p->npad * dsa_proj_k::kBK * 2;
+    p->stages = kMaxStages;
+    while (p->stages > 2 && proj_smem(p->stages, stage_bytes) > kSmemLimit) --p->stages;
+    p->smem = proj_smem(p->stages, stage_bytes);
+    const long long units = (long long)p->tiles * p->kblocks;
+    p->grid = (int)(units < sms ? units : sms);
+    e = cudaFuncSetAttribute(dsa_proj_k::qkv_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem);
+    if (e != cudaSuccess) {
+        free_proj(p);
+        return cuda_fail(e, "projection kernel attribute (is this an sm_103 device?)");
+    }
+
+    const size_t n = (size_t)batch * p->HD;
+    int rc = dev_alloc((void **)&p->part, sizeof(float) * 2 * (size_t)p->grid * p->npad * dsa_proj_k::kBM,
+                       "projection partials");
+    if (rc == DSA_OK) rc = dev_alloc((void **)&p->counters, sizeof(int) * (size_t)p->tiles, "projection counters");
+    if (rc == DSA_OK) rc = dev_alloc((void **)&p->status, 16, "projection status");
+    if (rc == DSA_OK) rc = dev_alloc((void **)&p->staging, sizeof(__nv_bfloat16) * 3 * n, "q, k, v staging");
+    if (rc != DSA_OK) {
+        free_proj(p);  // keeps the allocation's error message
+        return rc;
+    }
+    if ((e = cudaMemset(p->counters, 0, sizeof(int) * (size_t)p->tiles)) != cudaSuccess ||
+        (e = cudaMemset(p->status, 0, 16)) != cudaSuccess) {
+        free_proj(p);
+        return cuda_fail(e, "cudaMemset");
+    }
+    *out = p;
+    return DSA_OK;
+}
+
+int dsa_proj_destroy(dsa_proj p)
+{
+    if (!p) return DSA_OK;
+    if (!valid(p)) return fail(DSA_ERR_STATE, "invalid projection context");
+    cudaDeviceSynchronize();
+    free_proj(p);
+    return DSA_OK;
+}
+
+int dsa_qkv_rope(dsa_proj p, const void *x, const void *W, int pos, void *q, void *k, void *v, void *stream)
+{
+    return dsa_detail::proj_launch(p, x, W, pos, q, k, v, (cudaStream_t)stream);
+}
+
+int dsa_proj_sync_status(dsa_proj p, void *stream)
+{
+    if (!valid(p)) return fail(DSA_ERR_STATE, "invalid projection context");
+    cudaStream_t st = (cudaStream_t)stream;
+    int word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, p->status, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "status copy");
+    if (word == 0) return DSA_OK;
+    // A launch that gave up may leave counters of shared tiles part-way.
+    if ((e = cudaMemsetAsync(p->counters, 0, sizeof(int) * (size_t)p->tiles, st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(p->status, 0, 16, st)) != cudaSuccess || (e = cudaStreamSynchronize(st)) != cudaSuccess)
+        return cuda_fail(e, "status reset");
+    return fail(DSA_ERR_TIMEOUT, "a bounded wait in the projection kernel gave up");
+}
+
+int dsa_proj_set_wait_limit(dsa_proj p, uint32_t limit)
+{
+    if (!valid(p)) return fail(DSA_ERR_STATE, "invalid projection context");
+    p->wait_limit = limit;
+    return DSA_OK;
+}
+
+}  // extern "C"

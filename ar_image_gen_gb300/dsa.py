@@ -45,7 +45,9 @@ EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa
            "dsa_get_skip_mask", "dsa_get_last_selection", "dsa_sync_status", "dsa_last_error",
            "dsa_state_bytes", "dsa_plan_step", "dsa_set_kv_scales", "dsa_set_splits", "dsa_set_pipeline",
            "dsa_set_wait_limit", "dsa_debug_copy_state",
-           "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc", "dsa_diag_trace"]
+           "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc", "dsa_diag_trace",
+           "dsa_proj_create", "dsa_proj_destroy", "dsa_qkv_rope", "dsa_decode_step_fused", "dsa_proj_sync_status",
+           "dsa_proj_set_wait_limit"]
 
 
 class dsa_step_plan(ctypes.Structure):
@@ -78,6 +80,12 @@ _L.dsa_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
 _L.dsa_debug_fail_alloc_after.argtypes = [_I]
 _L.dsa_decode_step_noalloc.argtypes = [_I] * 8 + [_P] * 9
 _L.dsa_diag_trace.argtypes = [_I] * 5 + [_P] * 3 + [_I] + [_P] * 6
+_L.dsa_proj_create.argtypes = [_I] * 4 + [ctypes.POINTER(_P)]
+_L.dsa_proj_destroy.argtypes = [_P]
+_L.dsa_qkv_rope.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P]
+_L.dsa_decode_step_fused.argtypes = [_P] * 6
+_L.dsa_proj_sync_status.argtypes = [_P, _P]
+_L.dsa_proj_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
 
 
 class DSAError(RuntimeError):
@@ -236,7 +244,63 @@ def diag_trace(Q, Kp, Kd, dists, step_mass=None, stream=None):
     return mass, vert, diag
 
 
-# ---- convenience wrapper ---------------------------------------------------
+def dsa_proj_create(batch, heads, head_dim, hidden):
+    p = _P()
+    return _L.dsa_proj_create(batch, heads, head_dim, hidden, ctypes.byref(p)), p
+
+
+def dsa_proj_destroy(p) -> int:
+    return _L.dsa_proj_destroy(p)
+
+
+def dsa_qkv_rope(p, x, W, pos, q, k, v, stream=None) -> int:
+    return _L.dsa_qkv_rope(p, _ptr(x), _ptr(W), pos, _ptr(q), _ptr(k), _ptr(v), _stream(stream))
+
+
+def dsa_decode_step_fused(h, p, x, W, out, stream=None) -> int:
+    return _L.dsa_decode_step_fused(h, p, _ptr(x), _ptr(W), _ptr(out), _stream(stream))
+
+
+def dsa_proj_sync_status(p, stream=None) -> int:
+    return _L.dsa_proj_sync_status(p, _stream(stream))
+
+
+def dsa_proj_set_wait_limit(p, limit) -> int:
+    return _L.dsa_proj_set_wait_limit(p, limit)
+
+
+# ---- convenience wrappers --------------------------------------------------
+
+class Proj:
+    """A QKV projection context (include/dsa_proj.h): `batch` tokens, `heads`
+    heads of `head_dim`, `hidden` input features."""
+
+    def __init__(self, batch, heads, head_dim, hidden):
+        code, p = dsa_proj_create(batch, heads, head_dim, hidden)
+        _check(code, "dsa_proj_create")
+        self.p = p
+        self.batch, self.heads, self.head_dim, self.hidden = batch, heads, head_dim, hidden
+
+    def close(self):
+        if getattr(self, "p", None):
+            dsa_proj_destroy(self.p)
+            self.p = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def qkv_rope(self, x, W, pos, q, k, v, stream=None):
+        _check(dsa_qkv_rope(self.p, x, W, pos, q, k, v, stream), "dsa_qkv_rope")
+
+    def sync_status(self, stream=None) -> int:
+        return dsa_proj_sync_status(self.p, stream)
+
+    def set_wait_limit(self, limit: int):
+        _check(dsa_proj_set_wait_limit(self.p, limit), "dsa_proj_set_wait_limit")
+
 
 class DSA:
     """One handle: `heads` streams of one layer stepping together."""
@@ -265,6 +329,10 @@ class DSA:
 
     def decode_step(self, q, k_new, v_new, out, stream=None):
         _check(dsa_decode_step(self.h, q, k_new, v_new, out, stream), "dsa_decode_step")
+
+    def decode_step_fused(self, proj: "Proj", x, W, out, stream=None):
+        """Projection of x by W (position L_p + t) and the decode step on it."""
+        _check(dsa_decode_step_fused(self.h, proj.p, x, W, out, stream), "dsa_decode_step_fused")
 
     @property
     def t(self) -> int:

@@ -189,3 +189,35 @@ class TraceGen:
         v = base_v + 0.5 * nv
         cast = lambda x: x.reshape(self.S, wl.head_dim).to(self.out_dtype).contiguous()
         return cast(q), cast(k), cast(v)
+
+
+class ProjGen:
+    """Seeded inputs of the QKV projection that feeds a decode step: the
+    newest token's hidden state x [batch, hidden] ~ N(0, 1) per step, and one
+    weight W [3 * heads * head_dim, hidden] ~ N(0, 1 / hidden) per layer (the
+    q rows of all heads, then k, then v), both bf16, so that q, k and v come
+    out with unit variance.  hidden defaults to heads * head_dim (4096 for
+    the 7B models the workloads stand in for)."""
+
+    def __init__(self, wl: Workload, layer: int = 0, device: str | torch.device = "cpu", batch: int | None = None,
+                 hidden: int | None = None, seed: int | None = None):
+        self.wl = wl
+        self.layer = layer
+        self.device = torch.device(device)
+        self.batch = wl.batch if batch is None else batch
+        self.hidden = wl.heads * wl.head_dim if hidden is None else hidden
+        self.seed = wl.seed if seed is None else seed
+
+    def _gen(self, kind: int, step: int) -> torch.Generator:
+        g = torch.Generator(device=self.device)
+        g.manual_seed(((self.seed * 1009 + self.layer) * 7 + kind) * 1_000_003 + step + 500_000)
+        return g
+
+    def weight(self) -> torch.Tensor:
+        rows = 3 * self.wl.heads * self.wl.head_dim
+        W = torch.randn((rows, self.hidden), generator=self._gen(5, 0), device=self.device, dtype=torch.float32)
+        return (W * self.hidden ** -0.5).to(torch.bfloat16).contiguous()
+
+    def x(self, t: int) -> torch.Tensor:
+        x = torch.randn((self.batch, self.hidden), generator=self._gen(6, t), device=self.device, dtype=torch.float32)
+        return x.to(torch.bfloat16).contiguous()

@@ -98,3 +98,27 @@ def test_diag_rejects_bad_arguments(dsa, kw):
     rc = dsa.dsa_diag_trace(a["heads"], a["head_dim"], a["L_p"], a["L_dec"], a["dtype"], fake, fake, fake, dist, None,
                             z, z, z)
     assert rc == dsa.DSA_ERR_ARG and "dsa_diag_trace" in dsa.dsa_last_error()
+
+
+@pytest.mark.parametrize("args", [
+    (0, 32, 128, 4096),      # no tokens
+    (257, 32, 128, 4096),    # batch beyond one tensor-core tile's N
+    (8, 32, 96, 4096),       # unsupported head_dim
+    (8, 3, 64, 4096),        # heads * head_dim not a multiple of 128
+    (8, 32, 128, 4000),      # hidden not a multiple of 64
+    (8, 0, 128, 4096),       # no heads
+])
+def test_proj_create_rejects_bad_arguments(dsa, args):
+    code, p = dsa.dsa_proj_create(*args)
+    assert code == dsa.DSA_ERR_ARG
+    assert not p.value
+    assert dsa.dsa_last_error()
+
+
+def test_proj_calls_on_a_null_context_fail_cleanly(dsa):
+    null = ctypes.c_void_p()
+    assert dsa.dsa_proj_destroy(null) == dsa.DSA_OK
+    assert dsa.dsa_qkv_rope(null, 16, 16, 0, 16, 16, 16) == dsa.DSA_ERR_STATE
+    assert dsa.dsa_proj_sync_status(null) == dsa.DSA_ERR_STATE
+    assert dsa.dsa_proj_set_wait_limit(null, 0) == dsa.DSA_ERR_STATE
+    assert dsa.dsa_decode_step_fused(null, null, 16, 16, 16) == dsa.DSA_ERR_STATE
