@@ -54,13 +54,15 @@ constexpr int kUK = 16;        // K of one tcgen05.mma kind::f16
 constexpr int kATile = kBM * kBK * 2;
 constexpr int kMaxBatch = 256;
 constexpr int kEpiThreads = 128;
-constexpr int kChunk = 16;     // accumulator columns per tcgen05.ld
+constexpr int kXchFloats = 32 * kBM;  // epilogue exchange buffer: 32 columns x 128 features
 constexpr uint32_t kEpiBar = 1;
+constexpr int kExtraBars = 4;            // acc_full, acc_empty, drain, red_full
+constexpr uint32_t kBulkPiece = 32768;  // bytes per bulk copy of a partial
 
 struct ProjParams {
     __nv_bfloat16 *q, *k, *v;  // [B, HD] each
-    float *part;               // [2 * grid][npad][128] partials of split tiles
-    int *counters;             // [tiles] finished segments per split tile
+    float *part;               // [grid][npad / 16][4][128] float4 partials of shared tiles
+    int *counters;             // [tiles] published pieces per shared tile
     int *status;
     int B, npad, HD, D, tiles, kblocks, stages, tmem_cols;
     int pos;
@@ -68,40 +70,96 @@ struct ProjParams {
     double inv_freq[64];       // 10000^(-2j/D), j < D/2
 };
 
-// The CTA whose k-block run [start(c), start(c + 1)) holds work unit u,
-// with start(c) = c U / G.
-__device__ __forceinline__ int owner(long long u, long long U, int G)
-{
-    return (int)(((u + 1) * G + U - 1) / U) - 1;
-}
-__device__ __forceinline__ long long run_start(int c, long long U, int G) { return (long long)c * U / G; }
+// Work units (tile, k-block) are numbered u = tile * kblocks + kb.  CTA c of
+// the G in the grid takes the run of units [start(c), start(c + 1)) with
+// start(c) = c U / G (the host keeps U * G below 2^31).
+__device__ __forceinline__ int run_start(int c, int U, int G) { return (int)((unsigned)c * (unsigned)U / (unsigned)G); }
 
+// The CTA whose run holds unit u: the largest c with start(c) <= u.
+__device__ __forceinline__ int owner(int u, int U, int G) { return (int)(((unsigned)(u + 1) * G + U - 1) / U) - 1; }
+
+// One piece of a CTA's run: k-blocks [kb0, kb1) of `tile`, and the CTAs
+// whose runs share the tile (first, count).  A run's pieces after its first
+// start at a tile boundary, so a tile shared by several CTAs is split into
+// a head (k-block 0, always the LAST piece of its CTA's run) and pieces that
+// are each the FIRST piece of a later CTA's run.  Each CTA therefore writes
+// at most one partial (slot c), and the head's CTA, which finishes the tile
+// last in time, sums them.
 struct Seg {
-    int tile, kb0, kb1;  // k-blocks [kb0, kb1) of `tile`
-    int first, nseg;     // CTAs sharing the tile: first, count
+    int tile, kb0, kb1;
+    int first, nseg;
 };
 
-__device__ __forceinline__ Seg make_seg(long long u, long long u1, const ProjParams &p, long long U, int G)
+__device__ __forceinline__ Seg make_seg(int u, int u1, int kblocks, int U, int G)
 {
     Seg s;
-    s.tile = (int)(u / p.kblocks);
-    s.kb0 = (int)(u - (long long)s.tile * p.kblocks);
-    const long long tile_end = (long long)(s.tile + 1) * p.kblocks;
-    s.kb1 = (int)((u1 < tile_end ? u1 : tile_end) - (long long)s.tile * p.kblocks);
-    s.first = owner((long long)s.tile * p.kblocks, U, G);
+    s.tile = u / kblocks;
+    s.kb0 = u - s.tile * kblocks;
+    const int tile_end = (s.tile + 1) * kblocks;
+    s.kb1 = (u1 < tile_end ? u1 : tile_end) - s.tile * kblocks;
+    s.first = owner(s.tile * kblocks, U, G);
     s.nseg = owner(tile_end - 1, U, G) - s.first + 1;
     return s;
 }
 
-// Partial slot of the segment of `tile` held by CTA c: 2c if the segment is
-// the first of c's run, 2c + 1 if it is the last (a shared tile is always one
-// of the two).
-__device__ __forceinline__ int slot_of(int c, int tile, const ProjParams &p, long long U, int G)
+__device__ __forceinline__ void set_status(int *status, int bit) { atomicOr(status, bit); }
+
+__device__ __forceinline__ int ld_acquire(const int *p)
 {
-    return 2 * c + (run_start(c, U, G) >= (long long)tile * p.kblocks ? 0 : 1);
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
-__device__ __forceinline__ void set_status(int *status, int bit) { atomicOr(status, bit); }
+// Orders this thread's earlier generic-proxy view of global memory (the
+// acquire above) before its later bulk copies read global memory.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+// Two floats rounded to bf16 (nearest even), low half first.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// y[4i .. 4i + 3] += v
+__device__ __forceinline__ void add4(float (&y)[32], int i, const float4 &v)
+{
+    y[4 * i] += v.x;
+    y[4 * i + 1] += v.y;
+    y[4 * i + 2] += v.z;
+    y[4 * i + 3] += v.w;
+}
+
+// Bounded wait for a barrier phase by polling (no suspend hint): the
+// producer and MMA threads are alone on their warps and each hand-off sits
+// on the launch's critical path.  Gives up after `limit` polls or about one
+// second (limit 0: at once).
+__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, uint32_t limit)
+{
+    if (limit == 0) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; i < limit; ++i) {
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitNs) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+    }
+    return false;
+}
+
+// Bounded wait until the counter reaches `want` (the other pieces of a
+// shared tile have published their partials).
+__device__ __forceinline__ bool wait_count(const int *ctr, int want, uint32_t limit)
+{
+    if (limit == 0) return false;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (ld_acquire(ctr) >= want) return true;
+        if ((i & 63u) == 63u && globaltimer_ns() - t0 > kWaitNs) return false;
+        __nanosleep(64);
+    }
+    return false;
+}
 
 // cos and sin of pos * inv_freq: the angle in fp64, reduced by 2 pi in two
 // parts (Cody and Waite), then the fp32 functions on |r| <= pi.
@@ -116,29 +174,185 @@ __device__ __forceinline__ void rope_cs(int pos, double inv_freq, float &c, floa
     sincosf((float)r, &s, &c);
 }
 
-// RoPE (q and k tiles) and bf16 store of 16 accumulator columns of output
-// feature f0 + m; y holds this thread's values for batch columns
-// 16 cc .. 16 cc + 15.  All 128 epilogue threads call it together.
-__device__ __forceinline__ void finish_chunk(float (&y)[16], int cc, int m, bool rope, int half, float cs, float sn,
-                                             float *xch, __nv_bfloat16 *dst, const ProjParams &p)
+// RoPE (q and k tiles) and bf16 store of `ncol` (16 or 32) accumulator
+// columns c0 .. c0 + ncol - 1 (batch rows) of the tile; y[j] is this thread's
+// value for feature m and column c0 + j.  Through `xch` ([32][128] floats) a
+// head's halves meet (feature m pairs with m ^ half) and the tile is turned
+// so that each thread stores 8 consecutive features of one row as one
+// 16-byte vector.  All 128 epilogue threads call it together.
+__device__ __forceinline__ void finish_cols(float (&y)[32], int ncol, int c0, int m, int et, bool rope, int half,
+                                            float cs, float sn, float *xch, __nv_bfloat16 *dst, const ProjParams &p)
 {
-    if (rope) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) xch[j * kBM + m] = y[j];
-        named_bar_sync(kEpiBar, kEpiThreads);
+    for (int j = 0; j < 32; ++j)
+        if (j < ncol) xch[j * kBM + m] = y[j];
+    named_bar_sync(kEpiBar, kEpiThreads);
+    if (rope) {
         const bool low = (m & half) == 0;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float o = xch[j * kBM + (m ^ half)];
-            y[j] = low ? fmaf(-o, sn, y[j] * cs) : fmaf(o, sn, y[j] * cs);
+        for (int j = 0; j < 32; ++j) {
+            if (j < ncol) {
+                const float o = xch[j * kBM + (m ^ half)];
+                y[j] = low ? fmaf(-o, sn, y[j] * cs) : fmaf(o, sn, y[j] * cs);
+            }
         }
         named_bar_sync(kEpiBar, kEpiThreads);
-    }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const int b = cc * kChunk + j;
-        if (b < p.B) dst[(size_t)b * p.HD + m] = __float2bfloat16_rn(y[j]);
+        for (int j = 0; j < 32; ++j)
+            if (j < ncol) xch[j * kBM + m] = y[j];
+        named_bar_sync(kEpiBar, kEpiThreads);
     }
+    const int g = et & 15, r = et >> 4;  // 8 features [8 g, 8 g + 8) of row r of each group of 8 rows
+    for (int j = r; j < ncol; j += 8) {
+        const int b = c0 + j;
+        if (b < p.B) {
+            const float4 lo = *reinterpret_cast<const float4 *>(xch + j * kBM + 8 * g);
+            const float4 hi = *reinterpret_cast<const float4 *>(xch + j * kBM + 8 * g + 4);
+            uint4 v;
+            v.x = pack_bf16x2(lo.x, lo.y);
+            v.y = pack_bf16x2(lo.z, lo.w);
+            v.z = pack_bf16x2(hi.x, hi.y);
+            v.w = pack_bf16x2(hi.z, hi.w);
+            *reinterpret_cast<uint4 *>(dst + (size_t)b * p.HD + 8 * g) = v;
+        }
+    }
+    named_bar_sync(kEpiBar, kEpiThreads);  // xch is rewritten by the next call
+}
+
+// ncol (16 or 32) accumulator columns of this thread's TMEM lane into y.
+__device__ __forceinline__ void load_cols(uint32_t taddr, int ncol, float (&y)[32])
+{
+    if (ncol == 32) {
+        tmem_ld32(taddr, y);
+    } else {
+        tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(&y[0]));
+    }
+}
+
+// The four epilogue warps (threads 64..191): per piece of the CTA's run,
+// drain the accumulator from tensor memory and either write the output
+// (an unshared tile), publish an fp32 partial (a non-head piece of a shared
+// tile), or, for the head of a shared tile, wait until the other pieces are
+// published, fetch them into the now idle stage memory with bulk copies and
+// add them to the head's accumulator in k order (deterministic), then write
+// the output.  Every branch below is uniform over the 128 threads.
+__device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int G, int u0, int u1, uint32_t tmem,
+                                         uint32_t acc_full, uint32_t acc_empty, uint32_t red_full,
+                                         const unsigned char *smem, uint32_t sbase, uint32_t stage_bytes, int *flags,
+                                         float *xch)
+{
+    const int et = threadIdx.x - 64;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qw = warp & 3;       // the TMEM lane quarter this warp may read
+    const int m = qw * 32 + lane;  // output feature within the tile = accumulator row
+    const uint32_t trow = tmem + ((uint32_t)(qw * 32) << 16);
+    const int half = p.D / 2;
+    const int nchunks = p.npad / 16;
+    const uint32_t pbytes = (uint32_t)p.npad * kBM * 4;  // one partial
+    const size_t pslot = (size_t)nchunks * 4 * kBM;      // float4s per partial slot
+    float4 *const part4 = reinterpret_cast<float4 *>(p.part);
+    uint32_t aph = 0;
+    bool red_armed = false;
+    int nseen = 0;
+    for (int u = u0; u < u1; ++nseen) {
+        const Seg sg = make_seg(u, u1, p.kblocks, U, G);
+        u += sg.kb1 - sg.kb0;
+        const int part = sg.tile * kBM / p.HD;
+        const int f0 = sg.tile * kBM - part * p.HD;
+        const bool rope = part < 2;
+        __nv_bfloat16 *dst = (part == 0 ? p.q : (part == 1 ? p.k : p.v)) + f0;
+        float cs = 1.f, sn = 0.f;
+        if (rope) rope_cs(p.pos, p.inv_freq[m % half], cs, sn);  // tiles start at head boundaries
+        // One thread waits; the others learn the outcome at the barrier.
+        if (et == 0) flags[nseen & 1] = wait_spin(acc_full, aph, p.wait_limit) ? 1 : 0;
+        named_bar_sync(kEpiBar, kEpiThreads);
+        if (!flags[nseen & 1]) {
+            if (et == 0) set_status(p.status, ST_TIMEOUT);
+            break;
+        }
+        tc_fence_after();
+        aph ^= 1u;
+        if (sg.nseg > 1 && sg.kb0 > 0) {
+            // A non-head piece (the first of this CTA's run): publish its
+            // partial in slot c, laid out [chunk][4][128 features] of float4
+            // so that stores and the head's reads are contiguous per warp.
+            float4 *mine = part4 + (size_t)c * pslot + m;
+            for (int c0 = 0; c0 < p.npad; c0 += 32) {
+                const int ncol = p.npad - c0 >= 32 ? 32 : 16;
+                float y[32];
+                load_cols(trow + (uint32_t)c0, ncol, y);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (4 * i < ncol)
+                        __stcg(mine + (size_t)(c0 / 4 + i) * kBM,
+                               make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]));
+            }
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+            __threadfence();
+            named_bar_sync(kEpiBar, kEpiThreads);
+            if (et == 0) atomicAdd(p.counters + sg.tile, 1);
+            continue;
+        }
+        const int nother = sg.nseg - 1;  // published pieces to add (0: unshared tile)
+        const bool bulk = nother > 0 && (uint64_t)nother * pbytes <= (uint64_t)p.stages * stage_bytes;
+        if (nother > 0) {
+            if (et == 0) {
+                int ok = wait_count(p.counters + sg.tile, nother, p.wait_limit) ? 1 : 0;
+                if (ok && bulk) {
+                    // All MMAs of this run are done (the head is its last
+                    // piece), so the stage memory is free for the partials.
+                    fence_proxy_async_all();
+                    mbar_arrive_expect_tx(red_full, (uint32_t)nother * pbytes);
+                    for (int jj = 0; jj < nother; ++jj) {
+                        const unsigned char *src = reinterpret_cast<const unsigned char *>(part4 + (size_t)(sg.first + 1 + jj) * pslot);
+                        for (uint32_t off = 0; off < pbytes; off += kBulkPiece) {
+                            const uint32_t n = pbytes - off < kBulkPiece ? pbytes - off : kBulkPiece;
+                            bulk_g2s(sbase + (uint32_t)jj * pbytes + off, src + off, n, red_full);
+                        }
+                    }
+                    red_armed = true;
+                    ok = wait_spin(red_full, 0, p.wait_limit) ? 1 : 0;
+                }
+                flags[2] = ok;
+            }
+            named_bar_sync(kEpiBar, kEpiThreads);
+            if (!flags[2]) {
+                if (et == 0) set_status(p.status, ST_TIMEOUT);
+                break;
+            }
+            if (bulk) (void)mbar_try_wait(red_full, 0);  // completed: makes the copied bytes visible here too
+        }
+        for (int c0 = 0; c0 < p.npad; c0 += 32) {
+            const int ncol = p.npad - c0 >= 32 ? 32 : 16;
+            float y[32];
+            load_cols(trow + (uint32_t)c0, ncol, y);
+            if (c0 + ncol >= p.npad) {
+                tc_fence_before();
+                mbar_arrive(acc_empty);
+            }
+            for (int jj = 0; jj < nother; ++jj) {  // the other pieces, in k order
+                float4 v[8];
+                if (bulk) {
+                    const float4 *src = reinterpret_cast<const float4 *>(smem + (size_t)jj * pbytes) + (size_t)(c0 / 4) * kBM + m;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (4 * i < ncol) v[i] = src[i * kBM];
+                } else {
+                    const float4 *src = part4 + (size_t)(sg.first + 1 + jj) * pslot + (size_t)(c0 / 4) * kBM + m;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (4 * i < ncol) v[i] = __ldcg(src + i * kBM);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (4 * i < ncol) add4(y, i, v[i]);
+            }
+            finish_cols(y, ncol, c0, m, et, rope, half, cs, sn, xch, dst, p);
+        }
+        if (nother > 0 && et == 0) atomicExch(p.counters + sg.tile, 0);
+    }
+    if (red_armed) drain_phase(red_full, 0);  // (et == 0 only) copies in flight land before exit
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -151,32 +365,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char *smem = smem_raw + (sbase - raw);
     const uint32_t stage_bytes = kATile + (uint32_t)p.npad * kBK * 2;
     const uint32_t off_bar = (uint32_t)p.stages * stage_bytes;
-    const uint32_t bar0 = sbase + off_bar;
+    const uint32_t bar0 = sbase + off_bar;           // full[s] at bar0 + 8 s, empty[s] at bar0 + 8 (stages + s)
     const uint32_t acc_full = bar0 + 16u * p.stages;
     const uint32_t acc_empty = acc_full + 8u;
     const uint32_t drain = acc_full + 16u;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + off_bar + 8u * (2 * p.stages + 3));
-    int *flags = reinterpret_cast<int *>(tmem_slot + 1);  // [0], [1]: accumulator ready; [2]: last of a shared tile
-    float *xch = reinterpret_cast<float *>(smem + ((off_bar + 8u * (2 * p.stages + 3) + 16u + 15u) & ~15u));
+    const uint32_t red_full = acc_full + 24u;       // partials of a shared tile landed in the stage memory
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + off_bar + 8u * (2 * p.stages + kExtraBars));
+    // flags[0], [1]: accumulator ready (alternating); [2]: partials published; [3]: partials landed
+    int *flags = reinterpret_cast<int *>(tmem_slot + 1);
+    float *xch = reinterpret_cast<float *>(smem + ((off_bar + 8u * (2 * p.stages + kExtraBars) + 32u + 15u) & ~15u));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
-    const long long U = (long long)p.tiles * p.kblocks;
-    const long long u0 = run_start(c, U, G), u1 = run_start(c + 1, U, G);
-
-    // Nothing the previous grid in the stream may still use is read or
-    // written before it completes; then the next grid may start its CTAs.
-    pdl_wait();
-    pdl_launch_dependents();
+    const int U = p.tiles * p.kblocks;
+    const int u0 = run_start(c, U, G), u1 = run_start(c + 1, U, G);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
-            mbar_init(bar0 + 8u * s, 1);                // full[s]: one expect_tx arrival + TMA bytes
-            mbar_init(bar0 + 8u * (p.stages + s), 1);   // empty[s]: one MMA commit
+            mbar_init(bar0 + 8u * s, 1);                // one expect_tx arrival + the TMA bytes
+            mbar_init(bar0 + 8u * (p.stages + s), 1);   // one MMA commit
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, kEpiThreads);
         mbar_init(drain, 1);
+        mbar_init(red_full, 1);
         fence_barrier_init();
         prefetch_tmap(&mapW);
         prefetch_tmap(&mapX);
@@ -189,49 +401,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    long long issued = 0;  // k-blocks whose copies warp 0 issued
+    int issued = 0;  // k-blocks whose copies warp 0 issued
 
+    // Programmatic dependent launch: this grid may start while the previous
+    // kernel in the stream finishes.  W is never written by the kernels
+    // around it, so warp 0 starts streaming it at once; x, the outputs, the
+    // partials and the counters are touched only after the wait (every
+    // thread waits for itself), and then the next grid may start its CTAs.
     if (warp == 0) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();  // W is read once per launch
-            uint32_t s = 0, ph = 0;
-            bool ok = true;
-            for (long long u = u0; u < u1 && ok;) {
-                const Seg sg = make_seg(u, u1, p, U, G);
-                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!wait_phase(bar0 + 8u * (p.stages + s), ph ^ 1u, p.wait_limit)) {
-                        set_status(p.status, ST_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t a = sbase + s * stage_bytes;
-                    mbar_arrive_expect_tx(bar0 + 8u * s, stage_bytes);
-                    tma_load_2d_hint(a, &mapW, kb * kBK, sg.tile * kBM, bar0 + 8u * s, pol);
-                    tma_load_2d(a + kATile, &mapX, kb * kBK, 0, bar0 + 8u * s);
-                    ++issued;
-                    if (++s == (uint32_t)p.stages) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-                u += sg.kb1 - sg.kb0;
+            const int total = u1 - u0;
+            const int pre = total < p.stages ? total : p.stages;
+            for (int i = 0; i < pre; ++i) {  // first use of stages 0 .. pre - 1: nothing to wait for
+                const int u = u0 + i, tile = u / p.kblocks, kb = u - tile * p.kblocks;
+                mbar_arrive_expect_tx(bar0 + 8u * i, stage_bytes);
+                tma_load_2d_hint(sbase + (uint32_t)i * stage_bytes, &mapW, kb * kBK, tile * kBM, bar0 + 8u * i, pol);
             }
+            pdl_wait();
+            pdl_launch_dependents();
+            for (int i = 0; i < pre; ++i) {
+                const int kb = (u0 + i) % p.kblocks;
+                tma_load_2d(sbase + (uint32_t)i * stage_bytes + kATile, &mapX, kb * kBK, 0, bar0 + 8u * i);
+            }
+            issued = pre;
+            for (int i = pre; i < total; ++i) {
+                const uint32_t s = (uint32_t)(i % p.stages), ph = (uint32_t)((i / p.stages) & 1);
+                if (!wait_spin(bar0 + 8u * (p.stages + s), ph ^ 1u, p.wait_limit)) {
+                    set_status(p.status, ST_TIMEOUT);
+                    break;
+                }
+                const int u = u0 + i, tile = u / p.kblocks, kb = u - tile * p.kblocks;
+                const uint32_t a = sbase + s * stage_bytes;
+                mbar_arrive_expect_tx(bar0 + 8u * s, stage_bytes);
+                tma_load_2d_hint(a, &mapW, kb * kBK, tile * kBM, bar0 + 8u * s, pol);
+                tma_load_2d(a + kATile, &mapX, kb * kBK, 0, bar0 + 8u * s);
+                ++issued;
+            }
+        } else {
+            pdl_wait();
+            pdl_launch_dependents();
         }
         __syncwarp();
     } else if (warp == 1) {
+        pdl_wait();
+        pdl_launch_dependents();
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kBM, p.npad);
             uint32_t s = 0, ph = 0, aph = 0;
             bool ok = true;
-            for (long long u = u0; u < u1 && ok;) {
-                const Seg sg = make_seg(u, u1, p, U, G);
-                if (!wait_phase(acc_empty, aph ^ 1u, p.wait_limit)) {
+            for (int u = u0; u < u1 && ok;) {
+                const Seg sg = make_seg(u, u1, p.kblocks, U, G);
+                if (!wait_spin(acc_empty, aph ^ 1u, p.wait_limit)) {
                     set_status(p.status, ST_TIMEOUT);
                     break;
                 }
                 tc_fence_after();
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!wait_phase(bar0 + 8u * s, ph, p.wait_limit)) {
+                    if (!wait_spin(bar0 + 8u * s, ph, p.wait_limit)) {
                         set_status(p.status, ST_TIMEOUT);
                         ok = false;
                         break;
@@ -256,84 +483,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        const int et = threadIdx.x - 64;  // 0..127
-        const int qw = warp & 3;          // the TMEM lane quarter this warp may read
-        const int m = qw * 32 + lane;     // output feature within the tile = accumulator row
-        const uint32_t trow = tmem + ((uint32_t)(qw * 32) << 16);
-        const int half = p.D / 2;
-        const int nchunks = p.npad / kChunk;
-        uint32_t aph = 0;
-        int nseen = 0;
-        for (long long u = u0; u < u1; ++nseen) {
-            const Seg sg = make_seg(u, u1, p, U, G);
-            u += sg.kb1 - sg.kb0;
-            const int part = sg.tile * kBM / p.HD;
-            const int f0 = sg.tile * kBM - part * p.HD;
-            const bool rope = part < 2;
-            __nv_bfloat16 *dst = (part == 0 ? p.q : (part == 1 ? p.k : p.v)) + f0;
-            float cs = 1.f, sn = 0.f;
-            if (rope) rope_cs(p.pos, p.inv_freq[(m % p.D) % half], cs, sn);
-            // One thread waits for the accumulator; the others learn the
-            // outcome at the barrier, so every epilogue thread takes the same
-            // path through the named barriers below.
-            if (et == 0) flags[nseen & 1] = wait_phase(acc_full, aph, p.wait_limit) ? 1 : 0;
-            named_bar_sync(kEpiBar, kEpiThreads);
-            if (!flags[nseen & 1]) {
-                if (et == 0) set_status(p.status, ST_TIMEOUT);
-                break;
-            }
-            tc_fence_after();
-            aph ^= 1u;
-            if (sg.nseg == 1) {
-                for (int cc = 0; cc < nchunks; ++cc) {
-                    float y[16];
-                    tmem_ld16(trow + (uint32_t)(cc * kChunk), y);
-                    if (cc == nchunks - 1) {
-                        tc_fence_before();
-                        mbar_arrive(acc_empty);
-                    }
-                    finish_chunk(y, cc, m, rope, half, cs, sn, xch, dst, p);
-                }
-            } else {
-                float *mine = p.part + (size_t)slot_of(c, sg.tile, p, U, G) * p.npad * kBM;
-                for (int cc = 0; cc < nchunks; ++cc) {
-                    float y[16];
-                    tmem_ld16(trow + (uint32_t)(cc * kChunk), y);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) __stcg(mine + (size_t)(cc * kChunk + j) * kBM + m, y[j]);
-                }
-                tc_fence_before();
-                mbar_arrive(acc_empty);
-                __threadfence();
-                named_bar_sync(kEpiBar, kEpiThreads);
-                if (et == 0) flags[2] = atomicAdd(p.counters + sg.tile, 1) == sg.nseg - 1 ? 1 : 0;
-                named_bar_sync(kEpiBar, kEpiThreads);
-                if (flags[2]) {
-                    // Last of the tile's CTAs: sum the partials in segment order.
-                    __threadfence();
-                    for (int cc = 0; cc < nchunks; ++cc) {
-                        float y[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) y[j] = 0.f;
-                        for (int jj = 0; jj < sg.nseg; ++jj) {
-                            const float *src =
-                                p.part + (size_t)slot_of(sg.first + jj, sg.tile, p, U, G) * p.npad * kBM;
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) y[j] += __ldcg(src + (size_t)(cc * kChunk + j) * kBM + m);
-                        }
-                        finish_chunk(y, cc, m, rope, half, cs, sn, xch, dst, p);
-                    }
-                    if (et == 0) atomicExch(p.counters + sg.tile, 0);
-                }
-            }
-        }
+        pdl_wait();
+        pdl_launch_dependents();
+        epilogue(p, c, U, G, u0, u1, tmem, acc_full, acc_empty, red_full, smem, sbase, stage_bytes, flags, xch);
     }
 
     __syncthreads();
     if (warp == 0 && lane == 0) {
         // Every copy issued has landed before the CTA's shared memory goes.
         for (int s = 0; s < p.stages && s < issued; ++s) {
-            const long long armed = (issued - 1 - s) / p.stages + 1;
+            const int armed = (issued - 1 - s) / p.stages + 1;
             drain_phase(bar0 + 8u * s, (uint32_t)((armed - 1) & 1));
         }
     }
@@ -370,8 +529,8 @@ constexpr int kMaxStages = 8;
 size_t proj_smem(int stages, size_t stage_bytes)
 {
     const size_t off_bar = (size_t)stages * stage_bytes;
-    const size_t off_xch = (off_bar + 8 * (2 * (size_t)stages + 3) + 16 + 15) & ~(size_t)15;
-    return 1024 + off_xch + sizeof(float) * dsa_proj_k::kChunk * dsa_proj_k::kBM;
+    const size_t off_xch = (off_bar + 8 * (2 * (size_t)stages + dsa_proj_k::kExtraBars) + 32 + 15) & ~(size_t)15;
+    return 1024 + off_xch + sizeof(float) * dsa_proj_k::kXchFloats;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder()
@@ -549,6 +708,10 @@ int dsa_proj_create(int batch, int heads, int head_dim, int hidden, dsa_proj *ou
     p->smem = proj_smem(p->stages, stage_bytes);
     const long long units = (long long)p->tiles * p->kblocks;
     p->grid = (int)(units < sms ? units : sms);
+    if (units * (p->grid + 1) > INT_MAX) {
+        free_proj(p);
+        return fail(DSA_ERR_ARG, "3 * heads * head_dim / 128 x hidden / 64 work units too many for this device");
+    }
     e = cudaFuncSetAttribute(dsa_proj_k::qkv_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem);
     if (e != cudaSuccess) {
         free_proj(p);
@@ -556,7 +719,7 @@ int dsa_proj_create(int batch, int heads, int head_dim, int hidden, dsa_proj *ou
     }
 
     const size_t n = (size_t)batch * p->HD;
-    int rc = dev_alloc((void **)&p->part, sizeof(float) * 2 * (size_t)p->grid * p->npad * dsa_proj_k::kBM,
+    int rc = dev_alloc((void **)&p->part, sizeof(float) * (size_t)p->grid * p->npad * dsa_proj_k::kBM,
                        "projection partials");
     if (rc == DSA_OK) rc = dev_alloc((void **)&p->counters, sizeof(int) * (size_t)p->tiles, "projection counters");
     if (rc == DSA_OK) rc = dev_alloc((void **)&p->status, 16, "projection status");

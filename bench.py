@@ -57,6 +57,16 @@ def measured_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_tflops() -> float:
+    """Burst bf16 dense-GEMM TFLOP/s of this machine's GPUs (cuBLAS, measured),
+    else the fallback figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def profiled_traffic(workload: str):
     """DRAM bytes per launch of the decode kernel from the committed ncu
     summary, or None when the kernel changed since the capture."""
@@ -655,6 +665,110 @@ def run_sweep(args) -> None:
             torch.cuda.empty_cache()
 
 
+def run_fused(args) -> None:
+    """The fused layer step (QKV projection with RoPE on the tensor cores,
+    then the decode kernel on its output) for every layer of the workload,
+    phase-3 steady state; plus the projection kernel alone, back to back over
+    the layers (each layer's W is read from HBM: 30 x 100 MB per step at
+    janus-b96) and with events around each launch.  One JSON line; not the
+    benchmark contract's line."""
+    import numpy as np
+    import torch
+
+    from __graft_entry__ import build
+    from ar_image_gen_gb300.dsa import Proj
+    from ar_image_gen_gb300.synth import ProjGen
+    from oracle.proj import qkv_rope as oracle_qkv_rope
+
+    build()
+    wl = _workload(args)
+    peak, peak_kind = measured_peak()
+    stack = Stack(wl, pool_steps=args.pool)
+    t_start = wl.N_r + wl.sink
+    stack.advance(t_start)
+    pgens = [ProjGen(wl, layer=layer, device="cuda") for layer in range(wl.layers)]
+    Ws = [g.weight() for g in pgens]
+    projs = [Proj(wl.batch, wl.heads, wl.head_dim, g.hidden) for g in pgens]
+    xpool = [[g.x(t_start + i) for g in pgens] for i in range(args.pool)]
+    hidden, HD, B = pgens[0].hidden, wl.heads * wl.head_dim, wl.batch
+    proj_bytes = 3 * HD * hidden * 2 + B * hidden * 2 + 3 * B * HD * 2
+    proj_flops = 2.0 * B * hidden * 3 * HD
+    stream = torch.cuda.current_stream()
+    q, k, v = (torch.empty((wl.streams, wl.head_dim), dtype=torch.bfloat16, device="cuda") for _ in range(3))
+
+    def fused_steps(n):
+        t = stack.handles[0].t
+        for i in range(n):
+            xs = xpool[(t + i - t_start) % args.pool]
+            for layer, h in enumerate(stack.handles):
+                h.decode_step_fused(projs[layer], xs[layer], Ws[layer], stack.outs[layer], stream)
+
+    def proj_steps(n, events=False):
+        evs = []
+        for i in range(n):
+            xs = xpool[i % args.pool]
+            for layer in range(wl.layers):
+                if events:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                projs[layer].qkv_rope(xs[layer], Ws[layer], wl.L_p + t_start + i, q, k, v, stream)
+                if events:
+                    e1.record(stream)
+                    evs.append((e0, e1))
+        return evs
+
+    def timed(fn, *a):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        r = fn(*a)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), r
+
+    fused_steps(args.warmup)
+    plan = stack.handles[0].plan()
+    steps = max(3, min(args.steps, 200))
+    with ClockSampler(None) as clk:
+        el_fused, _ = timed(fused_steps, steps)
+        proj_steps(args.warmup)
+        el_proj, _ = timed(proj_steps, steps)
+    _, evs = timed(proj_steps, max(3, min(steps, 20)), True)
+    iso = statistics.fmean(a.elapsed_time(b) for a, b in evs)
+    per_proj = el_proj / (steps * wl.layers)
+    status = max([h.sync_status() for h in stack.handles] + [p.sync_status() for p in projs], key=abs)
+    # the oracle's projection (numpy fp64) on one layer, for scale
+    x0 = xpool[0][0].double().cpu().numpy()
+    W0 = Ws[0].double().cpu().numpy()
+    t0 = time.perf_counter()
+    oracle_qkv_rope(x0, W0, wl.heads, wl.head_dim, wl.L_p + t_start)
+    cpu_s = time.perf_counter() - t0
+    n_fused = wl.streams * wl.layers * steps
+    line = {
+        "mode": "fused layer step (QKV projection + RoPE on tcgen05, then sparse decode attention)",
+        "config": workload_config(wl, f"phase-3 steady state from t = {t_start}; hidden {hidden}"),
+        "fused": {"value": n_fused / (el_fused / 1e3), "unit": UNIT, "ms_per_step": el_fused / steps,
+                  "ms_per_layer": el_fused / (steps * wl.layers),
+                  "hbm_gbs": (proj_bytes + plan.algo_bytes) * wl.layers * steps / (el_fused / 1e3) / 1e9,
+                  "frac": (proj_bytes + plan.algo_bytes) * wl.layers * steps / (el_fused / 1e3) / 1e9 / peak,
+                  "algo_bytes_per_layer": proj_bytes + plan.algo_bytes, "launches_per_layer": 2 if plan.nsplit == 1 else 3},
+        "projection": {"kernel": "dsa_proj_k::qkv_rope_kernel", "bound": "hbm", "launch_ms": per_proj,
+                       "isolated_launch_ms": iso, "algo_bytes_per_launch": proj_bytes,
+                       "achieved": proj_bytes / (per_proj / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                       "peak_kind": f"{peak_kind} hbm_gbs", "frac": proj_bytes / (per_proj / 1e3) / 1e9 / peak,
+                       "tflops": proj_flops / (per_proj / 1e3) / 1e12,
+                       "tensor_frac_of_bf16_peak": proj_flops / (per_proj / 1e3) / 1e12 / measured_bf16_tflops()},
+        "clocks": clk.summary(), "steps": steps, "warmup": args.warmup,
+        "cpu_baseline": {"seconds_per_layer_projection": cpu_s, "kind": "oracle", "cores": "numpy BLAS",
+                         "sample": "layer 0, one step, fp64 x W^T and RoPE"},
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+    for p_ in projs:
+        p_.close()
+    stack.close()
+
+
 def run_diag(args) -> None:
     """Attention diagnostics (section 3.4: Fig. 8 prompt / local / middle
     weight, Fig. 10 vertical vs diagonal score-vector similarity) of the dense
@@ -726,6 +840,7 @@ def main(argv=None):
     ap.add_argument("--pipeline", type=int, default=0, help="--sweep: force this pipeline shape (1 or 2)")
     ap.add_argument("--trace", action="store_true", help="--sweep: also time whole traces (all phases, 3 runs)")
     ap.add_argument("--diag", action="store_true", help="attention diagnostics of each workload family's dense trace")
+    ap.add_argument("--fused", action="store_true", help="fused layer step: QKV projection + decode, and the projection alone")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -734,6 +849,9 @@ def main(argv=None):
         return
     if args.diag:
         run_diag(args)
+        return
+    if args.fused:
+        run_fused(args)
         return
     rank, ws = dist_setup()
     res = run_reference(args, rank, ws) if args.impl == "reference" else run_ours(args, rank, ws)

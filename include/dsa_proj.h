@@ -45,9 +45,9 @@ typedef struct dsa_proj_ctx *dsa_proj; /* opaque; library-owned */
  *
  * batch in [1, 256]; head_dim 64 or 128; heads * head_dim a multiple of 128
  * (an even head count at head_dim 64); hidden a positive multiple of 64.
- * Allocates on the current device: the split-reduction scratch (at most
- * 2 x SMs x batch (rounded up to 16) x 128 floats plus one counter per 128
- * output features) and bf16 staging for one step's q, k, v (3 x batch x
+ * Allocates on the current device: the split-reduction scratch (SMs x
+ * batch (rounded up to 16) x 128 floats plus one counter per 128 output
+ * features) and bf16 staging for one step's q, k, v (3 x batch x
  * heads x head_dim), used by dsa_decode_step_fused.  Errors: DSA_ERR_ARG,
  * DSA_ERR_OOM, DSA_ERR_CUDA.
  */
@@ -63,10 +63,12 @@ int dsa_proj_destroy(dsa_proj p);
  * W: device, [3 * heads * head_dim, hidden] bf16, row major (see above).
  * q, k, v: device, [batch * heads, head_dim] bf16 each (caller-owned).
  * All 16-byte aligned.  Asynchronous on `stream` (a cudaStream_t; NULL is
- * the legacy default stream); launched as a programmatic dependent launch
- * that reads nothing before the previous kernel in the stream completes.
- * Deterministic: a split output tile is summed in a fixed order.  Launches
- * that use one context must not overlap (one stream, or ordered streams).
+ * the legacy default stream); launched as a programmatic dependent launch:
+ * it starts reading W while the previous kernel in the stream finishes (so
+ * W must not be written by that kernel), and touches x, q, k, v and its
+ * scratch only after that kernel has completed.  Deterministic: an output
+ * tile shared by several CTAs is summed in a fixed order.  Launches that use
+ * one context must not overlap (one stream, or ordered streams).
  * Errors: DSA_ERR_STATE (invalid context), DSA_ERR_ARG (NULL, unaligned or
  * negative arguments), DSA_ERR_CUDA (launch).  Device-side faults (a bounded
  * wait that gave up) are reported by dsa_proj_sync_status.
