@@ -79,12 +79,12 @@ __device__ __forceinline__ int run_start(int c, int U, int G) { return (int)((un
 __device__ __forceinline__ int owner(int u, int U, int G) { return (int)(((unsigned)(u + 1) * G + U - 1) / U) - 1; }
 
 // One piece of a CTA's run: k-blocks [kb0, kb1) of `tile`, and the CTAs
-// whose runs share the tile (first, count).  A run's pieces after its first
-// start at a tile boundary, so a tile shared by several CTAs is split into
-// a head (k-block 0, always the LAST piece of its CTA's run) and pieces that
-// are each the FIRST piece of a later CTA's run.  Each CTA therefore writes
-// at most one partial (slot c), and the head's CTA, which finishes the tile
-// last in time, sums them.
+// whose runs share the tile (first, count; `first` holds k-block 0, the
+// others follow in k order).  A run's pieces after its first start at a tile
+// boundary, so a shared tile consists of a head (k-block 0), which is the
+// LAST piece of its CTA's run, and pieces that are each the FIRST piece of a
+// later CTA's run: every CTA publishes at most one partial (slot c), and the
+// head's CTA, which reaches the tile at the end of its run, sums them.
 struct Seg {
     int tile, kb0, kb1;
     int first, nseg;
@@ -175,34 +175,30 @@ __device__ __forceinline__ void rope_cs(int pos, double inv_freq, float &c, floa
 }
 
 // RoPE (q and k tiles) and bf16 store of `ncol` (16 or 32) accumulator
-// columns c0 .. c0 + ncol - 1 (batch rows) of the tile; y[j] is this thread's
-// value for feature m and column c0 + j.  Through `xch` ([32][128] floats) a
-// head's halves meet (feature m pairs with m ^ half) and the tile is turned
-// so that each thread stores 8 consecutive features of one row as one
-// 16-byte vector.  All 128 epilogue threads call it together.
-__device__ __forceinline__ void finish_cols(float (&y)[32], int ncol, int c0, int m, int et, bool rope, int half,
+// columns c0 .. c0 + ncol - 1 (batch rows) of the tile; y[j] is this
+// thread's value for feature f of the tile and column c0 + j.  A feature's
+// RoPE partner (f +- D/2) sits 8 lanes away in the same warp (the W rows
+// reach the tile interleaved, see the W tensor map), so the rotation needs
+// one shuffle per value.  Through `xch` ([32][128] floats) the tile is then
+// turned so that each thread stores 8 consecutive features of one row as
+// one 16-byte vector.  All 128 epilogue threads call it together.
+__device__ __forceinline__ void finish_cols(float (&y)[32], int ncol, int c0, int f, int et, bool rope, bool upper,
                                             float cs, float sn, float *xch, __nv_bfloat16 *dst, const ProjParams &p)
 {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-        if (j < ncol) xch[j * kBM + m] = y[j];
-    named_bar_sync(kEpiBar, kEpiThreads);
     if (rope) {
-        const bool low = (m & half) == 0;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             if (j < ncol) {
-                const float o = xch[j * kBM + (m ^ half)];
-                y[j] = low ? fmaf(-o, sn, y[j] * cs) : fmaf(o, sn, y[j] * cs);
+                const float o = __shfl_xor_sync(0xffffffffu, y[j], 8);
+                y[j] = upper ? fmaf(o, sn, y[j] * cs) : fmaf(-o, sn, y[j] * cs);
             }
         }
-        named_bar_sync(kEpiBar, kEpiThreads);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (j < ncol) xch[j * kBM + m] = y[j];
-        named_bar_sync(kEpiBar, kEpiThreads);
     }
-    const int g = et & 15, r = et >> 4;  // 8 features [8 g, 8 g + 8) of row r of each group of 8 rows
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+        if (j < ncol) xch[j * kBM + f] = y[j];
+    named_bar_sync(kEpiBar, kEpiThreads);
+    const int g = et & 15, r = et >> 4;  // 8 features [8 g, 8 g + 8) of rows r, r + 8, ...
     for (int j = r; j < ncol; j += 8) {
         const int b = c0 + j;
         if (b < p.B) {
@@ -229,13 +225,51 @@ __device__ __forceinline__ void load_cols(uint32_t taddr, int ncol, float (&y)[3
     }
 }
 
+// Drains this thread's accumulator lane, 32 columns at a time (16 for an odd
+// last chunk), with the TMEM load of the next chunk in flight while `fn`
+// processes the current one: fn(y, ncol, c0, last) with y[0 .. ncol) the
+// fp32 values of columns c0 .. c0 + ncol - 1; `last` marks the final chunk,
+// whose load is the last use of the accumulator.
+template <typename Fn>
+__device__ __forceinline__ void drain_lane(uint32_t trow, int npad, Fn &&fn)
+{
+    uint32_t ra[32], rb[32];
+    auto issue = [&](int c0, uint32_t(&r)[32]) {
+        if (npad - c0 >= 32)
+            tmem_ld32_async(trow + (uint32_t)c0, r);
+        else
+            tmem_ld16_async(trow + (uint32_t)c0, r);
+    };
+    auto run = [&](uint32_t(&r)[32], int c0, bool last) {
+        float y[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(r[j]);
+        fn(y, npad - c0 >= 32 ? 32 : 16, c0, last);
+    };
+    issue(0, ra);
+    tmem_wait_ld(ra);
+    for (int c0 = 0; c0 < npad; c0 += 64) {
+        const bool b_next = c0 + 32 < npad;
+        if (b_next) issue(c0 + 32, rb);
+        run(ra, c0, !b_next);
+        if (!b_next) break;
+        tmem_wait_ld(rb);
+        const bool a_next = c0 + 64 < npad;
+        if (a_next) issue(c0 + 64, ra);
+        run(rb, c0 + 32, !a_next);
+        if (!a_next) break;
+        tmem_wait_ld(ra);
+    }
+}
+
 // The four epilogue warps (threads 64..191): per piece of the CTA's run,
-// drain the accumulator from tensor memory and either write the output
-// (an unshared tile), publish an fp32 partial (a non-head piece of a shared
-// tile), or, for the head of a shared tile, wait until the other pieces are
-// published, fetch them into the now idle stage memory with bulk copies and
-// add them to the head's accumulator in k order (deterministic), then write
-// the output.  Every branch below is uniform over the 128 threads.
+// drain the accumulator from tensor memory and write the output tile; for a
+// tile shared by several CTAs, every piece but the head (k-block 0) publishes
+// an fp32 partial, and the head's CTA, for which the head is the last piece
+// of its run (so its stage memory is idle), waits until the others are out,
+// fetches them with bulk copies and adds all pieces in k order, its own
+// straight from tensor memory.  Every branch below is uniform over the 128
+// threads.
 __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int G, int u0, int u1, uint32_t tmem,
                                          uint32_t acc_full, uint32_t acc_empty, uint32_t red_full,
                                          const unsigned char *smem, uint32_t sbase, uint32_t stage_bytes, int *flags,
@@ -243,13 +277,15 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
 {
     const int et = threadIdx.x - 64;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qw = warp & 3;       // the TMEM lane quarter this warp may read
-    const int m = qw * 32 + lane;  // output feature within the tile = accumulator row
+    const int qw = warp & 3;        // the TMEM lane quarter this warp may read
+    const int L = qw * 32 + lane;   // accumulator row = TMEM lane
+    const int rem = L % p.D;
+    const bool upper = (rem >> 3) & 1;                   // lane L holds the upper half of its head
+    const int jr = (rem >> 4) * 8 + (L & 7);             // rotation index within the half
+    const int f = L - rem + (upper ? p.D / 2 : 0) + jr;  // feature within the tile
     const uint32_t trow = tmem + ((uint32_t)(qw * 32) << 16);
-    const int half = p.D / 2;
-    const int nchunks = p.npad / 16;
-    const uint32_t pbytes = (uint32_t)p.npad * kBM * 4;  // one partial
-    const size_t pslot = (size_t)nchunks * 4 * kBM;      // float4s per partial slot
+    const uint32_t pbytes = (uint32_t)p.npad * kBM * 4;   // one partial
+    const size_t pslot = (size_t)(p.npad / 16) * 4 * kBM;  // float4s per partial slot
     float4 *const part4 = reinterpret_cast<float4 *>(p.part);
     uint32_t aph = 0;
     bool red_armed = false;
@@ -262,7 +298,7 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
         const bool rope = part < 2;
         __nv_bfloat16 *dst = (part == 0 ? p.q : (part == 1 ? p.k : p.v)) + f0;
         float cs = 1.f, sn = 0.f;
-        if (rope) rope_cs(p.pos, p.inv_freq[m % half], cs, sn);  // tiles start at head boundaries
+        if (rope) rope_cs(p.pos, p.inv_freq[jr], cs, sn);
         // One thread waits; the others learn the outcome at the barrier.
         if (et == 0) flags[nseen & 1] = wait_spin(acc_full, aph, p.wait_limit) ? 1 : 0;
         named_bar_sync(kEpiBar, kEpiThreads);
@@ -273,39 +309,41 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
         tc_fence_after();
         aph ^= 1u;
         if (sg.nseg > 1 && sg.kb0 > 0) {
-            // A non-head piece (the first of this CTA's run): publish its
-            // partial in slot c, laid out [chunk][4][128 features] of float4
-            // so that stores and the head's reads are contiguous per warp.
-            float4 *mine = part4 + (size_t)c * pslot + m;
-            for (int c0 = 0; c0 < p.npad; c0 += 32) {
-                const int ncol = p.npad - c0 >= 32 ? 32 : 16;
-                float y[32];
-                load_cols(trow + (uint32_t)c0, ncol, y);
+            // Not the head (so the first piece of this run): publish the
+            // partial in slot c, laid out [16-column chunk][4][128 lanes] of
+            // float4 so that stores and the head's reads are contiguous per warp.
+            float4 *out4 = part4 + (size_t)c * pslot + L;
+            drain_lane(trow, p.npad, [&](float(&y)[32], int ncol, int c0, bool last) {
+                if (last) {
+                    tc_fence_before();
+                    mbar_arrive(acc_empty);
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     if (4 * i < ncol)
-                        __stcg(mine + (size_t)(c0 / 4 + i) * kBM,
+                        __stcg(out4 + (size_t)(c0 / 4 + i) * kBM,
                                make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]));
+            });
+            named_bar_sync(kEpiBar, kEpiThreads);  // every store of the partial issued
+            if (et == 0) {
+                __threadfence();
+                atomicAdd(p.counters + sg.tile, 1);
             }
-            tc_fence_before();
-            mbar_arrive(acc_empty);
-            __threadfence();
-            named_bar_sync(kEpiBar, kEpiThreads);
-            if (et == 0) atomicAdd(p.counters + sg.tile, 1);
             continue;
         }
-        const int nother = sg.nseg - 1;  // published pieces to add (0: unshared tile)
+        const int nother = sg.nseg - 1;  // published pieces to add (0: an unshared tile)
         const bool bulk = nother > 0 && (uint64_t)nother * pbytes <= (uint64_t)p.stages * stage_bytes;
         if (nother > 0) {
             if (et == 0) {
                 int ok = wait_count(p.counters + sg.tile, nother, p.wait_limit) ? 1 : 0;
                 if (ok && bulk) {
-                    // All MMAs of this run are done (the head is its last
-                    // piece), so the stage memory is free for the partials.
+                    // The head is the last piece of this run: every MMA of the
+                    // run is done and the stage memory is idle.
                     fence_proxy_async_all();
                     mbar_arrive_expect_tx(red_full, (uint32_t)nother * pbytes);
                     for (int jj = 0; jj < nother; ++jj) {
-                        const unsigned char *src = reinterpret_cast<const unsigned char *>(part4 + (size_t)(sg.first + 1 + jj) * pslot);
+                        const unsigned char *src =
+                            reinterpret_cast<const unsigned char *>(part4 + (size_t)(sg.first + 1 + jj) * pslot);
                         for (uint32_t off = 0; off < pbytes; off += kBulkPiece) {
                             const uint32_t n = pbytes - off < kBulkPiece ? pbytes - off : kBulkPiece;
                             bulk_g2s(sbase + (uint32_t)jj * pbytes + off, src + off, n, red_full);
@@ -323,23 +361,21 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
             }
             if (bulk) (void)mbar_try_wait(red_full, 0);  // completed: makes the copied bytes visible here too
         }
-        for (int c0 = 0; c0 < p.npad; c0 += 32) {
-            const int ncol = p.npad - c0 >= 32 ? 32 : 16;
-            float y[32];
-            load_cols(trow + (uint32_t)c0, ncol, y);
-            if (c0 + ncol >= p.npad) {
+        drain_lane(trow, p.npad, [&](float(&y)[32], int ncol, int c0, bool last) {
+            if (last) {
                 tc_fence_before();
                 mbar_arrive(acc_empty);
             }
-            for (int jj = 0; jj < nother; ++jj) {  // the other pieces, in k order
+            for (int jj = 0; jj < nother; ++jj) {  // the other pieces, in k order after the head
                 float4 v[8];
                 if (bulk) {
-                    const float4 *src = reinterpret_cast<const float4 *>(smem + (size_t)jj * pbytes) + (size_t)(c0 / 4) * kBM + m;
+                    const float4 *src =
+                        reinterpret_cast<const float4 *>(smem + (size_t)jj * pbytes) + (size_t)(c0 / 4) * kBM + L;
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         if (4 * i < ncol) v[i] = src[i * kBM];
                 } else {
-                    const float4 *src = part4 + (size_t)(sg.first + 1 + jj) * pslot + (size_t)(c0 / 4) * kBM + m;
+                    const float4 *src = part4 + (size_t)(sg.first + 1 + jj) * pslot + (size_t)(c0 / 4) * kBM + L;
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         if (4 * i < ncol) v[i] = __ldcg(src + i * kBM);
@@ -348,11 +384,11 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
                 for (int i = 0; i < 8; ++i)
                     if (4 * i < ncol) add4(y, i, v[i]);
             }
-            finish_cols(y, ncol, c0, m, et, rope, half, cs, sn, xch, dst, p);
-        }
+            finish_cols(y, ncol, c0, f, et, rope, upper, cs, sn, xch, dst, p);
+        });
         if (nother > 0 && et == 0) atomicExch(p.counters + sg.tile, 0);
     }
-    if (red_armed) drain_phase(red_full, 0);  // (et == 0 only) copies in flight land before exit
+    if (red_armed) drain_phase(red_full, 0);  // (et == 0 only) the copies have landed before exit
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -416,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < pre; ++i) {  // first use of stages 0 .. pre - 1: nothing to wait for
                 const int u = u0 + i, tile = u / p.kblocks, kb = u - tile * p.kblocks;
                 mbar_arrive_expect_tx(bar0 + 8u * i, stage_bytes);
-                tma_load_2d_hint(sbase + (uint32_t)i * stage_bytes, &mapW, kb * kBK, tile * kBM, bar0 + 8u * i, pol);
+                tma_load_5d_hint(sbase + (uint32_t)i * stage_bytes, &mapW, kb * kBK, 0, 0, 0, tile * (kBM / p.D), bar0 + 8u * i, pol);
             }
             pdl_wait();
             pdl_launch_dependents();
@@ -434,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int u = u0 + i, tile = u / p.kblocks, kb = u - tile * p.kblocks;
                 const uint32_t a = sbase + s * stage_bytes;
                 mbar_arrive_expect_tx(bar0 + 8u * s, stage_bytes);
-                tma_load_2d_hint(a, &mapW, kb * kBK, tile * kBM, bar0 + 8u * s, pol);
+                tma_load_5d_hint(a, &mapW, kb * kBK, 0, 0, 0, tile * (kBM / p.D), bar0 + 8u * s, pol);
                 tma_load_2d(a + kATile, &mapX, kb * kBK, 0, bar0 + 8u * s);
                 ++issued;
             }
@@ -564,6 +600,29 @@ int encode_operand(CUtensorMap *map, const void *base, int rows, int cols, int b
     return DSA_OK;
 }
 
+// W [3 H D, hidden] seen by TMA as a 5-D tensor whose box is one 128-row
+// tile of 64 columns with the two halves of each head interleaved in blocks
+// of 8 rows: dimensions (column, row r < 8, half h < 2, block k < D/16,
+// group of D rows), row = D group + (D/2) h + 8 k + r, box (64, 8, 2, D/16,
+// 128/D).  The box lands in shared memory in the order r, h, k, group, so
+// tile row (= MMA row = TMEM lane) 16 k + 8 h + r of a head holds feature
+// (D/2) h + 8 k + r, and every feature's rotary partner is 8 lanes away.
+int encode_w_interleaved(CUtensorMap *map, const void *W, int HD, int D, int hidden)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+    if (!encode) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t row = (cuuint64_t)hidden * 2;
+    const cuuint64_t dims[5] = {(cuuint64_t)hidden, 8, 2, (cuuint64_t)(D / 16), (cuuint64_t)(3 * HD / D)};
+    const cuuint64_t strides[4] = {row, row * (D / 2), row * 8, row * D};
+    const cuuint32_t box[5] = {(cuuint32_t)dsa_proj_k::kBK, 8, 2, (cuuint32_t)(D / 16), (cuuint32_t)(dsa_proj_k::kBM / D)};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(W), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled (W) failed (%d)", (int)r);
+    return DSA_OK;
+}
+
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 }  // namespace
@@ -624,7 +683,7 @@ int proj_launch(dsa_proj_ctx *pr, const void *x, const void *W, int pos, void *q
         return fail(DSA_ERR_ARG, "x, W, q, k and v must be 16-byte aligned");
     if (pos < 0) return fail(DSA_ERR_ARG, "pos must be >= 0 (got %d)", pos);
     CUtensorMap mapW, mapX;
-    int rc = encode_operand(&mapW, W, 3 * pr->HD, pr->hidden, dsa_proj_k::kBM, true);
+    int rc = encode_w_interleaved(&mapW, W, pr->HD, pr->D, pr->hidden);
     if (rc == DSA_OK) rc = encode_operand(&mapX, x, pr->B, pr->hidden, pr->npad, false);
     if (rc != DSA_OK) return rc;
 
