@@ -10,9 +10,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libdsa.so")
-SOURCES = [os.path.join(CSRC, f) for f in ("dsa_api.cu", "dsa_diag.cu", "dsa_proj.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("dsa_api.cu", "dsa_diag.cu", "dsa_proj.cu", "dsa_policy.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("dsa_decode.cuh", "dsa_ptx.cuh", "dsa_tc.cuh", "dsa_internal.h")] + [
-    os.path.join(ROOT, "include", h) for h in ("dsa.h", "dsa_diag.h", "dsa_proj.h")]
+    os.path.join(ROOT, "include", h) for h in ("dsa.h", "dsa_diag.h", "dsa_proj.h", "dsa_policy.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -47,7 +47,8 @@ EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa
            "dsa_set_wait_limit", "dsa_debug_copy_state",
            "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc", "dsa_diag_trace",
            "dsa_proj_create", "dsa_proj_destroy", "dsa_qkv_rope", "dsa_decode_step_fused", "dsa_proj_sync_status",
-           "dsa_proj_set_wait_limit"]
+           "dsa_proj_set_wait_limit", "dsa_pol_create", "dsa_pol_destroy", "dsa_pol_prefill", "dsa_pol_decode_step",
+           "dsa_pol_get_positions", "dsa_pol_get_last_eviction", "dsa_pol_sync_status", "dsa_pol_set_wait_limit"]
 
 
 class dsa_step_plan(ctypes.Structure):
@@ -86,6 +87,17 @@ _L.dsa_qkv_rope.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P]
 _L.dsa_decode_step_fused.argtypes = [_P] * 6
 _L.dsa_proj_sync_status.argtypes = [_P, _P]
 _L.dsa_proj_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
+_L.dsa_pol_create.argtypes = [_I] * 6 + [ctypes.POINTER(_P)]
+_L.dsa_pol_destroy.argtypes = [_P]
+_L.dsa_pol_prefill.argtypes = [_P] * 4
+_L.dsa_pol_decode_step.argtypes = [_P] * 6
+_L.dsa_pol_get_positions.argtypes = [_P] * 3
+_L.dsa_pol_get_last_eviction.argtypes = [_P] * 3
+_L.dsa_pol_sync_status.argtypes = [_P] * 2
+_L.dsa_pol_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
+DSA_POLICY_TOVA = 1
+DSA_POLICY_H2O = 2
+POLICIES = {"tova": DSA_POLICY_TOVA, "h2o": DSA_POLICY_H2O}
 
 
 class DSAError(RuntimeError):
@@ -269,7 +281,87 @@ def dsa_proj_set_wait_limit(p, limit) -> int:
     return _L.dsa_proj_set_wait_limit(p, limit)
 
 
+def dsa_pol_create(heads, head_dim, L_p, N_att, policy, dtype):
+    h = _P()
+    return _L.dsa_pol_create(heads, head_dim, L_p, N_att, policy, dtype, ctypes.byref(h)), h
+
+
+def dsa_pol_destroy(h) -> int:
+    return _L.dsa_pol_destroy(h)
+
+
+def dsa_pol_prefill(h, K, V, stream=None) -> int:
+    return _L.dsa_pol_prefill(h, _ptr(K), _ptr(V), _stream(stream))
+
+
+def dsa_pol_decode_step(h, q, k_new, v_new, out, stream=None) -> int:
+    return _L.dsa_pol_decode_step(h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out), _stream(stream))
+
+
+def dsa_pol_get_positions(h, host_dst: np.ndarray, stream=None) -> int:
+    assert host_dst.dtype == np.int32 and host_dst.flags["C_CONTIGUOUS"]
+    return _L.dsa_pol_get_positions(h, host_dst.ctypes.data, _stream(stream))
+
+
+def dsa_pol_get_last_eviction(h, host_dst: np.ndarray, stream=None) -> int:
+    assert host_dst.dtype == np.int32 and host_dst.flags["C_CONTIGUOUS"]
+    return _L.dsa_pol_get_last_eviction(h, host_dst.ctypes.data, _stream(stream))
+
+
+def dsa_pol_sync_status(h, stream=None) -> int:
+    return _L.dsa_pol_sync_status(h, _stream(stream))
+
+
+def dsa_pol_set_wait_limit(h, limit) -> int:
+    return _L.dsa_pol_set_wait_limit(h, limit)
+
+
 # ---- convenience wrappers --------------------------------------------------
+
+class Policy:
+    """A score-based eviction baseline handle (include/dsa_policy.h):
+    `heads` streams, `policy` "tova" or "h2o", N_att attended decode
+    entries, bf16 or f32 rows."""
+
+    def __init__(self, heads, head_dim, L_p, N_att, policy, dtype="bf16"):
+        code, h = dsa_pol_create(heads, head_dim, L_p, N_att, POLICIES[policy], DTYPES[dtype])
+        _check(code, "dsa_pol_create")
+        self.h = h
+        self.heads, self.head_dim, self.L_p, self.N_att, self.policy = heads, head_dim, L_p, N_att, policy
+
+    def close(self):
+        if getattr(self, "h", None):
+            dsa_pol_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prefill(self, K, V, stream=None):
+        _check(dsa_pol_prefill(self.h, K, V, stream), "dsa_pol_prefill")
+
+    def decode_step(self, q, k_new, v_new, out, stream=None):
+        _check(dsa_pol_decode_step(self.h, q, k_new, v_new, out, stream), "dsa_pol_decode_step")
+
+    def positions(self, stream=None) -> np.ndarray:
+        dst = np.zeros((self.heads, self.N_att), dtype=np.int32)
+        _check(dsa_pol_get_positions(self.h, dst, stream), "dsa_pol_get_positions")
+        return dst
+
+    def last_eviction(self, stream=None) -> np.ndarray:
+        dst = np.zeros(self.heads, dtype=np.int32)
+        _check(dsa_pol_get_last_eviction(self.h, dst, stream), "dsa_pol_get_last_eviction")
+        return dst
+
+    def sync_status(self, stream=None) -> int:
+        return dsa_pol_sync_status(self.h, stream)
+
+    def set_wait_limit(self, limit: int):
+        _check(dsa_pol_set_wait_limit(self.h, limit), "dsa_pol_set_wait_limit")
+
 
 class Proj:
     """A QKV projection context (include/dsa_proj.h): `batch` tokens, `heads`

@@ -67,8 +67,11 @@ class PolicyStream:
     def step(self, q, k, v, pick: int = -1):
         """One decode step.  Returns (out [d], info dict).  `pick`, if not
         -1, is another implementation's evicted position: when the oracle's
-        own choice is a near tie with it (within 1e-4 of max(|a|, |b|, 1)),
-        the oracle adopts it and continues from it."""
+        own choice is a near tie with it, the oracle adopts it and continues
+        from it.  Near tie: TOVA logits within 1e-4 of max(|a|, |b|, 1) (the
+        rule for the diagonal method's argmin); H2O accumulated weights, which
+        are non-negative and often far below 1, within 1e-4 of max(|a|, |b|)
+        plus 1e-7."""
         q = np.asarray(q, dtype=np.float64)
         t = self.t
         entry = [t, np.asarray(k, dtype=np.float64).copy(), np.asarray(v, dtype=np.float64).copy(), 0.0]
@@ -139,7 +142,8 @@ class PolicyStream:
             else:
                 a, b = scores[best], scores[j]
                 info["pick_score"] = b
-                if abs(a - b) <= 1e-4 * max(abs(a), abs(b), 1.0):
+                tol = 1e-4 * max(abs(a), abs(b), 1.0) if self.policy == "tova" else 1e-4 * max(abs(a), abs(b)) + 1e-7
+                if abs(a - b) <= tol:
                     chosen = j
                     info["adopted"] = 1
                 else:

@@ -122,3 +122,29 @@ def test_proj_calls_on_a_null_context_fail_cleanly(dsa):
     assert dsa.dsa_proj_sync_status(null) == dsa.DSA_ERR_STATE
     assert dsa.dsa_proj_set_wait_limit(null, 0) == dsa.DSA_ERR_STATE
     assert dsa.dsa_decode_step_fused(null, null, 16, 16, 16) == dsa.DSA_ERR_STATE
+
+
+@pytest.mark.parametrize("args", [
+    (0, 128, 16, 9, 1, 0),       # no streams
+    (4, 96, 16, 9, 1, 0),        # unsupported head_dim
+    (4, 128, -1, 9, 1, 0),       # negative prompt
+    (4, 128, 16, 0, 1, 0),       # N_att < 1
+    (4, 128, 16, 9, 3, 0),       # unknown policy
+    (4, 128, 16, 9, 2, 2),       # FP8 storage not offered for the baselines
+])
+def test_policy_create_rejects_bad_arguments(dsa, args):
+    code, h = dsa.dsa_pol_create(*args)
+    assert code == dsa.DSA_ERR_ARG
+    assert not h.value
+    assert dsa.dsa_last_error()
+
+
+def test_policy_calls_on_a_null_handle_fail_cleanly(dsa):
+    import numpy as np
+
+    null = ctypes.c_void_p()
+    assert dsa.dsa_pol_destroy(null) == dsa.DSA_OK
+    assert dsa.dsa_pol_prefill(null, None, None) == dsa.DSA_ERR_STATE
+    assert dsa.dsa_pol_decode_step(null, 16, 16, 16, 16) == dsa.DSA_ERR_STATE
+    assert dsa.dsa_pol_get_positions(null, np.zeros(4, dtype=np.int32)) == dsa.DSA_ERR_STATE
+    assert dsa.dsa_pol_sync_status(null) == dsa.DSA_ERR_STATE

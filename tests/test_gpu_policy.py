@@ -1,0 +1,148 @@
+"""The score-based eviction baselines (TOVA, H2O) on the GPU, through the C
+ABI, against the fp64 oracle (oracle/policies.py) on the same seeded
+grid-structured traces as the diagonal method.
+
+Per step: outputs within max |out - oracle| <= 2e-3 + 1e-2 |oracle|; the
+evicted position equal to the oracle's, except at a near tie, where the
+oracle adopts the kernel's choice and continues from it; every few steps
+the set of positions each stream's cache holds is compared exactly.
+"""
+from dataclasses import dataclass, field
+
+import numpy as np
+import pytest
+import torch
+
+from ar_image_gen_gb300.synth import TraceGen, Workload
+from oracle.policies import PolicyStream
+from tests.parity import ATOL, RTOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from __graft_entry__ import build
+    build()
+
+
+@dataclass
+class Report:
+    steps: int = 0
+    evictions: int = 0
+    adopted: int = 0
+    max_err: float = 0.0
+    failures: list = field(default_factory=list)
+
+    @property
+    def ok(self):
+        return not self.failures
+
+
+def run_policy(wl: Workload, policy: str, steps: int, sample=None, check_every: int = 1) -> Report:
+    from ar_image_gen_gb300.dsa import DSA_OK, Policy
+
+    gen = TraceGen(wl, device="cuda")
+    S, d = gen.S, wl.head_dim
+    sample = list(range(S)) if sample is None else list(sample)
+    idx = torch.tensor(sample, device="cuda")
+    h = Policy(S, d, wl.L_p, wl.N_att, policy, wl.dtype)
+    Kp, Vp = gen.prompt()
+    h.prefill(Kp, Vp)
+    orc = [PolicyStream(d, wl.L_p, wl.N_att, policy) for _ in sample]
+    Kh, Vh = Kp[idx].double().cpu().numpy(), Vp[idx].double().cpu().numpy()
+    for i, o in enumerate(orc):
+        o.prefill(Kh[i], Vh[i])
+    out = torch.empty((S, d), dtype=Kp.dtype, device="cuda")
+    rep = Report()
+    for t in range(steps):
+        q, k, v = gen.step(t)
+        h.decode_step(q, k, v, out)
+        ev = h.last_eviction()  # synchronizes
+        qh, kh, vh = (x[idx].double().cpu().numpy() for x in (q, k, v))
+        got = out[idx].double().cpu().numpy()
+        for i, s in enumerate(sample):
+            ref, info = orc[i].step(qh[i], kh[i], vh[i], pick=int(ev[s]))
+            err = np.abs(got[i] - ref)
+            rep.max_err = max(rep.max_err, float(err.max()))
+            if (err > ATOL + RTOL * np.abs(ref)).any():
+                rep.failures.append(("out", t, s, float(err.max())))
+            if info["oracle_pick"] >= 0:
+                rep.evictions += 1
+            rep.adopted += info["adopted"]
+            if info["mismatch"] or info["evicted"] != int(ev[s]):
+                rep.failures.append(("evict", t, s, int(ev[s]), info["oracle_pick"], info["min_score"],
+                                     info["pick_score"]))
+        if t % check_every == check_every - 1 or t == steps - 1:
+            pos = h.positions()
+            for i, s in enumerate(sample):
+                have = sorted(int(x) for x in pos[s] if x >= 0)
+                if have != orc[i].positions():
+                    rep.failures.append(("cache", t, s, have[:8], orc[i].positions()[:8]))
+        rep.steps += 1
+        if len(rep.failures) > 10:
+            break
+    st = h.sync_status()
+    if st != DSA_OK:
+        rep.failures.append(("status", st))
+    h.close()
+    return rep
+
+
+def small(name, L_p, N_att, grid=10, heads=4, batch=1, d=128, dtype="bf16", seed=13):
+    return Workload(name, 1, heads, d, dtype, L_p, grid, N_att, N_att, 0, batch, seed)
+
+
+CASES = {
+    # name: (workload, policy, steps)
+    "tova-bf16": (small("tova", 16, 9), "tova", 100),
+    "tova-f32-d64": (small("tovaf", 12, 7, d=64, dtype="f32"), "tova", 90),
+    "tova-n_att-1": (small("tova1", 8, 1, grid=8, heads=3), "tova", 50),
+    "tova-empty-prompt": (small("tova0", 0, 6, grid=9, heads=3), "tova", 70),
+    "tova-bf16-d64-long-window": (small("tovaw", 20, 40, grid=11, heads=2, d=64), "tova", 121),
+    "h2o-bf16": (small("h2o", 16, 9), "h2o", 100),
+    "h2o-f32-d64": (small("h2of", 12, 8, d=64, dtype="f32"), "h2o", 90),
+    "h2o-n_att-1": (small("h2o1", 8, 1, grid=8, heads=3), "h2o", 50),
+    "h2o-n_att-2": (small("h2o2", 8, 2, grid=8, heads=3), "h2o", 50),
+    "h2o-empty-prompt": (small("h2o0", 0, 6, grid=9, heads=3), "h2o", 70),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_policy_parity(name):
+    wl, policy, steps = CASES[name]
+    rep = run_policy(wl, policy, steps)
+    assert rep.ok, (rep.failures[:5], rep.max_err)
+    assert rep.steps == steps
+    if wl.N_att <= steps:
+        assert rep.evictions > 0
+
+
+@pytest.mark.parametrize("policy", ["tova", "h2o"])
+def test_policy_full_size_janus_b96(policy):
+    """Janus-Pro-7B-shaped layer at full size (batch 96 x 32 heads = 3072
+    streams, more than the grid's warps, so warps carry several streams),
+    L_p 64, N_att 29, through 200 steps; 16 sampled streams on the oracle."""
+    wl = Workload("janus-b96", 1, 32, 128, "bf16", 64, 24, 29, 29, 0, 96, 20260918)
+    rep = run_policy(wl, policy, 200, sample=list(range(0, 3072, 193)), check_every=20)
+    assert rep.ok, (rep.failures[:5], rep.max_err)
+    assert rep.evictions > 0
+
+
+def test_policy_timeout_is_reported():
+    from ar_image_gen_gb300.dsa import DSA_ERR_TIMEOUT, Policy
+
+    wl = small("tto", 16, 9)
+    gen = TraceGen(wl, device="cuda")
+    h = Policy(gen.S, wl.head_dim, wl.L_p, wl.N_att, "tova")
+    Kp, Vp = gen.prompt()
+    h.prefill(Kp, Vp)
+    h.set_wait_limit(0)
+    q, k, v = gen.step(0)
+    out = torch.empty_like(q)
+    h.decode_step(q, k, v, out)
+    assert h.sync_status() == DSA_ERR_TIMEOUT
+    torch.cuda.synchronize()  # the context stays usable
+    h.close()
