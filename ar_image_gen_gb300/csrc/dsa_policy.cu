@@ -40,7 +40,10 @@ using namespace dsa;
 
 constexpr int kWarps = 4;
 constexpr int kNbuf = 2;
-constexpr int kStage = 8192;
+// Stage sizes: 8 KB (three CTAs, 12 warps per SM) or 6 KB (four CTAs, 16
+// warps per SM), picked per handle so that the streams take as few rounds
+// of warps as possible.
+constexpr int kStages[2] = {8192, 6144};
 constexpr uint32_t kNoWaitLimit = 0xffffffffu;
 
 struct PolParams {
@@ -62,14 +65,14 @@ struct PolParams {
     int warp_smem;       // bytes of shared memory per warp
 };
 
-template <typename T, int D>
+template <typename T, int D, int STAGE>
 struct PCfg {
     static constexpr int VEC = Elem<T>::VEC;
     static constexpr int LPR = D / (2 * VEC);
     static constexpr int RPW = 32 / LPR;
     static constexpr int KROW = D * (int)sizeof(T);
     static constexpr int ROW = 2 * KROW;
-    static constexpr int SR = kStage / ROW;  // rows per stage
+    static constexpr int SR = STAGE / ROW;  // rows per stage
     static constexpr int NIT = SR / RPW;
     static_assert(SR % RPW == 0, "stage rows fill whole warp instructions");
 };
@@ -99,10 +102,11 @@ __device__ __forceinline__ Rows stream_rows(const PolParams &p, int s)
     return r;
 }
 
-template <typename T, int D, int POL>
+template <typename T, int D, int POL, int STAGE>
 __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
 {
-    using C = PCfg<T, D>;
+    using C = PCfg<T, D, STAGE>;
+    constexpr int kStage = STAGE;
     using EL = Elem<T>;
     using IO = typename EL::IO;
     using Vec = typename EL::Vec;
@@ -408,7 +412,7 @@ struct dsa_pol_ctx {
     uint32_t magic;
     int S, D, L_p, R, policy, dtype;
     int t, prefilled, evicted_last;
-    int sms, grid, warp_smem, smem;
+    int sms, grid, warp_smem, smem, shape;
     uint32_t wait_limit;
     void *prefix, *slots;
     int32_t *slot_pos, *free_slot, *last_evict;
@@ -434,32 +438,40 @@ void free_pol(dsa_pol_ctx *h)
     delete h;
 }
 
-template <typename T, int D, int POL>
+template <typename T, int D, int POL, int STAGE>
 cudaError_t pol_occupancy(int smem, int *ctas)
 {
-    cudaError_t e = cudaFuncSetAttribute(dsa_pol_k::policy_kernel<T, D, POL>,
+    cudaError_t e = cudaFuncSetAttribute(dsa_pol_k::policy_kernel<T, D, POL, STAGE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, dsa_pol_k::policy_kernel<T, D, POL>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, dsa_pol_k::policy_kernel<T, D, POL, STAGE>,
                                                          32 * dsa_pol_k::kWarps, smem);
 }
 
-template <typename T, int D>
-cudaError_t pol_occupancy_d(int policy, int smem, int *ctas)
+template <typename T, int D, int POL>
+cudaError_t pol_occupancy_s(int shape, int smem, int *ctas)
 {
-    return policy == DSA_POLICY_H2O ? pol_occupancy<T, D, DSA_POLICY_H2O>(smem, ctas)
-                                    : pol_occupancy<T, D, DSA_POLICY_TOVA>(smem, ctas);
+    return shape == 0 ? pol_occupancy<T, D, POL, dsa_pol_k::kStages[0]>(smem, ctas)
+                      : pol_occupancy<T, D, POL, dsa_pol_k::kStages[1]>(smem, ctas);
 }
 
-cudaError_t pol_occupancy_any(int dtype, int D, int policy, int smem, int *ctas)
+template <typename T, int D>
+cudaError_t pol_occupancy_d(int policy, int shape, int smem, int *ctas)
+{
+    return policy == DSA_POLICY_H2O ? pol_occupancy_s<T, D, DSA_POLICY_H2O>(shape, smem, ctas)
+                                    : pol_occupancy_s<T, D, DSA_POLICY_TOVA>(shape, smem, ctas);
+}
+
+cudaError_t pol_occupancy_any(int dtype, int D, int policy, int shape, int smem, int *ctas)
 {
     if (dtype == DSA_BF16)
-        return D == 64 ? pol_occupancy_d<__nv_bfloat16, 64>(policy, smem, ctas)
-                       : pol_occupancy_d<__nv_bfloat16, 128>(policy, smem, ctas);
-    return D == 64 ? pol_occupancy_d<float, 64>(policy, smem, ctas) : pol_occupancy_d<float, 128>(policy, smem, ctas);
+        return D == 64 ? pol_occupancy_d<__nv_bfloat16, 64>(policy, shape, smem, ctas)
+                       : pol_occupancy_d<__nv_bfloat16, 128>(policy, shape, smem, ctas);
+    return D == 64 ? pol_occupancy_d<float, 64>(policy, shape, smem, ctas)
+                   : pol_occupancy_d<float, 128>(policy, shape, smem, ctas);
 }
 
-template <typename T, int D, int POL>
+template <typename T, int D, int POL, int STAGE>
 cudaError_t pol_launch(const dsa_pol_k::PolParams &p, int grid, int smem, cudaStream_t st)
 {
     cudaLaunchConfig_t cfg = {};
@@ -472,14 +484,21 @@ cudaError_t pol_launch(const dsa_pol_k::PolParams &p, int grid, int smem, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dsa_pol_k::policy_kernel<T, D, POL>, p);
+    return cudaLaunchKernelEx(&cfg, dsa_pol_k::policy_kernel<T, D, POL, STAGE>, p);
+}
+
+template <typename T, int D, int POL>
+cudaError_t pol_launch_s(int shape, const dsa_pol_k::PolParams &p, int grid, int smem, cudaStream_t st)
+{
+    return shape == 0 ? pol_launch<T, D, POL, dsa_pol_k::kStages[0]>(p, grid, smem, st)
+                      : pol_launch<T, D, POL, dsa_pol_k::kStages[1]>(p, grid, smem, st);
 }
 
 template <typename T, int D>
-cudaError_t pol_launch_d(int policy, const dsa_pol_k::PolParams &p, int grid, int smem, cudaStream_t st)
+cudaError_t pol_launch_d(int policy, int shape, const dsa_pol_k::PolParams &p, int grid, int smem, cudaStream_t st)
 {
-    return policy == DSA_POLICY_H2O ? pol_launch<T, D, DSA_POLICY_H2O>(p, grid, smem, st)
-                                    : pol_launch<T, D, DSA_POLICY_TOVA>(p, grid, smem, st);
+    return policy == DSA_POLICY_H2O ? pol_launch_s<T, D, DSA_POLICY_H2O>(shape, p, grid, smem, st)
+                                    : pol_launch_s<T, D, DSA_POLICY_TOVA>(shape, p, grid, smem, st);
 }
 
 template <typename T, int D>
@@ -530,22 +549,41 @@ int dsa_pol_create(int heads, int head_dim, int L_p, int N_att, int policy, int 
     h->policy = policy;
     h->dtype = dtype;
     h->wait_limit = dsa_pol_k::kNoWaitLimit;
-    h->warp_smem = (dsa_pol_k::kNbuf * dsa_pol_k::kStage + 16 + (policy == DSA_POLICY_H2O ? 4 * N_att : 0) + 127) / 128 * 128;
-    h->smem = dsa_pol_k::kWarps * h->warp_smem;
-
-    int dev = 0, ctas = 0;
+    int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = pol_occupancy_any(dtype, head_dim, policy, h->smem, &ctas);
-    if (e != cudaSuccess || ctas < 1) {
+    if (e != cudaSuccess) {
         free_pol(h);
-        cudaGetLastError();
-        return e != cudaSuccess ? cuda_fail(e, "policy kernel setup (is this an sm_103 device?)")
-                                : fail(DSA_ERR_ARG, "N_att too large for the policy kernel's shared memory");
+        return cuda_fail(e, "device query");
     }
-    const long long want = (heads + dsa_pol_k::kWarps - 1) / dsa_pol_k::kWarps;
-    const long long cap = (long long)h->sms * ctas;
-    h->grid = (int)(want < cap ? want : cap);
+    // Per stage shape: shared memory, resident CTAs, and the rounds of warps
+    // the streams take; the shape with fewer rounds wins (8 KB on a tie).
+    long long best_rounds = LLONG_MAX;
+    for (int sh = 0; sh < 2; ++sh) {
+        const int ws = (dsa_pol_k::kNbuf * dsa_pol_k::kStages[sh] + 16 + (policy == DSA_POLICY_H2O ? 4 * N_att : 0) + 127) /
+                       128 * 128;
+        int ctas = 0;
+        e = pol_occupancy_any(dtype, head_dim, policy, sh, dsa_pol_k::kWarps * ws, &ctas);
+        if (e != cudaSuccess || ctas < 1) {
+            cudaGetLastError();
+            continue;
+        }
+        const long long warps = (long long)h->sms * ctas * dsa_pol_k::kWarps;
+        const long long rounds = (heads + warps - 1) / warps;
+        if (rounds < best_rounds) {
+            best_rounds = rounds;
+            h->shape = sh;
+            h->warp_smem = ws;
+            h->smem = dsa_pol_k::kWarps * ws;
+            const long long want = (heads + dsa_pol_k::kWarps - 1) / dsa_pol_k::kWarps;
+            const long long cap = (long long)h->sms * ctas;
+            h->grid = (int)(want < cap ? want : cap);
+        }
+    }
+    if (best_rounds == LLONG_MAX) {
+        free_pol(h);
+        return fail(DSA_ERR_CUDA, "policy kernel setup failed (is this an sm_103 device, and N_att within shared memory?)");
+    }
 
     const size_t S = (size_t)heads, row = (size_t)row_bytes(dtype, head_dim);
     int rc = dev_alloc(&h->prefix, S * L_p * row, "policy prompt prefix");
@@ -636,11 +674,11 @@ int dsa_pol_decode_step(dsa_pol h, const void *q, const void *k_new, const void 
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e;
     if (h->dtype == DSA_BF16)
-        e = h->D == 64 ? pol_launch_d<__nv_bfloat16, 64>(h->policy, p, h->grid, h->smem, st)
-                       : pol_launch_d<__nv_bfloat16, 128>(h->policy, p, h->grid, h->smem, st);
+        e = h->D == 64 ? pol_launch_d<__nv_bfloat16, 64>(h->policy, h->shape, p, h->grid, h->smem, st)
+                       : pol_launch_d<__nv_bfloat16, 128>(h->policy, h->shape, p, h->grid, h->smem, st);
     else
-        e = h->D == 64 ? pol_launch_d<float, 64>(h->policy, p, h->grid, h->smem, st)
-                       : pol_launch_d<float, 128>(h->policy, p, h->grid, h->smem, st);
+        e = h->D == 64 ? pol_launch_d<float, 64>(h->policy, h->shape, p, h->grid, h->smem, st)
+                       : pol_launch_d<float, 128>(h->policy, h->shape, p, h->grid, h->smem, st);
     if (e != cudaSuccess) return cuda_fail(e, "policy decode launch");
     h->evicted_last = p.full;
     h->t += 1;
@@ -673,6 +711,29 @@ int dsa_pol_sync_status(dsa_pol h, void *stream)
     if (rc != DSA_OK) return rc;
     if (word & dsa::ST_TIMEOUT) return fail(DSA_ERR_TIMEOUT, "a bounded wait in the policy kernel gave up");
     if (word & dsa::ST_CHECK) return fail(DSA_ERR_DEVICE_CHECK, "policy state inconsistent (free slot out of range)");
+    return DSA_OK;
+}
+
+int dsa_pol_set_shape(dsa_pol h, int shape)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid policy handle");
+    if (shape < 0 || shape > 2) return fail(DSA_ERR_ARG, "shape must be 0 (automatic), 1 or 2 (got %d)", shape);
+    if (shape == 0) return DSA_OK;  // keep the choice made at creation
+    const int sh = shape - 1;
+    const int ws = (dsa_pol_k::kNbuf * dsa_pol_k::kStages[sh] + 16 + (h->policy == DSA_POLICY_H2O ? 4 * h->R : 0) + 127) /
+                   128 * 128;
+    int ctas = 0;
+    cudaError_t e = pol_occupancy_any(h->dtype, h->D, h->policy, sh, dsa_pol_k::kWarps * ws, &ctas);
+    if (e != cudaSuccess || ctas < 1) {
+        cudaGetLastError();
+        return fail(DSA_ERR_ARG, "stage shape %d cannot be launched for this handle", shape);
+    }
+    h->shape = sh;
+    h->warp_smem = ws;
+    h->smem = dsa_pol_k::kWarps * ws;
+    const long long want = (h->S + dsa_pol_k::kWarps - 1) / dsa_pol_k::kWarps;
+    const long long cap = (long long)h->sms * ctas;
+    h->grid = (int)(want < cap ? want : cap);
     return DSA_OK;
 }
 

@@ -48,7 +48,8 @@ EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa
            "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc", "dsa_diag_trace",
            "dsa_proj_create", "dsa_proj_destroy", "dsa_qkv_rope", "dsa_decode_step_fused", "dsa_proj_sync_status",
            "dsa_proj_set_wait_limit", "dsa_pol_create", "dsa_pol_destroy", "dsa_pol_prefill", "dsa_pol_decode_step",
-           "dsa_pol_get_positions", "dsa_pol_get_last_eviction", "dsa_pol_sync_status", "dsa_pol_set_wait_limit"]
+           "dsa_pol_get_positions", "dsa_pol_get_last_eviction", "dsa_pol_sync_status", "dsa_pol_set_wait_limit",
+           "dsa_pol_set_shape"]
 
 
 class dsa_step_plan(ctypes.Structure):
@@ -95,6 +96,7 @@ _L.dsa_pol_get_positions.argtypes = [_P] * 3
 _L.dsa_pol_get_last_eviction.argtypes = [_P] * 3
 _L.dsa_pol_sync_status.argtypes = [_P] * 2
 _L.dsa_pol_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
+_L.dsa_pol_set_shape.argtypes = [_P, _I]
 DSA_POLICY_TOVA = 1
 DSA_POLICY_H2O = 2
 POLICIES = {"tova": DSA_POLICY_TOVA, "h2o": DSA_POLICY_H2O}
@@ -316,6 +318,10 @@ def dsa_pol_set_wait_limit(h, limit) -> int:
     return _L.dsa_pol_set_wait_limit(h, limit)
 
 
+def dsa_pol_set_shape(h, shape) -> int:
+    return _L.dsa_pol_set_shape(h, shape)
+
+
 # ---- convenience wrappers --------------------------------------------------
 
 class Policy:
@@ -361,6 +367,9 @@ class Policy:
 
     def set_wait_limit(self, limit: int):
         _check(dsa_pol_set_wait_limit(self.h, limit), "dsa_pol_set_wait_limit")
+
+    def set_shape(self, shape: int):
+        _check(dsa_pol_set_shape(self.h, shape), "dsa_pol_set_shape")
 
 
 class Proj:

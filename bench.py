@@ -769,6 +769,70 @@ def run_fused(args) -> None:
     stack.close()
 
 
+def run_policies(args) -> None:
+    """The score-based eviction baselines (TOVA, H2O) next to the diagonal
+    method on the same workload and budget N_att: per workload family and
+    policy, `layers` distinct layers stepped back to back in the steady state
+    (t >= N_att, every step evicts), average launch time, stream-steps/s and
+    GB/s of algorithmic bytes (K|V rows read, q / k_new / v_new read, out and
+    the new entry written, plus 4 bytes of slot position per attended decode
+    row and, for H2O, 8 bytes of accumulated weight).  One JSON line each;
+    not the benchmark contract's line."""
+    import torch
+    from dataclasses import replace
+
+    from __graft_entry__ import build
+    from ar_image_gen_gb300.dsa import Policy
+    from ar_image_gen_gb300.synth import WORKLOADS, TraceGen
+
+    build()
+    peak, peak_kind = measured_peak()
+    layers = args.layers or 4
+    steps = max(8, min(args.steps, 40))
+    for key in (args.sweep_only.split(",") if args.sweep_only else ["janus-b96", "sweep512-s95", "lumina-s95-b32"]):
+        wl = replace(WORKLOADS[key], layers=layers)
+        d, e, a = wl.head_dim, 2, wl.N_att
+        for policy in ("tova", "h2o"):
+            hs, gens, outs = [], [], []
+            for layer in range(layers):
+                gen = TraceGen(wl, layer=layer, device="cuda")
+                h = Policy(wl.streams, d, wl.L_p, wl.N_att, policy, wl.dtype)
+                Kp, Vp = gen.prompt()
+                h.prefill(Kp, Vp)
+                hs.append(h)
+                gens.append(gen)
+                outs.append(torch.empty((wl.streams, d), dtype=Kp.dtype, device="cuda"))
+            pool = [[gens[l].step(t) for l in range(layers)] for t in range(4)]
+            stream = torch.cuda.current_stream()
+
+            def go(n):
+                for i in range(n):
+                    for l, h in enumerate(hs):
+                        q, k, v = pool[i % 4][l]
+                        h.decode_step(q, k, v, outs[l], stream)
+
+            go(wl.N_att + 3)  # fill the caches; every later step evicts
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            go(steps)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / (steps * layers)
+            per_stream = 2 * d * e * (wl.L_p + a - 1) + 4 * d * e + 2 * d * e + 4 * (a - 1) + (8 * (a - 1) if policy == "h2o" else 0)
+            nbytes = per_stream * wl.streams
+            status = max((h.sync_status() for h in hs), key=abs)
+            line = {"workload": key, "policy": policy, "streams": wl.streams, "layers": layers, "N_att": a,
+                    "L_p": wl.L_p, "ms_per_launch": ms, "stream_steps_per_s": wl.streams / (ms / 1e3),
+                    "algo_bytes_per_launch": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
+                    "frac": nbytes / (ms / 1e3) / 1e9 / peak, "peak": f"{peak} ({peak_kind})", "status": status}
+            print(json.dumps(line), flush=True)
+            for h in hs:
+                h.close()
+            del hs, pool, outs
+            torch.cuda.empty_cache()
+
+
 def run_diag(args) -> None:
     """Attention diagnostics (section 3.4: Fig. 8 prompt / local / middle
     weight, Fig. 10 vertical vs diagonal score-vector similarity) of the dense
@@ -841,6 +905,7 @@ def main(argv=None):
     ap.add_argument("--trace", action="store_true", help="--sweep: also time whole traces (all phases, 3 runs)")
     ap.add_argument("--diag", action="store_true", help="attention diagnostics of each workload family's dense trace")
     ap.add_argument("--fused", action="store_true", help="fused layer step: QKV projection + decode, and the projection alone")
+    ap.add_argument("--policies", action="store_true", help="score-based baselines (TOVA, H2O) on the same workloads")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -852,6 +917,9 @@ def main(argv=None):
         return
     if args.fused:
         run_fused(args)
+        return
+    if args.policies:
+        run_policies(args)
         return
     rank, ws = dist_setup()
     res = run_reference(args, rank, ws) if args.impl == "reference" else run_ours(args, rank, ws)

@@ -86,6 +86,12 @@ int dsa_pol_sync_status(dsa_pol h, void *stream);
 /* Test knob: polls per bounded wait before giving up (0: at once). */
 int dsa_pol_set_wait_limit(dsa_pol h, uint32_t limit);
 
+/* Test knob: force the stage shape (1: 8 KB stages, 12 warps per SM; 2: 6 KB
+ * stages, 16 warps per SM; 0: keep the automatic choice, which takes the
+ * shape that runs the streams in fewer rounds of warps).  Results do not
+ * depend on it. */
+int dsa_pol_set_shape(dsa_pol h, int shape);
+
 #ifdef __cplusplus
 }
 #endif

@@ -41,7 +41,7 @@ class Report:
         return not self.failures
 
 
-def run_policy(wl: Workload, policy: str, steps: int, sample=None, check_every: int = 1) -> Report:
+def run_policy(wl: Workload, policy: str, steps: int, sample=None, check_every: int = 1, shape: int = 0) -> Report:
     from ar_image_gen_gb300.dsa import DSA_OK, Policy
 
     gen = TraceGen(wl, device="cuda")
@@ -49,6 +49,8 @@ def run_policy(wl: Workload, policy: str, steps: int, sample=None, check_every: 
     sample = list(range(S)) if sample is None else list(sample)
     idx = torch.tensor(sample, device="cuda")
     h = Policy(S, d, wl.L_p, wl.N_att, policy, wl.dtype)
+    if shape:
+        h.set_shape(shape)
     Kp, Vp = gen.prompt()
     h.prefill(Kp, Vp)
     orc = [PolicyStream(d, wl.L_p, wl.N_att, policy) for _ in sample]
@@ -110,10 +112,11 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("shape", [1, 2])
 @pytest.mark.parametrize("name", list(CASES))
-def test_policy_parity(name):
+def test_policy_parity(name, shape):
     wl, policy, steps = CASES[name]
-    rep = run_policy(wl, policy, steps)
+    rep = run_policy(wl, policy, steps, shape=shape)
     assert rep.ok, (rep.failures[:5], rep.max_err)
     assert rep.steps == steps
     if wl.N_att <= steps:
