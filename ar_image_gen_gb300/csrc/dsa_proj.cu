@@ -19,12 +19,12 @@
 // per tile) sums the partials in segment order (deterministic) and writes
 // the tile.
 //
-// CTA of 6 warps: warp 0 issues the TMA loads of W and x tiles (128-byte
+// CTA of 10 warps: warp 0 issues the TMA loads of W and x tiles (128-byte
 // swizzle) into a ring of shared-memory stages, warp 1 issues tcgen05.mma
 // (M 128, N = padded batch, K 16; fp32 accumulator in tensor memory), warps
-// 2-5 drain the accumulator with tcgen05.ld (warp w reads TMEM lanes
-// 32 (w % 4) ..), apply RoPE (a head's halves exchange through shared
-// memory) and store bf16.  Every mbarrier wait is bounded; a wait that gives
+// 2-9 drain the accumulator with tcgen05.ld (warp w reads TMEM lanes
+// 32 (w % 4) ..; two warps per lane quarter split the batch columns),
+// apply RoPE (a head's halves meet through a warp shuffle) and store bf16.  Every mbarrier wait is bounded; a wait that gives
 // up sets a status bit and the CTA drains its copies and MMAs and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -47,15 +47,17 @@ namespace dsa_proj_k {
 
 using namespace dsa;
 
-constexpr int kThreads = 192;  // producer warp, MMA warp, 4 epilogue warps
+constexpr int kThreads = 320;  // producer warp, MMA warp, 8 epilogue warps
 constexpr int kBM = 128;       // output features per tile
 constexpr int kBK = 64;        // hidden elements per k-block (one 128-byte swizzled row)
 constexpr int kUK = 16;        // K of one tcgen05.mma kind::f16
 constexpr int kATile = kBM * kBK * 2;
 constexpr int kMaxBatch = 256;
-constexpr int kEpiThreads = 128;
-constexpr int kXchFloats = 32 * kBM;  // epilogue exchange buffer: 32 columns x 128 features
-constexpr uint32_t kEpiBar = 1;
+constexpr int kEpiThreads = 256;   // the epilogue warps
+constexpr int kGroupThreads = 128; // one column group of epilogue warps (one warp per TMEM lane quarter)
+constexpr int kXchBytes = 2 * 32 * kBM * 2;  // per group: 32 columns x 128 features of bf16
+constexpr uint32_t kEpiBar = 1;    // all epilogue warps
+constexpr uint32_t kGroupBar0 = 2; // column groups 0 and 1: barriers 2 and 3
 constexpr int kExtraBars = 4;            // acc_full, acc_empty, drain, red_full
 constexpr uint32_t kBulkPiece = 32768;  // bytes per bulk copy of a partial
 
@@ -179,11 +181,13 @@ __device__ __forceinline__ void rope_cs(int pos, double inv_freq, float &c, floa
 // thread's value for feature f of the tile and column c0 + j.  A feature's
 // RoPE partner (f +- D/2) sits 8 lanes away in the same warp (the W rows
 // reach the tile interleaved, see the W tensor map), so the rotation needs
-// one shuffle per value.  Through `xch` ([32][128] floats) the tile is then
-// turned so that each thread stores 8 consecutive features of one row as
-// one 16-byte vector.  All 128 epilogue threads call it together.
-__device__ __forceinline__ void finish_cols(float (&y)[32], int ncol, int c0, int f, int et, bool rope, bool upper,
-                                            float cs, float sn, float *xch, __nv_bfloat16 *dst, const ProjParams &p)
+// one shuffle per value.  Through the group's `xch` ([32][128] bf16) the
+// tile is then turned so that each thread stores 8 consecutive features of
+// one row as one 16-byte vector.  The 128 threads of one epilogue group
+// (gt = 0..127, named barrier `bar`) call it together.
+__device__ __forceinline__ void finish_cols(float (&y)[32], int ncol, int c0, int f, int gt, uint32_t bar, bool rope,
+                                            bool upper, float cs, float sn, __nv_bfloat16 *xch, __nv_bfloat16 *dst,
+                                            const ProjParams &p)
 {
     if (rope) {
 #pragma unroll
@@ -196,94 +200,67 @@ __device__ __forceinline__ void finish_cols(float (&y)[32], int ncol, int c0, in
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-        if (j < ncol) xch[j * kBM + f] = y[j];
-    named_bar_sync(kEpiBar, kEpiThreads);
-    const int g = et & 15, r = et >> 4;  // 8 features [8 g, 8 g + 8) of rows r, r + 8, ...
+        if (j < ncol) xch[j * kBM + f] = __float2bfloat16_rn(y[j]);
+    named_bar_sync(bar, kGroupThreads);
+    const int g = gt & 15, r = gt >> 4;  // 8 features [8 g, 8 g + 8) of rows r, r + 8, ...
     for (int j = r; j < ncol; j += 8) {
         const int b = c0 + j;
-        if (b < p.B) {
-            const float4 lo = *reinterpret_cast<const float4 *>(xch + j * kBM + 8 * g);
-            const float4 hi = *reinterpret_cast<const float4 *>(xch + j * kBM + 8 * g + 4);
-            uint4 v;
-            v.x = pack_bf16x2(lo.x, lo.y);
-            v.y = pack_bf16x2(lo.z, lo.w);
-            v.z = pack_bf16x2(hi.x, hi.y);
-            v.w = pack_bf16x2(hi.z, hi.w);
-            *reinterpret_cast<uint4 *>(dst + (size_t)b * p.HD + 8 * g) = v;
-        }
+        if (b < p.B)
+            *reinterpret_cast<uint4 *>(dst + (size_t)b * p.HD + 8 * g) =
+                *reinterpret_cast<const uint4 *>(xch + j * kBM + 8 * g);
     }
-    named_bar_sync(kEpiBar, kEpiThreads);  // xch is rewritten by the next call
+    named_bar_sync(bar, kGroupThreads);  // xch is rewritten by the next call
 }
 
-// ncol (16 or 32) accumulator columns of this thread's TMEM lane into y.
-__device__ __forceinline__ void load_cols(uint32_t taddr, int ncol, float (&y)[32])
-{
-    if (ncol == 32) {
-        tmem_ld32(taddr, y);
-    } else {
-        tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(&y[0]));
-    }
-}
-
-// Drains this thread's accumulator lane, 32 columns at a time (16 for an odd
-// last chunk), with the TMEM load of the next chunk in flight while `fn`
-// processes the current one: fn(y, ncol, c0, last) with y[0 .. ncol) the
-// fp32 values of columns c0 .. c0 + ncol - 1; `last` marks the final chunk,
-// whose load is the last use of the accumulator.
+// Drains columns [cb, ce) of this thread's accumulator lane, 32 columns at a
+// time (16 for an odd last chunk): fn(y, ncol, c0, last) with y[0 .. ncol)
+// the fp32 values of columns c0 .. c0 + ncol - 1; `last` marks the final
+// chunk, whose load is this thread's last use of the accumulator.  cb and ce
+// are multiples of 16; an empty range calls nothing.
 template <typename Fn>
-__device__ __forceinline__ void drain_lane(uint32_t trow, int npad, Fn &&fn)
+__device__ __forceinline__ void drain_lane(uint32_t trow, int cb, int ce, Fn &&fn)
 {
-    uint32_t ra[32], rb[32];
-    auto issue = [&](int c0, uint32_t(&r)[32]) {
-        if (npad - c0 >= 32)
-            tmem_ld32_async(trow + (uint32_t)c0, r);
-        else
-            tmem_ld16_async(trow + (uint32_t)c0, r);
-    };
-    auto run = [&](uint32_t(&r)[32], int c0, bool last) {
+    for (int c0 = cb; c0 < ce; c0 += 32) {
+        const int ncol = ce - c0 >= 32 ? 32 : 16;
         float y[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) y[j] = __uint_as_float(r[j]);
-        fn(y, npad - c0 >= 32 ? 32 : 16, c0, last);
-    };
-    issue(0, ra);
-    tmem_wait_ld(ra);
-    for (int c0 = 0; c0 < npad; c0 += 64) {
-        const bool b_next = c0 + 32 < npad;
-        if (b_next) issue(c0 + 32, rb);
-        run(ra, c0, !b_next);
-        if (!b_next) break;
-        tmem_wait_ld(rb);
-        const bool a_next = c0 + 64 < npad;
-        if (a_next) issue(c0 + 64, ra);
-        run(rb, c0 + 32, !a_next);
-        if (!a_next) break;
-        tmem_wait_ld(ra);
+        if (ncol == 32)
+            tmem_ld32(trow + (uint32_t)c0, y);
+        else
+            tmem_ld16(trow + (uint32_t)c0, *reinterpret_cast<float(*)[16]>(&y[0]));
+        fn(y, ncol, c0, c0 + ncol >= ce);
     }
 }
 
-// The four epilogue warps (threads 64..191): per piece of the CTA's run,
-// drain the accumulator from tensor memory and write the output tile; for a
-// tile shared by several CTAs, every piece but the head (k-block 0) publishes
-// an fp32 partial, and the head's CTA, for which the head is the last piece
-// of its run (so its stage memory is idle), waits until the others are out,
+// The eight epilogue warps (threads 64..319), two per TMEM lane quarter: the
+// warps of group 0 (2..5) take the first half of the batch columns, those of
+// group 1 (6..9) the rest.  Per piece of the CTA's run: drain the
+// accumulator from tensor memory and write the output tile; for a tile
+// shared by several CTAs, every piece but the head (k-block 0) publishes an
+// fp32 partial, and the head's CTA, for which the head is the last piece of
+// its run (so its stage memory is idle), waits until the others are out,
 // fetches them with bulk copies and adds all pieces in k order, its own
-// straight from tensor memory.  Every branch below is uniform over the 128
-// threads.
+// straight from tensor memory.  Every branch below is uniform over the 256
+// threads (decisions go through shared flags and the all-epilogue barrier).
 __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int G, int u0, int u1, uint32_t tmem,
                                          uint32_t acc_full, uint32_t acc_empty, uint32_t red_full,
                                          const unsigned char *smem, uint32_t sbase, uint32_t stage_bytes, int *flags,
-                                         float *xch)
+                                         __nv_bfloat16 *xch_base)
 {
-    const int et = threadIdx.x - 64;
+    const int et = threadIdx.x - 64;  // 0..255
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qw = warp & 3;        // the TMEM lane quarter this warp may read
-    const int L = qw * 32 + lane;   // accumulator row = TMEM lane
+    const int qw = warp & 3;          // the TMEM lane quarter this warp may read
+    const int grp = et >> 7;          // column group
+    const int gt = et & 127;          // thread within the group
+    const uint32_t gbar = kGroupBar0 + grp;
+    __nv_bfloat16 *xch = xch_base + grp * 32 * kBM;
+    const int L = qw * 32 + lane;     // accumulator row = TMEM lane
     const int rem = L % p.D;
     const bool upper = (rem >> 3) & 1;                   // lane L holds the upper half of its head
     const int jr = (rem >> 4) * 8 + (L & 7);             // rotation index within the half
     const int f = L - rem + (upper ? p.D / 2 : 0) + jr;  // feature within the tile
     const uint32_t trow = tmem + ((uint32_t)(qw * 32) << 16);
+    const int split = ((p.npad / 16 + 1) / 2) * 16;      // group 0: columns [0, split), group 1: [split, npad)
+    const int cb = grp == 0 ? 0 : split, ce = grp == 0 ? split : p.npad;
     const uint32_t pbytes = (uint32_t)p.npad * kBM * 4;   // one partial
     const size_t pslot = (size_t)(p.npad / 16) * 4 * kBM;  // float4s per partial slot
     float4 *const part4 = reinterpret_cast<float4 *>(p.part);
@@ -308,12 +285,16 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
         }
         tc_fence_after();
         aph ^= 1u;
+        if (cb >= ce) {  // a group without columns (batch <= 16) is done with the accumulator at once
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+        }
         if (sg.nseg > 1 && sg.kb0 > 0) {
             // Not the head (so the first piece of this run): publish the
             // partial in slot c, laid out [16-column chunk][4][128 lanes] of
             // float4 so that stores and the head's reads are contiguous per warp.
             float4 *out4 = part4 + (size_t)c * pslot + L;
-            drain_lane(trow, p.npad, [&](float(&y)[32], int ncol, int c0, bool last) {
+            drain_lane(trow, cb, ce, [&](float(&y)[32], int ncol, int c0, bool last) {
                 if (last) {
                     tc_fence_before();
                     mbar_arrive(acc_empty);
@@ -361,7 +342,7 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
             }
             if (bulk) (void)mbar_try_wait(red_full, 0);  // completed: makes the copied bytes visible here too
         }
-        drain_lane(trow, p.npad, [&](float(&y)[32], int ncol, int c0, bool last) {
+        drain_lane(trow, cb, ce, [&](float(&y)[32], int ncol, int c0, bool last) {
             if (last) {
                 tc_fence_before();
                 mbar_arrive(acc_empty);
@@ -384,8 +365,9 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
                 for (int i = 0; i < 8; ++i)
                     if (4 * i < ncol) add4(y, i, v[i]);
             }
-            finish_cols(y, ncol, c0, f, et, rope, upper, cs, sn, xch, dst, p);
+            finish_cols(y, ncol, c0, f, gt, gbar, rope, upper, cs, sn, xch, dst, p);
         });
+        named_bar_sync(kEpiBar, kEpiThreads);  // both groups are done with this piece
         if (nother > 0 && et == 0) atomicExch(p.counters + sg.tile, 0);
     }
     if (red_armed) drain_phase(red_full, 0);  // (et == 0 only) the copies have landed before exit
@@ -409,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + off_bar + 8u * (2 * p.stages + kExtraBars));
     // flags[0], [1]: accumulator ready (alternating); [2]: partials published; [3]: partials landed
     int *flags = reinterpret_cast<int *>(tmem_slot + 1);
-    float *xch = reinterpret_cast<float *>(smem + ((off_bar + 8u * (2 * p.stages + kExtraBars) + 32u + 15u) & ~15u));
+    __nv_bfloat16 *xch = reinterpret_cast<__nv_bfloat16 *>(smem + ((off_bar + 8u * (2 * p.stages + kExtraBars) + 32u + 15u) & ~15u));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
@@ -566,7 +548,7 @@ size_t proj_smem(int stages, size_t stage_bytes)
 {
     const size_t off_bar = (size_t)stages * stage_bytes;
     const size_t off_xch = (off_bar + 8 * (2 * (size_t)stages + dsa_proj_k::kExtraBars) + 32 + 15) & ~(size_t)15;
-    return 1024 + off_xch + sizeof(float) * dsa_proj_k::kXchFloats;
+    return 1024 + off_xch + dsa_proj_k::kXchBytes;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder()
