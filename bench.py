@@ -602,6 +602,8 @@ def _workload(args):
     wl = WORKLOADS[args.workload]
     if args.layers:
         wl = replace(wl, layers=args.layers)
+    if getattr(args, "calibrated", False):
+        wl = wl.calibrated()
     if args.kv == "fp8":
         wl = wl.fp8()
     return wl
@@ -849,6 +851,8 @@ def run_diag(args) -> None:
     build()
     for key, heads in (("janus-b32", 32), ("sweep512-s95", 32), ("lumina-s95-b16", 32), ("stress-s95", 8)):
         wl = WORKLOADS[key].with_batch(1)
+        if args.calibrated:
+            wl = wl.calibrated()
         g = wl.grid
         dists = sorted({d for d in (1, 2, 4, g - 1, g, g + 1, 2 * g, 4 * g) if 1 <= d < wl.L_dec})
         gen = TraceGen(wl, device="cuda")
@@ -864,7 +868,7 @@ def run_diag(args) -> None:
         mass, vert, diag = diag_trace(Q, Kp, Kd, dists)
         el = time.perf_counter() - t0
         flops = 2.0 * heads * wl.head_dim * sum(wl.L_p + i + 1 for i in range(wl.L_dec))
-        line = {"diagnostic": "attention mass and score-vector similarity", "workload": f"{key}, layer 0, batch 1",
+        line = {"diagnostic": "attention mass and score-vector similarity", "workload": f"{wl.name}, layer 0, batch 1",
                 "heads": heads, "L_p": wl.L_p, "L_dec": wl.L_dec,
                 "mass": {"prompt": mass[0], "local": mass[1], "middle": mass[2]},
                 "similarity": {str(d): {"vertical": v, "diagonal": dg} for d, v, dg in zip(dists, vert, diag)},
@@ -906,6 +910,8 @@ def main(argv=None):
     ap.add_argument("--diag", action="store_true", help="attention diagnostics of each workload family's dense trace")
     ap.add_argument("--fused", action="store_true", help="fused layer step: QKV projection + decode, and the projection alone")
     ap.add_argument("--policies", action="store_true", help="score-based baselines (TOVA, H2O) on the same workloads")
+    ap.add_argument("--calibrated", action="store_true",
+                    help="use the calibrated traces (Fig. 8 attention split) for --diag and the decode bench")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

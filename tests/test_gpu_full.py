@@ -66,3 +66,17 @@ def test_full_size_dense_parity(key):
     rep = run_parity(wl, sample=sample_streams(wl.streams, n), mask_every=256, threads=8)
     assert rep.ok, rep.summary()
     assert rep.selections == 0
+
+
+@pytest.mark.parametrize("key", ["janus-b96", "sweep512-s95", "lumina-s95-b32", "stress-s95"])
+def test_full_size_calibrated_parity(key):
+    """The calibrated traces (attention split as the page's Fig. 8 reports:
+    most weight on the prompt and the local tokens, 6-8.5 % on the middle
+    tokens) at full size: the logits are flatter than in the plain recipe,
+    so the argmin picks are closer together; skip sets stay exact up to
+    accepted near ties."""
+    wl = WORKLOADS[key].calibrated()
+    n = 12 if key == "stress-s95" else 24
+    rep = run_parity(wl, sample=sample_streams(wl.streams, n), mask_every=32, threads=8)
+    assert rep.ok, rep.summary()
+    assert rep.steps == wl.L_dec and rep.selections > 0
