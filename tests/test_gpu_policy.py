@@ -149,3 +149,14 @@ def test_policy_timeout_is_reported():
     assert h.sync_status() == DSA_ERR_TIMEOUT
     torch.cuda.synchronize()  # the context stays usable
     h.close()
+
+
+@pytest.mark.parametrize("policy", ["tova", "h2o"])
+def test_policy_full_size_lumina_b32(policy):
+    """Lumina-mGPT-shaped layer (batch 32 x 32 heads = 1024 streams, L_p 64,
+    N_att 205: 269 rows per stream, fewer streams than warps) through 260
+    steps, into the eviction phase; 8 sampled streams on the oracle."""
+    wl = Workload("lumina-s95-b32", 1, 32, 128, "bf16", 64, 64, 205, 205, 0, 32, 20260920)
+    rep = run_policy(wl, policy, 260, sample=list(range(0, 1024, 131)), check_every=26)
+    assert rep.ok, (rep.failures[:5], rep.max_err)
+    assert rep.evictions > 0

@@ -215,3 +215,11 @@ def test_fused_step_janus_b96_full_size():
     wl = Workload("janus-b96", 1, 32, 128, "bf16", 64, 24, 288, 29, 0, 96, 20260918)
     sample = list(range(0, 3072, 193))
     assert run_fused(wl, hidden=4096, steps=300, sample=sample) > 0
+
+
+def test_fused_step_lumina_b32_through_phase3():
+    """Lumina-mGPT-shaped layer (batch 32, 32 heads of 128, hidden 4096,
+    L_p 64, N_r 2048, N_att 205) through the selection phase into eviction
+    (2100 steps), fused vs two-call bit-exact and sampled oracle parity."""
+    wl = Workload("lumina-s95-b32", 1, 32, 128, "bf16", 64, 64, 2048, 205, 0, 32, 20260920)
+    assert run_fused(wl, hidden=4096, steps=2100, sample=list(range(0, 1024, 171))) > 0
