@@ -119,6 +119,8 @@ struct dsa_ctx {
     float2 *part_ml, *part_min;
     int *status;
     float *scales;         // FP8 storage: [4, S] K scale, V scale, their fp32 inverses (else NULL)
+    int *step_dev;         // graph mode: [0] the step t on the device, [1] CTAs finished (allocated on first use)
+    int graph_mode;
     CUtensorMap ring_map;  // 2-D view of the ring: [S * R rows, 2 * D], one-row box
 };
 
@@ -313,6 +315,7 @@ void free_ctx(dsa_ctx *h)
     cudaFree(h->part_min);
     cudaFree(h->status);
     cudaFree(h->scales);
+    cudaFree(h->step_dev);
     h->magic = 0;
     forget_handle(h);
     delete h;
@@ -692,6 +695,9 @@ int launch_decode_step(dsa_handle h, const void *q, const void *k_new, const voi
 {
     const Plan pl = make_plan(h, h->t);
     if ((long long)pl.nsplit * h->S > INT_MAX) return fail(DSA_ERR_ARG, "grid too large");
+    if (h->graph_mode && pl.phase != 3)
+        return fail(DSA_ERR_STATE, "graph mode runs the steady state only (t - sink >= N_r - sink); step %d is in phase %d",
+                    h->t, pl.phase);
     int rc = ensure_partials(h, pl.nsplit);
     if (rc != DSA_OK) return rc;
 
@@ -731,6 +737,8 @@ int launch_decode_step(dsa_handle h, const void *q, const void *k_new, const voi
     p.kinv = h->scales ? h->scales + 2 * (size_t)h->S : nullptr;
     p.vinv = h->scales ? h->scales + 3 * (size_t)h->S : nullptr;
     p.wait_limit = h->wait_limit;
+    p.step_dev = h->graph_mode ? h->step_dev : nullptr;
+    p.sink = h->sink;
 
     const bool other = note_launch(st, h);
     p.early = (other || after_proj) ? 1 : 0;
@@ -855,6 +863,39 @@ int dsa_set_kv_scales(dsa_handle h, const float *k_scale, const float *v_scale)
     int rc = upload_scales(h, k_scale, v_scale);
     if (rc != DSA_OK) return rc;
     h->prefilled = 0;  // rows stored with the old scales are gone: dsa_prefill must follow
+    return DSA_OK;
+}
+
+int dsa_set_graph_mode(dsa_handle h, int on)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (!on) {
+        h->graph_mode = 0;
+        return DSA_OK;
+    }
+    if (!h->step_dev) {
+        int rc = dev_alloc((void **)&h->step_dev, 2 * sizeof(int), "device step counter");
+        if (rc != DSA_OK) return rc;
+    }
+    // Earlier launches may still be in flight; the counter starts at the host's step.
+    cudaError_t e = cudaDeviceSynchronize();
+    const int init[2] = {h->t, 0};
+    if (e == cudaSuccess) e = cudaMemcpy(h->step_dev, init, sizeof init, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "device step counter");
+    h->graph_mode = 1;
+    return DSA_OK;
+}
+
+int dsa_sync_step(dsa_handle h, void *stream)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (!h->graph_mode) return DSA_OK;
+    int t = 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(&t, h->step_dev, sizeof t, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "device step copy");
+    h->t = t;
     return DSA_OK;
 }
 
@@ -1042,6 +1083,8 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.qscale = (float)(1.4426950408889634 / std::sqrt((double)head_dim));
     p.kscale = p.vscale = p.kinv = p.vinv = nullptr;
     p.wait_limit = kDefaultWaitLimit;
+    p.step_dev = nullptr;
+    p.sink = sink;
     p.early = 0;  // caller-owned state: the previous kernel may have written it
     e = launch_step(dtype, head_dim, pl.shape, p, h.ring_map, pl.grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");

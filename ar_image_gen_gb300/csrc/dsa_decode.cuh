@@ -106,6 +106,8 @@ struct DecodeParams {
     int select;           // 1: selection step (fused argmin)
     int noskip;           // 1: N_att == N_r, no offset is ever skipped
     int MW;               // mask words per stream
+    int *step_dev;        // graph mode: [0] the decode step t on the device, [1] CTAs finished (NULL: host values)
+    int sink;             // t - t' (graph mode derives t' mod R from [0])
     int early;            // 1: the previous grid in the stream does not write this state, so
                           // the mask, prefix and ring may be read before the grid dependency wait
     float qscale;         // log2(e) / sqrt(D), applied to q.k
@@ -430,6 +432,9 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
         pdl_wait();
         pdl_launch_dependents();
     }
+    // Graph mode: the step comes from device memory (advanced by the last CTA
+    // of the previous launch of this state, which has completed here).
+    const int tin_mod = p.step_dev ? (__ldcg(p.step_dev) - p.sink) % p.R : p.tin_mod;
     if (first_item < p.nitems && inreg && nwords > 0) load_words(first_item);
 
     bool aborted = false;
@@ -551,11 +556,11 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
             if (p.noskip) {
                 // offset r = rank: descending slots, at most two contiguous runs
                 if (lane == 0) {
-                    const int kA = min(k0 + nr, p.tin_mod + 1);
+                    const int kA = min(k0 + nr, tin_mod + 1);
                     const int nA = max(kA - k0, 0);
-                    if (nA > 0) bulk_g2s_hint(rd, rng + (size_t)(p.tin_mod - (kA - 1)) * C::ROW, nA * C::ROW, fb, pol);
+                    if (nA > 0) bulk_g2s_hint(rd, rng + (size_t)(tin_mod - (kA - 1)) * C::ROW, nA * C::ROW, fb, pol);
                     if (nr > nA)
-                        bulk_g2s_hint(rd + nA * C::ROW, rng + (size_t)(p.tin_mod - (k0 + nr - 1) + p.R) * C::ROW,
+                        bulk_g2s_hint(rd + nA * C::ROW, rng + (size_t)(tin_mod - (k0 + nr - 1) + p.R) * C::ROW,
                                       (nr - nA) * C::ROW, fb, pol);
                 }
             } else {
@@ -567,14 +572,14 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
                     int y[4];
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
-                        const int sl = p.tin_mod - (int)lst[k + m];
+                        const int sl = tin_mod - (int)lst[k + m];
                         y[m] = ybase + (sl < 0 ? sl + p.R : sl);
                     }
                     tma_gather4(rd + 4 * g4 * C::ROW, &tmap, 0, y[0], y[1], y[2], y[3], fb);
                 }
                 const int tail = nr - 4 * ngrp;
                 if (lane < tail) {
-                    int sl = p.tin_mod - (int)lst[k0 + 4 * ngrp + lane - I_klo];
+                    int sl = tin_mod - (int)lst[k0 + 4 * ngrp + lane - I_klo];
                     sl = sl < 0 ? sl + p.R : sl;
                     bulk_g2s_hint(rd + (4 * ngrp + lane) * C::ROW, rng + (size_t)sl * C::ROW, C::ROW, fb, pol);
                 }
@@ -645,7 +650,7 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
         // rank 0 is the current token (offset 0) unless it is itself skipped
         const bool has_cur = (klo == 0 && khi > 0 && !self_skip);
         T *const cur_dst = p.sinkmode ? reinterpret_cast<T *>(p.prefix) + ((size_t)s * p.Lcap + p.P) * 2 * D
-                                      : reinterpret_cast<T *>(p.ring) + ((size_t)s * p.R + p.tin_mod) * 2 * D;
+                                      : reinterpret_cast<T *>(p.ring) + ((size_t)s * p.R + tin_mod) * 2 * D;
         // FP8 storage: per-stream scales (1 otherwise)
         const float kinv = EL::SCALED ? __ldg(p.kinv + s) : 1.f;
         const float vinv = EL::SCALED ? __ldg(p.vinv + s) : 1.f;
@@ -822,6 +827,18 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
         for (int q = consumed; q < issued; ++q) drain_phase(bar0 + 8 * (q % C::NBUF), (q / C::NBUF) & 1);
     }
     __syncwarp();
+    if (p.step_dev) {
+        // Graph mode: the last CTA to finish advances the device step (every
+        // CTA of this launch has read it by then).
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(p.step_dev + 1, 1) == (int)gridDim.x - 1) {
+                p.step_dev[1] = 0;
+                atomicAdd(p.step_dev, 1);
+            }
+        }
+    }
 }
 
 // a7: merges the per-split partials of every stream after a decode launch

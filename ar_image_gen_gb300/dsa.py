@@ -45,7 +45,8 @@ EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa
            "dsa_get_skip_mask", "dsa_get_last_selection", "dsa_sync_status", "dsa_last_error",
            "dsa_state_bytes", "dsa_plan_step", "dsa_set_kv_scales", "dsa_set_splits", "dsa_set_pipeline",
            "dsa_set_wait_limit", "dsa_debug_copy_state",
-           "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc", "dsa_diag_trace",
+           "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc", "dsa_diag_trace", "dsa_set_graph_mode",
+           "dsa_sync_step",
            "dsa_proj_create", "dsa_proj_destroy", "dsa_qkv_rope", "dsa_decode_step_fused", "dsa_proj_sync_status",
            "dsa_proj_set_wait_limit", "dsa_pol_create", "dsa_pol_destroy", "dsa_pol_prefill", "dsa_pol_decode_step",
            "dsa_pol_get_positions", "dsa_pol_get_last_eviction", "dsa_pol_sync_status", "dsa_pol_set_wait_limit",
@@ -80,6 +81,8 @@ _L.dsa_debug_copy_state.argtypes = [_P, _P, _P]
 _L.dsa_set_pipeline.argtypes = [_P, _I]
 _L.dsa_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
 _L.dsa_debug_fail_alloc_after.argtypes = [_I]
+_L.dsa_set_graph_mode.argtypes = [_P, _I]
+_L.dsa_sync_step.argtypes = [_P, _P]
 _L.dsa_decode_step_noalloc.argtypes = [_I] * 8 + [_P] * 9
 _L.dsa_diag_trace.argtypes = [_I] * 5 + [_P] * 3 + [_I] + [_P] * 6
 _L.dsa_proj_create.argtypes = [_I] * 4 + [ctypes.POINTER(_P)]
@@ -224,6 +227,14 @@ def dsa_set_wait_limit(h, limit) -> int:
 
 def dsa_debug_fail_alloc_after(n) -> int:
     return _L.dsa_debug_fail_alloc_after(n)
+
+
+def dsa_set_graph_mode(h, on) -> int:
+    return _L.dsa_set_graph_mode(h, 1 if on else 0)
+
+
+def dsa_sync_step(h, stream=None) -> int:
+    return _L.dsa_sync_step(h, _stream(stream))
 
 
 def dsa_decode_step_noalloc(heads, head_dim, L_p, N_r, N_att, sink, dtype, t, prefix, ring, mask, last_sel,
@@ -479,3 +490,10 @@ class DSA:
 
     def set_wait_limit(self, limit: int):
         _check(dsa_set_wait_limit(self.h, limit), "dsa_set_wait_limit")
+
+    def set_graph_mode(self, on: bool):
+        """Steady-state steps replayable from a CUDA graph (the step lives on the device)."""
+        _check(dsa_set_graph_mode(self.h, on), "dsa_set_graph_mode")
+
+    def sync_step(self, stream=None):
+        _check(dsa_sync_step(self.h, stream), "dsa_sync_step")

@@ -359,6 +359,42 @@ def time_trace(stack, runs: int):
             "algo_bytes_per_trace": nbytes}
 
 
+def time_graph(stack, steps: int, ws: int) -> dict:
+    """Steady-state steps replayed from a CUDA graph that holds one decode
+    step of every layer (graph mode), timed with CUDA events; returns
+    stream-steps/s and the average launch time.  The handles return to host
+    steps afterwards."""
+    import torch
+
+    wl = stack.wl
+    for h in stack.handles:
+        h.set_graph_mode(True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for layer, h in enumerate(stack.handles):
+            q, k, v = stack.pool[0][layer]
+            h.decode_step(q, k, v, stack.outs[layer])
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(steps):
+            g.replay()
+    end.record(s)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(start.elapsed_time(end), ws)
+    for h in stack.handles:
+        h.sync_step()
+        h.set_graph_mode(False)
+    return {"value": wl.streams * wl.layers * steps * ws / (ms / 1e3), "unit": UNIT, "steps": steps,
+            "ms_per_step": ms / steps, "launch_ms": ms / (steps * wl.layers)}
+
+
 def time_e2e(stack, steps: int):
     """Same metric through the public API with host-resident inputs, as a
     pipelined caller would run it: every step copies q, k_new, v_new of all
@@ -466,6 +502,15 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     whole = plan.algo_bytes * wl.layers * args.steps * ws / (el_ms / 1e3) / 1e9
     traffic = profiled_traffic(wl.name)
 
+    # --- the same steady state replayed from a CUDA graph (graph mode: the
+    # step lives on the device; one capture of all layers, replayed per step;
+    # inputs are the pool's first step in every replay, which does not change
+    # the work)
+    graph = None
+    if args.graph:
+        graph = time_graph(stack, max(4, min(args.steps, 200)), ws)
+        graph["frac"] = plan.algo_bytes / (graph["launch_ms"] / 1e3) / 1e9 / measured_peak()[0]
+
     # --- end to end through the public API with host buffers
     e2e_steps = max(3, min(args.steps // 4, 100))
     e2e_ms, h2d, d2h = time_e2e(stack, e2e_steps)
@@ -534,6 +579,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         "clocks": clk.summary(),
         "last_step": {"sparse_ms": last_sparse_ms},
         "trace": trace,
+        "graph": graph,
         "dense": dense,
         "device_status": status,
     }
@@ -897,6 +943,7 @@ def main(argv=None):
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-trace", action="store_true", help="skip the whole-trace timing")
+    ap.add_argument("--graph", action="store_true", help="also time the steady state replayed from a CUDA graph")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-streams", type=int, default=256, help="streams per step of the reference arm")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")

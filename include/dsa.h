@@ -267,6 +267,28 @@ int dsa_debug_copy_state(dsa_handle h, void *host_prefix, void *host_ring);
  * real hang. */
 int dsa_set_wait_limit(dsa_handle h, uint32_t limit);
 
+/*
+ * dsa_set_graph_mode -- CUDA-graph-replayable steady-state steps (not part of
+ * the method; a runtime option).  With on != 0 the decode kernel takes the
+ * step t from a counter in device memory (started at the handle's current
+ * step) and the last CTA of every launch advances it, so a stream capture of
+ * one dsa_decode_step per handle (e.g. all layers of one decode step) can be
+ * replayed once per step with the same arguments: each replay decodes the
+ * next step.  Only the steady state may run in this mode (t - sink >=
+ * N_r - sink: every step evicts, none selects); dsa_decode_step returns
+ * DSA_ERR_STATE before it.  Replays do not pass through the host, so the
+ * handle's host-side step is stale until dsa_sync_step.  The inputs of a
+ * replayed step are whatever the captured pointers hold at replay time.
+ * Synchronizes the device when switching on.  on == 0 returns to host-side
+ * steps (call dsa_sync_step first).  Errors: DSA_ERR_STATE, DSA_ERR_OOM,
+ * DSA_ERR_CUDA.
+ */
+int dsa_set_graph_mode(dsa_handle h, int on);
+
+/* Graph mode: waits for `stream` and sets the handle's step from the device
+ * counter (no-op otherwise). */
+int dsa_sync_step(dsa_handle h, void *stream);
+
 /* Make the n-th following device allocation of this library fail (n >= 1),
  * or disable with n <= 0.  Host-side; tests the out-of-memory paths. */
 int dsa_debug_fail_alloc_after(int n);
