@@ -146,6 +146,7 @@ struct Elem<float> {
     using IO = float;                   // type of q, k_new, v_new, prompt K / V and out
     using Vec = uint4;                  // one stored vector of a K or V row
     static constexpr bool SCALED = false;
+    static constexpr float kWiden = 1.f;  // value of a stored element / the value the math reads
     static constexpr int VEC = 4;       // elements per Vec
     struct Q { float x[4]; };
     static __device__ __forceinline__ Q load_q(const uint4 &v)
@@ -181,6 +182,7 @@ struct Elem<__nv_bfloat16> {
     using IO = __nv_bfloat16;
     using Vec = uint4;
     static constexpr bool SCALED = false;
+    static constexpr float kWiden = 1.f;
     static constexpr int VEC = 8;
     struct Q { uint4 raw; };  // q stays packed bf16: the dot uses mixed-precision FMAs
     static __device__ __forceinline__ Q load_q(const uint4 &v) { return Q{v}; }
@@ -227,15 +229,29 @@ struct Elem<__nv_bfloat16> {
 // scale.  The kernel keeps the scales out of the inner loops: logits are
 // q . code (times the K scale, applied once per logit with the softmax
 // scale) and P.V accumulates p * code (times the V scale at the end).
-// Codes widen exactly to f16 (cvt), q is rounded to f16 once per item, and
+// q is rounded to f16 once per item, codes widen exactly to f16, and
 // products accumulate in fp32 (mixed-precision FMA).
+//
+// Widening by bit moves instead of a conversion instruction: a code with
+// sign s, exponent field e (4 bits) and mantissa m (3 bits), read as the
+// f16 bits s << 15 | e << 10 | m << 7, is the code's value times 2^-8 --
+// 2^(e-15) (1 + m/8) against 2^(e-7) (1 + m/8) for normal codes, and
+// 2^-14 m/8 against 2^-6 m/8 for subnormal ones (e = 0 in both formats).
+// The factor 2^8 (kWiden) goes into the K scale of each logit and the V
+// scale of each output; powers of two scale without rounding, so results
+// are those of the codes' exact f16 values.  (The NaN codes 0x7F / 0xFF
+// would read as finite values; the stored inputs are finite.)
 __device__ __forceinline__ uint32_t f16x2_bits(__half2 h) { return *reinterpret_cast<const uint32_t *>(&h); }
 
-// The two f16 halves (low, high) of the codes in the 16-bit value c2.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t c2)
+// f16x2 (value * 2^-8) of codes 1 and 3 of the four codes in w (byte i = code i).
+__device__ __forceinline__ uint32_t e4m3_odd_f16x2(uint32_t w)
 {
-    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(c2 & 0xffffu), __NV_E4M3);
-    return (uint32_t)r.x | ((uint32_t)r.y << 16);
+    return (w & 0x80008000u) | ((w >> 1) & 0x3F803F80u);
+}
+// f16x2 (value * 2^-8) of codes 0 and 2 of the four codes in w.
+__device__ __forceinline__ uint32_t e4m3_even_f16x2(uint32_t w)
+{
+    return ((w << 8) & 0x80008000u) | ((w << 7) & 0x3F803F80u);
 }
 
 // acc0 += lo(a) * lo(b), acc1 += hi(a) * hi(b) for f16x2 a, b in fp32.
@@ -254,31 +270,42 @@ struct Elem<__nv_fp8_e4m3> {
     using Vec = uint2;                  // 8 codes
     static constexpr bool SCALED = true;
     static constexpr int VEC = 8;
-    struct Q { uint32_t h[4]; };        // 8 q elements as f16 pairs
+    static constexpr float kWiden = 256.f;  // code value / widened f16 value
+    // 8 q elements as f16 pairs in the order the widened codes come in:
+    // (0, 2), (1, 3), (4, 6), (5, 7)
+    struct Q { uint32_t h[4]; };
     static __device__ __forceinline__ Q load_q(const uint4 &v)  // 8 bf16
     {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        Q q;
+        float f[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            q.h[i] = f16x2_bits(__floats2half2_rn(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u)));
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+        Q q;
+        q.h[0] = f16x2_bits(__floats2half2_rn(f[0], f[2]));
+        q.h[1] = f16x2_bits(__floats2half2_rn(f[1], f[3]));
+        q.h[2] = f16x2_bits(__floats2half2_rn(f[4], f[6]));
+        q.h[3] = f16x2_bits(__floats2half2_rn(f[5], f[7]));
         return q;
     }
+    // q . code * 2^-8 (partial sums)
     static __device__ __forceinline__ void dot(const Q &q, const uint2 &k, float &s0, float &s1)
     {
-        fma2_f16_f32(s0, s1, e4m3x2_to_f16x2(k.x), q.h[0]);
-        fma2_f16_f32(s0, s1, e4m3x2_to_f16x2(k.x >> 16), q.h[1]);
-        fma2_f16_f32(s0, s1, e4m3x2_to_f16x2(k.y), q.h[2]);
-        fma2_f16_f32(s0, s1, e4m3x2_to_f16x2(k.y >> 16), q.h[3]);
+        fma2_f16_f32(s0, s1, e4m3_even_f16x2(k.x), q.h[0]);
+        fma2_f16_f32(s0, s1, e4m3_odd_f16x2(k.x), q.h[1]);
+        fma2_f16_f32(s0, s1, e4m3_even_f16x2(k.y), q.h[2]);
+        fma2_f16_f32(s0, s1, e4m3_odd_f16x2(k.y), q.h[3]);
     }
-    // acc[0..7] += p * v (p rounded to f16, products in fp32)
+    // acc[0..7] += p * code * 2^-8 (p rounded to f16, products in fp32)
     static __device__ __forceinline__ void axpy(float p, const uint2 &v, float *acc)
     {
         const uint32_t pp = f16x2_bits(__float2half2_rn(p));
-        fma2_f16_f32(acc[0], acc[1], e4m3x2_to_f16x2(v.x), pp);
-        fma2_f16_f32(acc[2], acc[3], e4m3x2_to_f16x2(v.x >> 16), pp);
-        fma2_f16_f32(acc[4], acc[5], e4m3x2_to_f16x2(v.y), pp);
-        fma2_f16_f32(acc[6], acc[7], e4m3x2_to_f16x2(v.y >> 16), pp);
+        fma2_f16_f32(acc[0], acc[2], e4m3_even_f16x2(v.x), pp);
+        fma2_f16_f32(acc[1], acc[3], e4m3_odd_f16x2(v.x), pp);
+        fma2_f16_f32(acc[4], acc[6], e4m3_even_f16x2(v.y), pp);
+        fma2_f16_f32(acc[5], acc[7], e4m3_odd_f16x2(v.y), pp);
     }
     static __device__ __forceinline__ __nv_bfloat16 narrow(float x) { return __float2bfloat16_rn(x); }
     static __device__ __forceinline__ uint4 pack(const float *a, float scale)
@@ -654,7 +681,7 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
         // FP8 storage: per-stream scales (1 otherwise)
         const float kinv = EL::SCALED ? __ldg(p.kinv + s) : 1.f;
         const float vinv = EL::SCALED ? __ldg(p.vinv + s) : 1.f;
-        const float xs = EL::SCALED ? p.qscale * __ldg(p.kscale + s) : p.qscale;
+        const float xs = EL::SCALED ? p.qscale * (__ldg(p.kscale + s) * EL::kWiden) : p.qscale;
         const IO *kio = reinterpret_cast<const IO *>(p.knew) + (size_t)s * D;
         const IO *vio = reinterpret_cast<const IO *>(p.vnew) + (size_t)s * D;
         Vec kc0, kc1, vc0, vc1;
@@ -794,7 +821,7 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
         }
         if (p.nsplit == 1) {
             if (g == 0) {
-                const float inv = (EL::SCALED ? __ldg(p.vscale + s) : 1.f) / l;
+                const float inv = (EL::SCALED ? __ldg(p.vscale + s) * EL::kWiden : 1.f) / l;
                 uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<IO *>(p.out) + (size_t)s * D);
                 o[cl] = EL::pack(acc, inv);
                 o[cl + C::LPR] = EL::pack(acc + C::VEC, inv);
@@ -876,7 +903,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodePar
         }
     }
     typename EL::IO *o = reinterpret_cast<typename EL::IO *>(p.out) + (size_t)s * D + lane * DPL;
-    const float inv = (EL::SCALED ? __ldg(p.vscale + s) : 1.f) / Lx;
+    const float inv = (EL::SCALED ? __ldg(p.vscale + s) * EL::kWiden : 1.f) / Lx;
 #pragma unroll
     for (int e = 0; e < DPL; ++e) o[e] = EL::narrow(O[e] * inv);
     if (p.select) {
