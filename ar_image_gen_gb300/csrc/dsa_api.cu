@@ -76,6 +76,8 @@ namespace {
 using dsa_detail::cuda_fail;
 using dsa_detail::dev_alloc;
 using dsa_detail::fail;
+using dsa_detail::forget_handle;
+using dsa_detail::note_launch;
 
 constexpr uint32_t kMagic = 0x44534131u;  // "DSA1"
 constexpr uint32_t kDefaultWaitLimit = 0xffffffffu;
@@ -301,8 +303,6 @@ int ensure_partials(dsa_ctx *h, int nsplit)
     return DSA_OK;
 }
 
-void forget_handle(const dsa_ctx *h);
-
 void free_ctx(dsa_ctx *h)
 {
     if (!h) return;
@@ -451,18 +451,21 @@ cudaError_t launch_step(int dtype, int D, int shape, const dsa::DecodeParams &p,
     return D == 64 ? launch_merge<float, 64>(p, st) : launch_merge<float, 128>(p, st);
 }
 
-// The last handle this library launched a kernel for, per stream: a decode
-// step may read its state before the grid dependency wait only when the
-// kernel just before it in the stream was not one of this handle's own.
+// The last handle (of any kind) this library launched a kernel for, per
+// stream: a decode step may read its state before the grid dependency wait
+// only when the kernel just before it in the stream was not one of this
+// handle's own.
 std::mutex g_last_mu;
 struct LastLaunch {
     cudaStream_t stream;
-    const dsa_ctx *handle;
+    const void *handle;
 };
 LastLaunch g_last[16];
 int g_last_next;
 
-bool note_launch(cudaStream_t st, const dsa_ctx *h)
+}  // namespace
+
+bool dsa_detail::note_launch(cudaStream_t st, const void *h)
 {
     std::lock_guard<std::mutex> lock(g_last_mu);
     for (auto &e : g_last)
@@ -476,12 +479,14 @@ bool note_launch(cudaStream_t st, const dsa_ctx *h)
     return false;  // unknown stream: be conservative
 }
 
-void forget_handle(const dsa_ctx *h)
+void dsa_detail::forget_handle(const void *h)
 {
     std::lock_guard<std::mutex> lock(g_last_mu);
     for (auto &e : g_last)
-        if (e.handle == h) e.handle = reinterpret_cast<const dsa_ctx *>(&g_last_mu);  // a value no handle has
+        if (e.handle == h) e.handle = &g_last_mu;  // a value no handle has
 }
+
+namespace {
 
 template <typename T, int D>
 cudaError_t launch_prefill(const void *K, const void *V, void *prefix, const float *kinv, const float *vinv, int S,

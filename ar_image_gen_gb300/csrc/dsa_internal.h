@@ -16,6 +16,13 @@ __attribute__((visibility("hidden"))) int fail(int code, const char *fmt, ...);
 __attribute__((visibility("hidden"))) int cuda_fail(cudaError_t e, const char *what);
 __attribute__((visibility("hidden"))) int dev_alloc(void **p, size_t bytes, const char *what);
 
+// Records that `handle` (a decode or policy handle) launches a kernel on
+// stream `st` next; true if the library's previous launch on `st` was for
+// another handle (false for a stream not seen before).  forget_handle drops
+// a destroyed handle from the record.
+__attribute__((visibility("hidden"))) bool note_launch(cudaStream_t st, const void *handle);
+__attribute__((visibility("hidden"))) void forget_handle(const void *handle);
+
 // The QKV projection (dsa_proj.cu) as the fused decode step uses it.
 __attribute__((visibility("hidden"))) int proj_shape(const dsa_proj_ctx *p, int *batch, int *heads, int *head_dim);
 __attribute__((visibility("hidden"))) void proj_staging(const dsa_proj_ctx *p, void **q, void **k, void **v);

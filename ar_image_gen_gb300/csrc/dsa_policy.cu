@@ -10,10 +10,11 @@
 // t the attended decode entries are the occupied slots other than the
 // current token's slot (one or two contiguous runs) plus the current token.
 //
-// policy_kernel: a persistent grid whose warps take whole streams.  A warp
-// streams the stream's prompt rows and slot runs through its own shared-
-// memory stages (bulk copies, NBUF in flight, continuing into the next
-// stream), computes the logits with 8 lanes per row and an online softmax
+// policy_kernel: a persistent grid whose warps take whole streams (striped
+// over the CTAs, so that every CTA gets as many streams as the others give
+// or take one).  A warp streams the stream's prompt rows and slot runs
+// through its own shared-memory stages (bulk copies, nbuf in flight,
+// continuing into the next stream), computes the logits with 8 lanes per row and an online softmax
 // with P.V, holds the current token in registers (and stores it to its
 // slot), combines its row groups with shuffles, writes the output and
 // applies the eviction: TOVA's argmin of (logit, position) is tracked in the
@@ -39,10 +40,11 @@ namespace dsa_pol_k {
 using namespace dsa;
 
 constexpr int kWarps = 4;
-constexpr int kNbuf = 2;
-// Stage sizes: 8 KB (three CTAs, 12 warps per SM) or 6 KB (four CTAs, 16
-// warps per SM), picked per handle so that the streams take as few rounds
-// of warps as possible.
+constexpr int kMaxNbuf = 4;
+// Stage sizes 8 KB or 6 KB, and 2 to 4 stages per warp: the host picks per
+// handle the pair whose resident warps take the streams in the fewest
+// rounds, and among those the deepest pipeline per warp (with fewer streams
+// than warp slots, the idle warps' shared memory goes to the busy ones).
 constexpr int kStages[2] = {8192, 6144};
 constexpr uint32_t kNoWaitLimit = 0xffffffffu;
 
@@ -63,6 +65,9 @@ struct PolParams {
     float qscale;        // log2(e) / sqrt(D)
     uint32_t wait_limit;
     int warp_smem;       // bytes of shared memory per warp
+    int nbuf;            // stages per warp (2 .. kMaxNbuf)
+    int early;           // 1: the previous grid in the stream is not one of this handle's, so
+                         // the handle's own state may be read before the grid dependency wait
 };
 
 template <typename T, int D, int STAGE>
@@ -112,11 +117,12 @@ __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
     using Vec = typename EL::Vec;
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nbuf = p.nbuf;
     unsigned char *ws = smem + warp * p.warp_smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ws + kNbuf * kStage);
-    float *xs = reinterpret_cast<float *>(ws + kNbuf * kStage + 16);  // H2O: decode logits of the stream
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ws + nbuf * kStage);
+    float *xs = reinterpret_cast<float *>(ws + nbuf * kStage + 8 * kMaxNbuf);  // decode logits of the stream
     if (lane == 0) {
-        for (int b = 0; b < kNbuf; ++b) mbar_init(smem_u32(&bars[b]), 1);
+        for (int b = 0; b < nbuf; ++b) mbar_init(smem_u32(&bars[b]), 1);
         fence_barrier_init();
     }
     __syncwarp();
@@ -125,14 +131,11 @@ __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
     const int g = lane / C::LPR, cl = lane % C::LPR;
     const uint64_t pol = policy_evict_first();
     const int GW = gridDim.x * kWarps;
-    const int first = blockIdx.x * kWarps + warp;
-
-    // Everything this kernel reads may have been written by the previous
-    // kernel in the stream (the previous step of this handle).
-    pdl_wait();
-    pdl_launch_dependents();
+    const int first = warp * gridDim.x + blockIdx.x;
 
     int issued = 0, consumed = 0;
+    int ib = 0;            // buffer of the next issued stage
+    int cb = 0, cpar = 0;  // buffer and phase parity of the next consumed stage
     bool aborted = false;
     // issuer cursor over (stream, stage) of this warp's streams
     int is = first, ij = 0;
@@ -145,7 +148,8 @@ __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
                 iset = true;
             }
             if (ij * C::SR < ir.n) {
-                const int b = issued % kNbuf;
+                const int b = ib;
+                ib = ib + 1 == nbuf ? 0 : ib + 1;
                 const uint32_t fb = bar0 + 8 * b;
                 const uint32_t dst = buf0 + b * kStage;
                 const int u0 = ij * C::SR, u1 = min(u0 + C::SR, ir.n);
@@ -179,9 +183,18 @@ __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
         return false;
     };
     auto top_up = [&]() {
-        while (issued - consumed < kNbuf && issue_one()) {
+        while (issued - consumed < nbuf && issue_one()) {
         }
     };
+    // Programmatic dependent launch.  The previous grid in the stream may have
+    // written q, k_new and v_new, and, if it was this handle's own step or
+    // prefill, the handle's state.  Otherwise that state is final here (the
+    // previous grid let this one start only after its own wait, which
+    // followed this handle's last kernel), so the first stages are issued
+    // before the wait; q, k_new, v_new and every write come after it.
+    if (p.early) top_up();
+    pdl_wait();
+    pdl_launch_dependents();
     top_up();
 
     for (int s = first; s < p.S && !aborted; s += GW) {
@@ -198,18 +211,21 @@ __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
         float acc[2 * C::VEC];
 #pragma unroll
         for (int e = 0; e < 2 * C::VEC; ++e) acc[e] = 0.f;
-        float m = -INFINITY, l = 0.f, minv = INFINITY;
-        int minpos = INT_MAX, minslot = -1;
+        float m = -INFINITY, l = 0.f;
 
         for (int j = 0; j < nst; ++j) {
-            const int b = consumed % kNbuf;
-            const bool ok = wait_phase(bar0 + 8 * b, (consumed / kNbuf) & 1, p.wait_limit);
+            const int b = cb;
+            const bool ok = wait_phase(bar0 + 8 * b, (uint32_t)cpar, p.wait_limit);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) atomicOr(p.status, ST_TIMEOUT);
                 aborted = true;
                 break;
             }
             ++consumed;
+            if (++cb == nbuf) {
+                cb = 0;
+                cpar ^= 1;
+            }
             const unsigned char *st = ws + b * kStage;
             const int u0 = j * C::SR;
             const int nv = min(C::SR, rw.n - u0);
@@ -230,19 +246,7 @@ __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
                 x *= p.qscale;
                 sc[it] = valid ? x : -INFINITY;
                 const int k = u0 + row - p.L_p;  // decode rank of the row (< 0: prompt)
-                if (valid && k >= 0) {
-                    if (POL == DSA_POLICY_H2O) {
-                        if (cl == 0) xs[k] = x;
-                    } else if (p.full) {
-                        const int slot = k < rw.nA ? k : k + 1;
-                        const int pos = __ldg(spos + slot);
-                        if (lower(x, pos, minv, minpos)) {
-                            minv = x;
-                            minpos = pos;
-                            minslot = slot;
-                        }
-                    }
-                }
+                if (valid && k >= 0 && cl == 0) xs[k] = x;  // for the eviction, after the pass
             }
             float mx = sc[0];
 #pragma unroll
@@ -283,11 +287,6 @@ __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
             for (int o = C::LPR / 2; o >= 1; o >>= 1) xc += __shfl_xor_sync(0xffffffffu, xc, o);
             xc *= p.qscale;
         }
-        if (POL != DSA_POLICY_H2O && p.full && lower(xc, p.t, minv, minpos)) {
-            minv = xc;
-            minpos = p.t;
-            minslot = rw.fs;
-        }
         if (xc > m) {
             const float alpha = ex2(m - xc);
             l *= alpha;
@@ -312,14 +311,6 @@ __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
             l += __shfl_xor_sync(0xffffffffu, l, o);
 #pragma unroll
             for (int e = 0; e < 2 * C::VEC; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
-            const float ov = __shfl_xor_sync(0xffffffffu, minv, o);
-            const int op = __shfl_xor_sync(0xffffffffu, minpos, o);
-            const int osl = __shfl_xor_sync(0xffffffffu, minslot, o);
-            if (lower(ov, op, minv, minpos)) {
-                minv = ov;
-                minpos = op;
-                minslot = osl;
-            }
         }
         if (g == 0) {
             const float inv = 1.f / l;
@@ -327,19 +318,25 @@ __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
             o[cl] = EL::pack(acc, inv);
             o[cl + C::LPR] = EL::pack(acc + C::VEC, inv);
         }
-        if (POL == DSA_POLICY_H2O) {
-            // accumulated weights: every attended decode entry adds its
-            // normalised weight; the candidate with the lowest total (outside
-            // the recent window) is evicted
+        // The eviction.  TOVA: the lowest logit among the attended decode
+        // entries and the current token.  H2O: every attended decode entry
+        // adds its normalised weight to its slot's total; the lowest total
+        // outside the recent window goes.  Ties go to the older position.
+        float minv = INFINITY;
+        int minpos = INT_MAX, minslot = -1;
+        if (POL == DSA_POLICY_H2O || p.full) {
             __syncwarp();
             float *accw = p.acc + (size_t)s * p.R;
             const float inv = 1.f / l;
             const int nold = rw.nA + rw.nB;
-            const int oldest_recent = p.t - p.n_recent + 1;  // positions >= this are kept
+            const int oldest_recent = POL == DSA_POLICY_H2O ? p.t - p.n_recent + 1 : INT_MAX;  // positions >= this are kept
             for (int k = lane; k < nold; k += 32) {
                 const int slot = k < rw.nA ? k : k + 1;
-                const float a = __ldcg(accw + slot) + ex2(xs[k] - m) * inv;
-                accw[slot] = a;
+                float a = xs[k];
+                if (POL == DSA_POLICY_H2O) {
+                    a = __ldcg(accw + slot) + ex2(a - m) * inv;
+                    accw[slot] = a;
+                }
                 const int pos = __ldg(spos + slot);
                 if (p.full && pos < oldest_recent && lower(a, pos, minv, minpos)) {
                     minv = a;
@@ -347,9 +344,10 @@ __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
                     minslot = slot;
                 }
             }
-            const float ac = ex2(xc - m) * inv;
+            float ac = xc;
+            if (POL == DSA_POLICY_H2O) ac = ex2(xc - m) * inv;
             if (lane == 0) {
-                accw[rw.fs] = ac;
+                if (POL == DSA_POLICY_H2O) accw[rw.fs] = ac;
                 if (p.full && p.t < oldest_recent && lower(ac, p.t, minv, minpos)) {
                     minv = ac;
                     minpos = p.t;
@@ -385,7 +383,7 @@ __global__ void __launch_bounds__(32 * kWarps) policy_kernel(const PolParams p)
     }
     // A warp that gave up lets its own copies in flight land before exit.
     if (aborted && lane == 0) {
-        for (int q = consumed; q < issued; ++q) drain_phase(bar0 + 8 * (q % kNbuf), (q / kNbuf) & 1);
+        for (int q = consumed; q < issued; ++q) drain_phase(bar0 + 8 * (q % nbuf), (q / nbuf) & 1);
     }
     __syncwarp();
 }
@@ -412,7 +410,7 @@ struct dsa_pol_ctx {
     uint32_t magic;
     int S, D, L_p, R, policy, dtype;
     int t, prefilled, evicted_last;
-    int sms, grid, warp_smem, smem, shape;
+    int sms, grid, warp_smem, smem, shape, nbuf;
     uint32_t wait_limit;
     void *prefix, *slots;
     int32_t *slot_pos, *free_slot, *last_evict;
@@ -435,6 +433,7 @@ void free_pol(dsa_pol_ctx *h)
     cudaFree(h->acc);
     cudaFree(h->status);
     h->magic = 0;
+    dsa_detail::forget_handle(h);
     delete h;
 }
 
@@ -469,6 +468,62 @@ cudaError_t pol_occupancy_any(int dtype, int D, int policy, int shape, int smem,
                        : pol_occupancy_d<__nv_bfloat16, 128>(policy, shape, smem, ctas);
     return D == 64 ? pol_occupancy_d<float, 64>(policy, shape, smem, ctas)
                    : pol_occupancy_d<float, 128>(policy, shape, smem, ctas);
+}
+
+// Shared memory per warp for `nbuf` stages of stage size sh.
+int warp_bytes(const dsa_pol_ctx *h, int sh, int nbuf)
+{
+    return (nbuf * dsa_pol_k::kStages[sh] + 8 * dsa_pol_k::kMaxNbuf + 4 * h->R + 127) / 128 * 128;
+}
+
+// Resident CTAs per SM of the launch shape (stage size sh, nbuf stages per
+// warp); 0 if it cannot launch.
+int shape_ctas(const dsa_pol_ctx *h, int sh, int nbuf)
+{
+    int ctas = 0;
+    const cudaError_t e = pol_occupancy_any(h->dtype, h->D, h->policy, sh, dsa_pol_k::kWarps * warp_bytes(h, sh, nbuf), &ctas);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return ctas;
+}
+
+void apply_shape(dsa_pol_ctx *h, int sh, int nbuf, int ctas)
+{
+    h->shape = sh;
+    h->nbuf = nbuf;
+    h->warp_smem = warp_bytes(h, sh, nbuf);
+    h->smem = dsa_pol_k::kWarps * h->warp_smem;
+    const long long cap = (long long)h->sms * ctas;
+    h->grid = (int)(h->S < cap ? h->S : cap);  // streams are striped over the CTAs: none is left empty
+}
+
+// The automatic launch shape: the fewest rounds of resident warps over the
+// streams, then the most stage bytes per warp, then 8 KB stages.  Returns
+// false if no shape can launch.
+bool auto_shape(dsa_pol_ctx *h)
+{
+    long long best_rounds = LLONG_MAX;
+    int best_depth = 0, best_sh = -1, best_nb = 0, best_ctas = 0;
+    for (int sh = 0; sh < 2; ++sh)
+        for (int nb = 2; nb <= dsa_pol_k::kMaxNbuf; ++nb) {
+            const int ctas = shape_ctas(h, sh, nb);
+            if (ctas < 1) continue;
+            const long long warps = (long long)h->sms * ctas * dsa_pol_k::kWarps;
+            const long long rounds = (h->S + warps - 1) / warps;
+            const int depth = nb * dsa_pol_k::kStages[sh];
+            if (rounds < best_rounds || (rounds == best_rounds && depth > best_depth)) {
+                best_rounds = rounds;
+                best_depth = depth;
+                best_sh = sh;
+                best_nb = nb;
+                best_ctas = ctas;
+            }
+        }
+    if (best_sh < 0) return false;
+    apply_shape(h, best_sh, best_nb, best_ctas);
+    return true;
 }
 
 template <typename T, int D, int POL, int STAGE>
@@ -556,31 +611,7 @@ int dsa_pol_create(int heads, int head_dim, int L_p, int N_att, int policy, int 
         free_pol(h);
         return cuda_fail(e, "device query");
     }
-    // Per stage shape: shared memory, resident CTAs, and the rounds of warps
-    // the streams take; the shape with fewer rounds wins (8 KB on a tie).
-    long long best_rounds = LLONG_MAX;
-    for (int sh = 0; sh < 2; ++sh) {
-        const int ws = (dsa_pol_k::kNbuf * dsa_pol_k::kStages[sh] + 16 + (policy == DSA_POLICY_H2O ? 4 * N_att : 0) + 127) /
-                       128 * 128;
-        int ctas = 0;
-        e = pol_occupancy_any(dtype, head_dim, policy, sh, dsa_pol_k::kWarps * ws, &ctas);
-        if (e != cudaSuccess || ctas < 1) {
-            cudaGetLastError();
-            continue;
-        }
-        const long long warps = (long long)h->sms * ctas * dsa_pol_k::kWarps;
-        const long long rounds = (heads + warps - 1) / warps;
-        if (rounds < best_rounds) {
-            best_rounds = rounds;
-            h->shape = sh;
-            h->warp_smem = ws;
-            h->smem = dsa_pol_k::kWarps * ws;
-            const long long want = (heads + dsa_pol_k::kWarps - 1) / dsa_pol_k::kWarps;
-            const long long cap = (long long)h->sms * ctas;
-            h->grid = (int)(want < cap ? want : cap);
-        }
-    }
-    if (best_rounds == LLONG_MAX) {
+    if (!auto_shape(h)) {
         free_pol(h);
         return fail(DSA_ERR_CUDA, "policy kernel setup failed (is this an sm_103 device, and N_att within shared memory?)");
     }
@@ -635,6 +666,7 @@ int dsa_pol_prefill(dsa_pol h, const void *K, const void *V, void *stream)
         e = h->D == 64 ? pol_prefill<float, 64>(K, V, h->prefix, h->S, h->L_p, st)
                        : pol_prefill<float, 128>(K, V, h->prefix, h->S, h->L_p, st);
     if (e != cudaSuccess) return cuda_fail(e, "policy prefill launch");
+    dsa_detail::note_launch(st, h);  // the next step waits for the prefill before reading the state
     h->t = 0;
     h->prefilled = 1;
     h->evicted_last = 0;
@@ -671,7 +703,9 @@ int dsa_pol_decode_step(dsa_pol h, const void *q, const void *k_new, const void 
     p.qscale = (float)(1.4426950408889634 / std::sqrt((double)h->D));
     p.wait_limit = h->wait_limit;
     p.warp_smem = h->warp_smem;
+    p.nbuf = h->nbuf;
     cudaStream_t st = (cudaStream_t)stream;
+    p.early = dsa_detail::note_launch(st, h) ? 1 : 0;
     cudaError_t e;
     if (h->dtype == DSA_BF16)
         e = h->D == 64 ? pol_launch_d<__nv_bfloat16, 64>(h->policy, h->shape, p, h->grid, h->smem, st)
@@ -717,23 +751,17 @@ int dsa_pol_sync_status(dsa_pol h, void *stream)
 int dsa_pol_set_shape(dsa_pol h, int shape)
 {
     if (!valid(h)) return fail(DSA_ERR_STATE, "invalid policy handle");
-    if (shape < 0 || shape > 2) return fail(DSA_ERR_ARG, "shape must be 0 (automatic), 1 or 2 (got %d)", shape);
-    if (shape == 0) return DSA_OK;  // keep the choice made at creation
-    const int sh = shape - 1;
-    const int ws = (dsa_pol_k::kNbuf * dsa_pol_k::kStages[sh] + 16 + (h->policy == DSA_POLICY_H2O ? 4 * h->R : 0) + 127) /
-                   128 * 128;
-    int ctas = 0;
-    cudaError_t e = pol_occupancy_any(h->dtype, h->D, h->policy, sh, dsa_pol_k::kWarps * ws, &ctas);
-    if (e != cudaSuccess || ctas < 1) {
-        cudaGetLastError();
-        return fail(DSA_ERR_ARG, "stage shape %d cannot be launched for this handle", shape);
+    const int nshapes = 2 * (dsa_pol_k::kMaxNbuf - 1);
+    if (shape < 0 || shape > nshapes)
+        return fail(DSA_ERR_ARG, "shape must be 0 (automatic) or 1 .. %d (got %d)", nshapes, shape);
+    if (shape == 0) {
+        if (!auto_shape(h)) return fail(DSA_ERR_CUDA, "no launch shape for this handle");
+        return DSA_OK;
     }
-    h->shape = sh;
-    h->warp_smem = ws;
-    h->smem = dsa_pol_k::kWarps * ws;
-    const long long want = (h->S + dsa_pol_k::kWarps - 1) / dsa_pol_k::kWarps;
-    const long long cap = (long long)h->sms * ctas;
-    h->grid = (int)(want < cap ? want : cap);
+    const int sh = (shape - 1) % 2, nb = 2 + (shape - 1) / 2;
+    const int ctas = shape_ctas(h, sh, nb);
+    if (ctas < 1) return fail(DSA_ERR_ARG, "launch shape %d cannot be launched for this handle", shape);
+    apply_shape(h, sh, nb, ctas);
     return DSA_OK;
 }
 

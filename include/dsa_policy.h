@@ -86,10 +86,12 @@ int dsa_pol_sync_status(dsa_pol h, void *stream);
 /* Test knob: polls per bounded wait before giving up (0: at once). */
 int dsa_pol_set_wait_limit(dsa_pol h, uint32_t limit);
 
-/* Test knob: force the stage shape (1: 8 KB stages, 12 warps per SM; 2: 6 KB
- * stages, 16 warps per SM; 0: keep the automatic choice, which takes the
- * shape that runs the streams in fewer rounds of warps).  Results do not
- * depend on it. */
+/* Test knob: force the launch shape, stage size and stages per warp
+ * (1: 8 KB x 2, 2: 6 KB x 2, 3: 8 KB x 3, 4: 6 KB x 3, 5: 8 KB x 4, 6: 6 KB
+ * x 4), or 0 for the automatic choice: the shape whose resident warps take
+ * the streams in the fewest rounds, and among those the deepest pipeline
+ * per warp.  DSA_ERR_ARG if the shape cannot launch for this handle.
+ * Results do not depend on it. */
 int dsa_pol_set_shape(dsa_pol h, int shape);
 
 #ifdef __cplusplus

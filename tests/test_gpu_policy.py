@@ -112,7 +112,8 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("shape", [1, 2])
+# launch shapes: 1 / 2 = 8 KB / 6 KB stages, two per warp; 3 = 8 KB x 3; 6 = 6 KB x 4
+@pytest.mark.parametrize("shape", [1, 2, 3, 6])
 @pytest.mark.parametrize("name", list(CASES))
 def test_policy_parity(name, shape):
     wl, policy, steps = CASES[name]
@@ -160,3 +161,45 @@ def test_policy_full_size_lumina_b32(policy):
     rep = run_policy(wl, policy, 260, sample=list(range(0, 1024, 131)), check_every=26)
     assert rep.ok, (rep.failures[:5], rep.max_err)
     assert rep.evictions > 0
+
+
+@pytest.mark.parametrize("policy", ["tova", "h2o"])
+def test_policy_interleaved_handles_on_one_stream(policy):
+    """Three handles (layers) stepped round-robin on one stream, so that
+    every launch after the first follows another handle's and issues its
+    first stages before the grid dependency wait; each is compared bit for
+    bit (outputs, evictions, cache positions) with a twin stepped on a
+    stream of its own, whose launches always follow its own."""
+    from ar_image_gen_gb300.dsa import DSA_OK, Policy
+
+    wl = small("inter", 16, 9, heads=8, batch=8)
+    d, S = wl.head_dim, wl.streams
+    gens = [TraceGen(wl, layer=l, device="cuda") for l in range(3)]
+    A = [Policy(S, d, wl.L_p, wl.N_att, policy, wl.dtype) for _ in range(3)]
+    B = [Policy(S, d, wl.L_p, wl.N_att, policy, wl.dtype) for _ in range(3)]
+    own = [torch.cuda.Stream() for _ in range(3)]
+    main = torch.cuda.current_stream()
+    for l in range(3):
+        Kp, Vp = gens[l].prompt()
+        A[l].prefill(Kp, Vp)
+        B[l].prefill(Kp, Vp)
+    torch.cuda.synchronize()
+    outA = [torch.empty((S, d), dtype=torch.bfloat16, device="cuda") for _ in range(3)]
+    outB = [torch.empty_like(outA[0]) for _ in range(3)]
+    for t in range(40):
+        qkv = [gens[l].step(t) for l in range(3)]
+        torch.cuda.synchronize()
+        for l in range(3):
+            A[l].decode_step(*qkv[l], outA[l], main)
+        for l in range(3):
+            with torch.cuda.stream(own[l]):
+                B[l].decode_step(*qkv[l], outB[l], own[l])
+        torch.cuda.synchronize()
+        for l in range(3):
+            assert torch.equal(outA[l], outB[l]), (t, l)
+            assert np.array_equal(A[l].last_eviction(), B[l].last_eviction()), (t, l)
+    for l in range(3):
+        assert np.array_equal(A[l].positions(), B[l].positions())
+        assert A[l].sync_status() == DSA_OK and B[l].sync_status() == DSA_OK
+        A[l].close()
+        B[l].close()
