@@ -109,9 +109,9 @@ struct dsa_ctx {
     int prefilled;
     int last_select;
     int device, sm_count;
-    int ctas_per_sm[dsa::kPipes];  // resident CTAs per SM of each pipeline shape (0: unavailable)
+    int ctas_per_sm[dsa::kPipelines];  // resident CTAs per SM of each launch pipeline (0: unavailable)
     int forced_split;
-    int forced_pipe;  // 0: automatic, else pipeline shape + 1
+    int forced_pipe;  // 0: automatic, else launch pipeline + 1
     int pstride;
     uint32_t wait_limit;
     void *prefix, *ring;
@@ -147,12 +147,13 @@ int validate(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int
 }
 
 struct Plan {
-    int phase, tin, P, a, wlen, select, sinkmode, n, nsplit, chunk, nitems, grid, shape;
+    int phase, tin, P, a, wlen, select, sinkmode, n, nsplit, chunk, nitems, grid;
+    int pipe, shape, nbuf;  // launch pipeline: stage shape pipe & 1, 2 + (pipe >> 1) stages per warp
     long long rounds, stages;
     unsigned long long bytes;
 };
 
-long long resident_warps(const dsa_ctx *h, int sh) { return (long long)h->sm_count * h->ctas_per_sm[sh] * kWarpsPerCta; }
+long long resident_warps(const dsa_ctx *h, int pi) { return (long long)h->sm_count * h->ctas_per_sm[pi] * kWarpsPerCta; }
 
 // Work items per stream under pipeline shape sh.  Splitting a stream costs a
 // partial write and a merge; it pays when the streams alone leave most warps
@@ -161,43 +162,47 @@ long long resident_warps(const dsa_ctx *h, int sh) { return (long long)h->sm_cou
 // streams pieces (one round of items) once they fill at most half the warps,
 // with at least two stages of rows per piece; streams longer than an item's
 // row limit always split.
-int auto_splits(const dsa_ctx *h, int n, int sh)
+int auto_splits(const dsa_ctx *h, int n, int pi)
 {
+    const int sh = pi & 1;
     const int rows = stage_rows(h->dtype, h->D, sh);
     const int cap = chunk_cap(h->dtype, h->D, sh);
     const int need = (n + cap - 1) / cap;
-    const long long warps = resident_warps(h, sh);
+    const long long warps = resident_warps(h, pi);
     const int want = 2LL * h->S <= warps ? (int)(warps / h->S) : 1;
     const int by_rows = n / (2 * rows) > 1 ? n / (2 * rows) : 1;
     const int ns = want < by_rows ? want : by_rows;
     return ns > need ? ns : need;
 }
 
-// Items, grid and cost of pipeline shape sh for a step of n rows per stream.
-void shape_plan(const dsa_ctx *h, int sh, Plan &p)
+// Items, grid and cost of launch pipeline pi for a step of n rows per stream.
+void shape_plan(const dsa_ctx *h, int pi, Plan &p)
 {
+    const int sh = pi & 1;
     const int rows = stage_rows(h->dtype, h->D, sh);
     const int cap = chunk_cap(h->dtype, h->D, sh);
-    int ns = h->forced_split > 0 ? h->forced_split : auto_splits(h, p.n, sh);
+    int ns = h->forced_split > 0 ? h->forced_split : auto_splits(h, p.n, pi);
     const int need = (p.n + cap - 1) / cap;
     if (ns < need) ns = need;
     if (ns > p.n) ns = p.n;
     int chunk = (p.n + ns - 1) / ns;
     chunk = (chunk + rows - 1) / rows * rows;
     if (chunk > cap) chunk = cap;
+    p.pipe = pi;
     p.shape = sh;
+    p.nbuf = 2 + (pi >> 1);
     p.chunk = chunk;
     p.nsplit = (p.n + chunk - 1) / chunk;
     p.nitems = p.nsplit * h->S;
     // Give every warp the same number of items: with k = ceil(items / resident
     // warps) rounds of items, use just enough warps for k items each, so no
     // warp runs a round that most others do not.
-    const long long max_warps = resident_warps(h, sh);
+    const long long max_warps = resident_warps(h, pi);
     p.rounds = (p.nitems + max_warps - 1) / max_warps;
     const long long warps = (p.nitems + p.rounds - 1) / p.rounds;
     p.grid = (int)((warps + kWarpsPerCta - 1) / kWarpsPerCta);
     // A warp's run time is its rounds times the stages of one item, each
-    // stage about one copy latency over the NBUF stages in flight.
+    // stage about one copy latency over the two stages in flight.
     const int item_rows = chunk < p.n ? chunk : p.n;
     p.stages = p.rounds * ((item_rows + rows - 1) / rows);
 }
@@ -262,6 +267,26 @@ Plan make_plan(const dsa_ctx *h, int t)
             Plan q = p;
             shape_plan(h, 1, q);
             if (launch_cost(q, h->dtype) < launch_cost(p, h->dtype)) p = q;
+        }
+        // A third stage per warp (two CTAs per SM, 8 warps) pays where the
+        // two-stage plan splits streams to fill one round of warps and three
+        // stages let every stream stay one work item in one round: no split
+        // partials, no merge launch (janus-b32 13.4 -> 11.6 us, lumina-s95-b32
+        // 29.7 -> 27.3 us on GB300).  Where it costs rounds it loses (two-round
+        // launches gained nothing or lost up to 4 %), and with FP8 rows, whose
+        // warps are bound by their own arithmetic, it always loses.
+        if (h->dtype != DSA_FP8_E4M3 && p.nsplit > 1 && p.rounds == 1 && h->forced_split == 0) {
+            Plan best{};
+            bool have = false;
+            for (int pi = 2; pi < dsa::kPipelines; ++pi) {
+                if (h->ctas_per_sm[pi] < 1) continue;
+                Plan q = p;
+                shape_plan(h, pi, q);
+                if (q.nsplit != 1 || q.rounds > p.rounds) continue;
+                if (!have || launch_cost(q, h->dtype) < launch_cost(best, h->dtype)) best = q;
+                have = true;
+            }
+            if (have) p = best;
         }
     }
     return p;
@@ -351,39 +376,46 @@ int encode_ring_map(dsa_ctx *h)
 }
 
 template <typename T, int D, int SH>
-int occupancy()
+int occupancy(int nbuf)
 {
     using C = dsa::KCfg<T, D, SH>;
-    static int cached = -1;
-    if (cached < 0) {
-        cudaError_t e =
-            cudaFuncSetAttribute(dsa::decode_kernel<T, D, SH>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    static int cached[dsa::kMaxNbuf + 1] = {-1, -1, -1, -1};
+    static_assert(dsa::kMaxNbuf == 3, "one cache entry per stage count");
+    if (cached[nbuf] < 0) {
+        // The attribute allows the largest layout, so every stage count launches.
+        cudaError_t e = cudaFuncSetAttribute(dsa::decode_kernel<T, D, SH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::smem(dsa::kMaxNbuf));
         if (e != cudaSuccess) return -1;
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dsa::decode_kernel<T, D, SH>, C::THREADS, C::SMEM);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dsa::decode_kernel<T, D, SH>, C::THREADS, C::smem(nbuf));
         if (e != cudaSuccess) return -1;
-        cached = n;
+        cached[nbuf] = n;
     }
-    return cached;
+    return cached[nbuf];
 }
 
 template <int SH>
-int occupancy_sh(int dtype, int D)
+int occupancy_sh(int dtype, int D, int nbuf)
 {
-    if (dtype == DSA_BF16) return D == 64 ? occupancy<__nv_bfloat16, 64, SH>() : occupancy<__nv_bfloat16, 128, SH>();
-    if (dtype == DSA_FP8_E4M3) return D == 64 ? occupancy<__nv_fp8_e4m3, 64, SH>() : occupancy<__nv_fp8_e4m3, 128, SH>();
-    return D == 64 ? occupancy<float, 64, SH>() : occupancy<float, 128, SH>();
+    if (dtype == DSA_BF16)
+        return D == 64 ? occupancy<__nv_bfloat16, 64, SH>(nbuf) : occupancy<__nv_bfloat16, 128, SH>(nbuf);
+    if (dtype == DSA_FP8_E4M3)
+        return D == 64 ? occupancy<__nv_fp8_e4m3, 64, SH>(nbuf) : occupancy<__nv_fp8_e4m3, 128, SH>(nbuf);
+    return D == 64 ? occupancy<float, 64, SH>(nbuf) : occupancy<float, 128, SH>(nbuf);
 }
 
-// Resident CTAs per SM of both pipeline shapes; shape 0 must be launchable.
+// Resident CTAs per SM of every launch pipeline (0: cannot launch); the
+// first (shape 0, two stages per warp) must be launchable.
 int query_occupancy(int dtype, int D, int *ctas)
 {
-    ctas[0] = occupancy_sh<0>(dtype, D);
-    if (ctas[0] < 1) return cuda_fail(cudaGetLastError(), "kernel occupancy query (is this an sm_103 device?)");
-    ctas[1] = occupancy_sh<1>(dtype, D);
-    if (ctas[1] < 1) {
-        ctas[1] = 0;
-        cudaGetLastError();
+    for (int pi = 0; pi < dsa::kPipelines; ++pi) {
+        const int nbuf = 2 + (pi >> 1);
+        ctas[pi] = (pi & 1) ? occupancy_sh<1>(dtype, D, nbuf) : occupancy_sh<0>(dtype, D, nbuf);
+        if (ctas[pi] < 1) {
+            if (pi == 0) return cuda_fail(cudaGetLastError(), "kernel occupancy query (is this an sm_103 device?)");
+            ctas[pi] = 0;
+            cudaGetLastError();
+        }
     }
     return DSA_OK;
 }
@@ -398,7 +430,7 @@ cudaError_t launch_decode(const dsa::DecodeParams &p, const CUtensorMap &map, in
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.dynamicSmemBytes = C::smem(p.nbuf);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -670,7 +702,7 @@ int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out)
     out->nsplit = p.nsplit;
     out->chunk = p.chunk;
     out->grid = p.grid;
-    out->pipeline = p.shape + 1;
+    out->pipeline = p.pipe + 1;
     out->algo_bytes = p.bytes;
     return DSA_OK;
 }
@@ -730,6 +762,7 @@ int launch_decode_step(dsa_handle h, const void *q, const void *k_new, const voi
     p.a = pl.a;
     p.n = pl.n;
     p.nsplit = pl.nsplit;
+    p.nbuf = pl.nbuf;
     p.chunk = pl.chunk;
     p.pstride = h->pstride;
     p.nitems = pl.nitems;
@@ -847,7 +880,8 @@ int dsa_set_splits(dsa_handle h, int nsplit)
 int dsa_set_pipeline(dsa_handle h, int pipeline)
 {
     if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
-    if (pipeline < 0 || pipeline > dsa::kPipes) return fail(DSA_ERR_ARG, "pipeline must be 0, 1 or 2 (got %d)", pipeline);
+    if (pipeline < 0 || pipeline > dsa::kPipelines)
+        return fail(DSA_ERR_ARG, "pipeline must be 0 .. %d (got %d)", dsa::kPipelines, pipeline);
     if (pipeline > 0 && h->ctas_per_sm[pipeline - 1] < 1)
         return fail(DSA_ERR_ARG, "pipeline %d cannot be launched on this device", pipeline);
     h->forced_pipe = pipeline;
@@ -1003,7 +1037,7 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     int sms = 0;
     rc = noalloc_setup(&scratch, &sms);
     if (rc != DSA_OK) return rc;
-    int occ[dsa::kPipes];
+    int occ[dsa::kPipelines];
     rc = query_occupancy(dtype, head_dim, occ);
     if (rc != DSA_OK) return rc;
 
@@ -1022,8 +1056,7 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     h.Lcap = L_p + sink;
     h.MW = (h.R + 31) / 32;
     h.sm_count = sms;
-    h.ctas_per_sm[0] = occ[0];
-    h.ctas_per_sm[1] = occ[1];
+    for (int pi = 0; pi < dsa::kPipelines; ++pi) h.ctas_per_sm[pi] = occ[pi];
     h.prefix = prefix;
     h.ring = ring;
     Plan pl = make_plan(&h, t);
@@ -1079,6 +1112,7 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.a = pl.a;
     p.n = pl.n;
     p.nsplit = pl.nsplit;
+    p.nbuf = pl.nbuf;
     p.chunk = pl.chunk;
     p.pstride = pl.nsplit;
     p.nitems = pl.nitems;

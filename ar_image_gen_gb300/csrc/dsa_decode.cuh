@@ -100,6 +100,7 @@ struct DecodeParams {
     int a;                // attended decode rows (host count)
     int n;                // P + a
     int nsplit;           // work items per stream
+    int nbuf;             // shared-memory stages per warp (2 .. kMaxNbuf)
     int chunk;            // rows per work item (multiple of the stage rows)
     int nitems;           // S * nsplit
     int pstride;          // partial slots per stream
@@ -337,11 +338,11 @@ struct Elem<__nv_fp8_e4m3> {
 #ifndef DSA_WARPS
 #define DSA_WARPS 4
 #endif
-#ifndef DSA_NBUF
-#define DSA_NBUF 2
-#endif
 
-constexpr int kPipes = 2;
+constexpr int kPipes = 2;      // stage shapes
+constexpr int kMaxNbuf = 3;    // stages per warp: 2 or 3, per launch (DecodeParams::nbuf)
+// Launch pipelines: shape pi & 1 with 2 + (pi >> 1) stages per warp.
+constexpr int kPipelines = kPipes * (kMaxNbuf - 1);
 
 template <int SH>
 struct Pipe;
@@ -369,13 +370,14 @@ struct KCfg {
     static constexpr int STAGE_BYTES = Pipe<SH>::STAGE_BYTES;
     static constexpr int SROWS = STAGE_BYTES / ROW;  // entries per stage
     static constexpr int NIT = SROWS / RPW;          // warp instructions per stage
-    static constexpr int NBUF = DSA_NBUF;            // stages per warp
     static constexpr int CHUNK_MAX = Pipe<SH>::CHUNK_MAX;  // decode ranks per work item
     static constexpr int MAXW = 8;                   // mask words per lane kept in registers
-    static constexpr int OFF_BAR = NBUF * STAGE_BYTES;
-    static constexpr int OFF_LIST = OFF_BAR + NBUF * 8;
-    static constexpr int WARP_SMEM = (OFF_LIST + 2 * CHUNK_MAX * 2 + 127) / 128 * 128;  // two item lists
-    static constexpr int SMEM = WARPS * WARP_SMEM;
+    // Shared memory of one warp with nbuf stages: the stages, their barriers
+    // (room for kMaxNbuf) and the two item lists; 128-byte aligned.
+    static constexpr __host__ __device__ int off_bar(int nbuf) { return nbuf * STAGE_BYTES; }
+    static constexpr __host__ __device__ int off_list(int nbuf) { return off_bar(nbuf) + kMaxNbuf * 8; }
+    static constexpr __host__ __device__ int warp_smem(int nbuf) { return (off_list(nbuf) + 2 * CHUNK_MAX * 2 + 127) / 128 * 128; }
+    static constexpr __host__ __device__ int smem(int nbuf) { return WARPS * warp_smem(nbuf); }
     static_assert(LPR >= 2 && LPR <= 16 && 32 % LPR == 0, "row must span a power-of-two lane group");
     static_assert(SROWS % RPW == 0 && NIT >= 1, "stage rows must fill whole warp instructions");
     static_assert(ROW % 128 == 0 || ROW == 256, "gather destinations must stay 128-byte aligned");
@@ -401,7 +403,7 @@ __device__ __forceinline__ bool better(float v, int r, float bv, int br)
 // scan over the stream's mask words, prefetched one item ahead), streams the
 // prompt rows (bulk copies) and the attended ring rows (TMA tile::gather4
 // through `tmap`, or contiguous bulk runs when nothing can be skipped)
-// through its own NBUF shared-memory stages (pipeline shape SH), reads q and the current token
+// through its own nbuf shared-memory stages (stage shape SH), reads q and the current token
 // straight into registers, and ends with a warp-shuffle combine.
 template <typename T, int D, int SH>
 __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const DecodeParams p,
@@ -414,11 +416,12 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    unsigned char *ws = smem + warp * C::WARP_SMEM;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ws + C::OFF_BAR);
-    uint16_t *list = reinterpret_cast<uint16_t *>(ws + C::OFF_LIST);
+    const int nbuf = p.nbuf;
+    unsigned char *ws = smem + warp * C::warp_smem(nbuf);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ws + C::off_bar(nbuf));
+    uint16_t *list = reinterpret_cast<uint16_t *>(ws + C::off_list(nbuf));
     if (lane == 0) {
-        for (int b = 0; b < C::NBUF; ++b) mbar_init(smem_u32(&bars[b]), 1);
+        for (int b = 0; b < nbuf; ++b) mbar_init(smem_u32(&bars[b]), 1);
         fence_barrier_init();
     }
     __syncwarp();
@@ -466,6 +469,8 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
 
     bool aborted = false;
     int issued = 0, consumed = 0;  // stages issued / consumed by this warp over all its items
+    int ib = 0;                    // buffer of the next issued stage
+    int cb = 0, cpar = 0;          // buffer and phase parity of the next consumed stage
 
     // ---- issuer: a cursor over the stages of this warp's items.  Each freed
     // buffer is refilled at once, with a stage of the next item once the
@@ -560,9 +565,10 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
         iss_ready = true;
     };
 
-    // a5: issue stage iss_j of the issuer's item into buffer issued % NBUF
+    // a5: issue stage iss_j of the issuer's item into buffer ib (= issued mod nbuf)
     auto issue_stage = [&]() {
-        const int b = issued % C::NBUF;
+        const int b = ib;
+        ib = ib + 1 == nbuf ? 0 : ib + 1;
         const uint32_t fb = bar0 + 8 * b;
         const uint32_t dst = buf0 + b * C::STAGE_BYTES;
         const int u0 = iss_j * C::SROWS;
@@ -635,9 +641,9 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
         }
     };
 
-    // Keeps NBUF stages of the warp's stream in flight (fewer at its end).
+    // Keeps nbuf stages of the warp's stream in flight (fewer at its end).
     auto top_up = [&](int con_seq) {
-        while (issued - consumed < C::NBUF) {
+        while (issued - consumed < nbuf) {
             const int before = issued;
             issue_next(con_seq);
             if (issued == before) return;
@@ -709,14 +715,18 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
         int minr = -1;
 
         for (int j = 0; j < nst; ++j) {
-            const int b = consumed % C::NBUF;
-            const bool ok = wait_phase(bar0 + 8 * b, (consumed / C::NBUF) & 1, p.wait_limit);
+            const int b = cb;
+            const bool ok = wait_phase(bar0 + 8 * b, (uint32_t)cpar, p.wait_limit);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) atomicOr(p.status, ST_TIMEOUT);
                 aborted = true;
                 break;
             }
             ++consumed;
+            if (++cb == nbuf) {
+                cb = 0;
+                cpar ^= 1;
+            }
             const unsigned char *st = ws + b * C::STAGE_BYTES;
             const int u0 = j * C::SROWS;
             const int nv = min(C::SROWS, nrows - u0);  // valid rows of the stage
@@ -851,7 +861,7 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
     }
     // A warp that gave up lets its own copies in flight land before exit.
     if (aborted && lane == 0) {
-        for (int q = consumed; q < issued; ++q) drain_phase(bar0 + 8 * (q % C::NBUF), (q / C::NBUF) & 1);
+        for (int q = consumed; q < issued; ++q) drain_phase(bar0 + 8 * (q % nbuf), (q / nbuf) & 1);
     }
     __syncwarp();
     if (p.step_dev) {

@@ -952,7 +952,7 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="time every workload family (one JSON line each)")
     ap.add_argument("--sweep-only", default="", help="comma-separated workloads for --sweep")
     ap.add_argument("--splits", type=int, default=0, help="--sweep: force this many work items per stream")
-    ap.add_argument("--pipeline", type=int, default=0, help="--sweep: force this pipeline shape (1 or 2)")
+    ap.add_argument("--pipeline", type=int, default=0, help="--sweep: force this launch pipeline (1 .. 4)")
     ap.add_argument("--trace", action="store_true", help="--sweep: also time whole traces (all phases, 3 runs)")
     ap.add_argument("--diag", action="store_true", help="attention diagnostics of each workload family's dense trace")
     ap.add_argument("--fused", action="store_true", help="fused layer step: QKV projection + decode, and the projection alone")

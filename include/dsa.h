@@ -180,7 +180,7 @@ typedef struct dsa_step_plan {
     int nsplit;                /* work items (pieces) per stream */
     int chunk;                 /* rows per work item */
     int grid;                  /* CTAs of the decode launch */
-    int pipeline;              /* pipeline shape of the launch (1 or 2, see dsa_set_pipeline) */
+    int pipeline;              /* launch pipeline (1 .. 4, see dsa_set_pipeline) */
     unsigned long long algo_bytes;
 } dsa_step_plan;
 
@@ -244,12 +244,13 @@ int dsa_set_kv_scales(dsa_handle h, const float *k_scale, const float *v_scale);
  * the decode path). */
 int dsa_set_splits(dsa_handle h, int nsplit);
 
-/* Force the pipeline shape of the decode kernel, or 0 for the automatic
- * choice per step.  1: 8 KB shared-memory stages per warp and at most 512
- * decode rows per work item; 2: 6 KB stages, at most 256 rows per item and
- * a third more resident warps.  Results do not depend on the shape beyond
- * fp32 rounding order (selections are identical).  DSA_ERR_ARG for other
- * values or a shape the device cannot launch. */
+/* Force the launch pipeline of the decode kernel, or 0 for the automatic
+ * choice per step.  1: two 8 KB shared-memory stages per warp and at most
+ * 512 decode rows per work item (12 warps per SM); 2: two 6 KB stages, at
+ * most 256 rows per item (16 warps per SM); 3 and 4: the stages of 1 and 2,
+ * three per warp (8 warps per SM).  Results do not depend on the pipeline
+ * beyond fp32 rounding order (selections are identical).  DSA_ERR_ARG for
+ * other values or a pipeline the device cannot launch. */
 int dsa_set_pipeline(dsa_handle h, int pipeline);
 
 /* Copy the stored KV state to host memory (synchronizes the device): the

@@ -110,9 +110,9 @@ def test_prefill_clears_a_sticky_status(dsa):
 def test_pipeline_knob_rejects_unknown_shapes(dsa):
     code, h = dsa.dsa_create(4, 128, 8, 16, 4, 0)
     assert code == dsa.DSA_OK
-    for bad in (-1, 3):
+    for bad in (-1, 5):
         assert dsa.dsa_set_pipeline(h, bad) == dsa.DSA_ERR_ARG
         assert "pipeline" in dsa.dsa_last_error()
-    for ok in (1, 2, 0):
+    for ok in (1, 2, 3, 4, 0):
         assert dsa.dsa_set_pipeline(h, ok) == dsa.DSA_OK
     assert dsa.dsa_destroy(h) == dsa.DSA_OK

@@ -44,7 +44,7 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("pipeline", [1, 2])
+@pytest.mark.parametrize("pipeline", [1, 2, 4])
 @pytest.mark.parametrize("name", list(CASES))
 def test_small_parity(name, pipeline):
     wl, steps, splits = CASES[name]

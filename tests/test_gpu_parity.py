@@ -64,14 +64,15 @@ def test_small_parity(name):
     assert rep.steps == steps
 
 
-# Both pipeline shapes forced on cases that reach their limits: ragged
-# splits, the sink fill, dense runs, fp32 rows of 1 KB (six-row stages in
-# shape 2) and windows longer than one item's row list (256 rows in shape 2).
+# Every launch pipeline forced on cases that reach their limits: ragged
+# splits, the sink fill, dense runs, fp32 rows of 1 KB (six-row stages with
+# 6 KB stages) and windows longer than one item's row list (256 rows with
+# 6 KB stages); pipelines 3 and 4 run three stages per warp.
 PIPE_CASES = ["ragged-split3", "sink4", "dense-split3", "f32-d128", "f32-d64-split4", "bf16-d64",
               "window-wider-than-a-stage-list", "long-prompt-split2"]
 
 
-@pytest.mark.parametrize("pipeline", [1, 2])
+@pytest.mark.parametrize("pipeline", [1, 2, 3, 4])
 @pytest.mark.parametrize("name", PIPE_CASES)
 def test_small_parity_each_pipeline(name, pipeline):
     wl, steps, splits = CASES[name]
@@ -102,9 +103,26 @@ def test_pipeline_choice_is_reported():
     h.set_pipeline(0)
     assert h.plan(400).pipeline == 1
     h.close()
+    # streams that would be split in two to fill the two-stage grid fit one
+    # round of the three-stage grid (8 warps per SM) unsplit: no merge launch
+    h = DSA(6 * sms, 128, 64, 288, 29, 0, "bf16")
+    p = h.plan(400)
+    assert (p.pipeline, p.nsplit) == (3, 1), (p.pipeline, p.nsplit)
+    h.close()
+    # a longer stream (164 rows) that FP8 rows would also split in two
+    # (32-row stages): three stages for bf16 rows, not for FP8 rows, whose
+    # warps are bound by their own arithmetic
+    h = DSA(6 * sms, 128, 64, 288, 100, 0, "bf16")
+    p = h.plan(400)
+    assert (p.pipeline, p.nsplit) == (3, 1), (p.pipeline, p.nsplit)
+    h.close()
+    h = DSA(6 * sms, 128, 64, 288, 100, 0, "fp8e4m3")
+    p = h.plan(400)
+    assert p.pipeline in (1, 2) and p.nsplit == 2, (p.pipeline, p.nsplit)
+    h.close()
 
 
-@pytest.mark.parametrize("pipeline", [1, 2])
+@pytest.mark.parametrize("pipeline", [1, 2, 3, 4])
 def test_split_count_does_not_change_the_result(pipeline):
     """The argmin is a total order on (logit, offset), and each logit is
     computed by the same lanes whatever the split or the pipeline shape:
