@@ -56,6 +56,34 @@ CASES = {
 }
 
 
+def test_window_wider_than_the_register_mask():
+    """A window of 8400 entries: once the window passes 8192 entries (256
+    mask words, more than a warp keeps in registers) the kernel reads the
+    mask words from global memory while it counts and lists the attended
+    offsets.  Every step of a stream pair through the whole selection phase
+    (N_att 8200: 200 selections per stream, all past 8192 entries) into
+    eviction; masks checked every 400 steps and at the end."""
+    wl = small("maskmem", 4, 8400, 8200, grid=92, heads=2, d=64)
+    rep = run_parity(wl, steps=8450, mask_every=400)
+    assert rep.ok, rep.summary()
+    assert rep.steps == 8450 and rep.selections == 2 * (8400 - 8200)
+
+
+def test_largest_window_is_accepted():
+    """N_r - sink = 65536 is the largest window (offsets are 16-bit in the
+    kernel's item lists); one entry more is rejected."""
+    from ar_image_gen_gb300 import dsa
+
+    code, h = dsa.dsa_create(2, 64, 4, 65536, 8, 0)
+    assert code == dsa.DSA_OK
+    assert dsa.dsa_destroy(h) == dsa.DSA_OK
+    code, h = dsa.dsa_create(2, 64, 4, 65540, 8, 4)
+    assert code == dsa.DSA_OK
+    assert dsa.dsa_destroy(h) == dsa.DSA_OK
+    code, h = dsa.dsa_create(2, 64, 4, 65537, 8, 0)
+    assert code == dsa.DSA_ERR_ARG
+
+
 @pytest.mark.parametrize("name", list(CASES))
 def test_small_parity(name):
     wl, steps, splits = CASES[name]
