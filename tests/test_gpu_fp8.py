@@ -147,3 +147,35 @@ def test_full_size_parity(key):
     rep = run_parity(wl, sample=sample_streams(wl.streams, n), mask_every=every, threads=8)
     assert rep.ok, rep.summary()
     assert rep.steps == wl.L_dec
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_every_code_reads_back_exactly(d):
+    """Every finite E4M3 code (254 of them, both zeros included) as a V
+    element of the one prompt row that takes all the attention (its key's
+    logit is 57 above the others in log2 units): each output element is
+    its code's value times the V scale, exactly (the scale is a power of
+    two and E4M3 values fit bf16), which pins the kernel's widening of
+    codes, normal and subnormal, of both signs.  Stream s holds codes
+    d s .. d s + d - 1, the two NaN codes replaced by zero."""
+    from ar_image_gen_gb300.dsa import DSA
+    from oracle.oracle import e4m3_decode
+
+    S, L_p, vs = 256 // d, 2, 2.0 ** -3
+    codes = np.arange(256).reshape(S, d)
+    vals = np.vectorize(lambda c: 0.0 if (c & 0x7F) == 0x7F else e4m3_decode(int(c)))(codes) * vs
+    V = torch.zeros((S, L_p, d), dtype=torch.float64)
+    V[:, 0, :] = torch.from_numpy(vals)
+    K = torch.zeros((S, L_p, d), dtype=torch.float64)
+    K[:, 0, 0] = 448.0  # the largest E4M3 value
+    h = DSA(S, d, L_p, 8, 4, 0, "fp8e4m3")
+    h.set_kv_scales(np.ones(S, np.float32), np.full(S, vs, np.float32))
+    h.prefill(K.to(torch.bfloat16).cuda(), V.to(torch.bfloat16).cuda())
+    q = torch.zeros((S, d), dtype=torch.bfloat16, device="cuda")
+    q[:, 0] = 1.0
+    zero = torch.zeros_like(q)
+    out = torch.empty_like(q)
+    h.decode_step(q, zero, zero, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.double().cpu(), torch.from_numpy(vals)), (out.double().cpu() - torch.from_numpy(vals)).abs().max()
+    h.close()
