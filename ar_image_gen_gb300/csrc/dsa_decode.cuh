@@ -328,13 +328,15 @@ struct Elem<__nv_fp8_e4m3> {
     }
 };
 
-// Pipeline shapes (compile-time): independent warps per CTA, shared-memory
-// stages per warp, and the decode rows one work item may list.  Shape 0
-// (8 KB stages, 512-row items, three CTAs of 4 warps per SM) keeps the most
-// bytes in flight per warp; shape 1 (6 KB stages, 256-row items, four CTAs
-// per SM) has a third more warps, so more streams (or pieces of streams) run
-// in one round.  Both hold about the same bytes in flight per SM; the host
-// picks one per launch.
+// Stage shapes (compile-time): warps per CTA, the size of a shared-memory
+// stage and the decode rows one work item may list.  With two stages per
+// warp, shape 0 (8 KB stages, 512-row items, three CTAs of 4 warps per SM)
+// keeps the most bytes in flight per warp and shape 1 (6 KB stages, 256-row
+// items, four CTAs per SM) has a third more warps, so more streams (or
+// pieces of streams) run in one round; both hold about the same bytes in
+// flight per SM.  The number of stages per warp (2 or 3; three leave two
+// CTAs per SM) is a launch parameter; the host picks shape and stage count
+// per launch.
 #ifndef DSA_WARPS
 #define DSA_WARPS 4
 #endif
