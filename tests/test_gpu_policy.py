@@ -203,3 +203,16 @@ def test_policy_interleaved_handles_on_one_stream(policy):
         assert A[l].sync_status() == DSA_OK and B[l].sync_status() == DSA_OK
         A[l].close()
         B[l].close()
+
+
+def test_policy_shape_knob_accepts_the_six_shapes_only():
+    from ar_image_gen_gb300 import dsa
+
+    code, h = dsa.dsa_pol_create(8, 128, 16, 9, dsa.DSA_POLICY_TOVA, dsa.DSA_BF16)
+    assert code == dsa.DSA_OK
+    for bad in (-1, 7):
+        assert dsa.dsa_pol_set_shape(h, bad) == dsa.DSA_ERR_ARG
+        assert "shape" in dsa.dsa_last_error()
+    for ok in (1, 2, 3, 4, 5, 6, 0):
+        assert dsa.dsa_pol_set_shape(h, ok) == dsa.DSA_OK
+    assert dsa.dsa_pol_destroy(h) == dsa.DSA_OK
