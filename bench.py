@@ -577,7 +577,8 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": workload_config(wl, f"phase-3 steady state from t = {t_start}"),
         "hbm_gbs": whole,
-        "roofline": {"bound": "hbm", "kernel": f"dsa::decode_kernel<{wl.dtype},{wl.head_dim},{plan.pipeline - 1}>",
+        "roofline": {"bound": "hbm", "kernel": f"dsa::decode_kernel<{wl.dtype},{wl.head_dim},{(plan.pipeline - 1) & 1}>, "
+                                                  f"{2 + (plan.pipeline - 1) // 2} stages per warp",
                      "achieved": achieved,
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
