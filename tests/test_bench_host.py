@@ -80,3 +80,28 @@ def test_workload_table_matches_the_sparsity_rule():
     assert n_att_for(1000, 0, 2000) == 1000
     d = WORKLOADS["janus-b96"].dense()
     assert d.N_r == d.N_att == d.L_dec == 576
+
+
+def test_clock_records_that_disqualify_a_run():
+    import bench
+
+    ok = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert bench.clocks_rejected(ok) is None
+    assert bench.clocks_rejected(dict(ok, reasons=["sw_power_cap"])) is None  # kept and noted
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert r in bench.clocks_rejected(dict(ok, reasons=[r]))
+    assert "no throttle reason" in bench.clocks_rejected(dict(ok, sm_mhz=1400.0))
+    assert bench.clocks_rejected(dict(ok, sm_mhz=1400.0, reasons=["sw_power_cap"])) is None
+    assert bench.clocks_rejected({"sm_mhz": None, "sm_max_mhz": None, "reasons": []}) is None
+
+
+def test_clock_sampler_parses_nvidia_smi_lines():
+    import bench
+
+    c = bench.ClockSampler(None)
+    c.lines = ["2070, 2070, 900.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+               "1980, 2070, 1300.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+               "garbage"]
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_max_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
+    assert s["sm_mhz"] == (2070 + 1980) / 2
