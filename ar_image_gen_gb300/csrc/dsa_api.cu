@@ -155,7 +155,7 @@ struct Plan {
 
 long long resident_warps(const dsa_ctx *h, int pi) { return (long long)h->sm_count * h->ctas_per_sm[pi] * kWarpsPerCta; }
 
-// Work items per stream under pipeline shape sh.  Splitting a stream costs a
+// Work items per stream under launch pipeline pi.  Splitting a stream costs a
 // partial write and a merge; it pays when the streams alone leave most warps
 // idle (each warp streams its rows through a short pipeline, so few warps
 // cannot keep HBM busy).  Streams are split into about resident-warps /
