@@ -950,6 +950,25 @@ int dsa_debug_copy_state(dsa_handle h, void *host_prefix, void *host_ring)
     return e == cudaSuccess ? DSA_OK : cuda_fail(e, "state copy");
 }
 
+int dsa_debug_set_step(dsa_handle h, int t, void *stream)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (h->A != h->R) return fail(DSA_ERR_ARG, "dsa_debug_set_step needs N_att == N_r (no selection)");
+    if (t < 0) return fail(DSA_ERR_ARG, "t must be >= 0 (got %d)", t);
+    if (!h->prefilled || h->t != 0 || h->graph_mode)
+        return fail(DSA_ERR_STATE, "dsa_debug_set_step needs a handle at step 0 after dsa_prefill, not in graph mode");
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t row = 2 * (size_t)h->D * elem_bytes(h->dtype);
+    cudaError_t e = cudaMemsetAsync(h->ring, 0, (size_t)h->S * h->R * row, st);
+    if (e == cudaSuccess && h->sink > 0)
+        e = cudaMemset2DAsync(static_cast<unsigned char *>(h->prefix) + (size_t)h->L_p * row, (size_t)h->Lcap * row, 0,
+                              (size_t)h->sink * row, (size_t)h->S, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    note_launch(st, h);
+    h->t = t;
+    return DSA_OK;
+}
+
 int dsa_set_wait_limit(dsa_handle h, uint32_t limit)
 {
     if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
@@ -1027,11 +1046,6 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     if (dtype == DSA_FP8_E4M3)
         return fail(DSA_ERR_ARG, "dsa_decode_step_noalloc: FP8 storage needs per-stream scales; use the handle API");
     if (t < 0) return fail(DSA_ERR_ARG, "t must be >= 0 (got %d)", t);
-    if (!ring || !mask || !last_sel || !q || !k_new || !v_new || !out || (L_p + sink > 0 && !prefix))
-        return fail(DSA_ERR_ARG, "state and input/output pointers must be non-NULL");
-    if (!aligned16(prefix) || !aligned16(ring) || !aligned16(q) || !aligned16(k_new) || !aligned16(v_new) ||
-        !aligned16(out) || ((uintptr_t)mask & 3u) || ((uintptr_t)last_sel & 3u))
-        return fail(DSA_ERR_ARG, "data pointers must be 16-byte aligned (mask and last_sel 4-byte aligned)");
 
     void *scratch = nullptr;
     int sms = 0;
@@ -1057,21 +1071,24 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     h.MW = (h.R + 31) / 32;
     h.sm_count = sms;
     for (int pi = 0; pi < dsa::kPipelines; ++pi) h.ctas_per_sm[pi] = occ[pi];
+    const Plan pl = make_plan(&h, t);
+    // Split streams keep their partials in the static scratch; a step that
+    // needs more than it holds is refused (before any pointer is used).
+    if ((long long)pl.nsplit * heads > INT_MAX) return fail(DSA_ERR_ARG, "grid too large");
+    const size_t need = pl.nsplit > 1 ? noalloc_scratch_bytes(heads, pl.nsplit, head_dim) : 256;
+    if (need > kNoAllocScratchBytes)
+        return fail(DSA_ERR_ARG,
+                    "dsa_decode_step_noalloc: %d streams in %d work items each need %zu bytes of scratch, more than "
+                    "the static %zu bytes; use the handle API (dsa_create / dsa_decode_step) for this size",
+                    heads, pl.nsplit, need, kNoAllocScratchBytes);
+
+    if (!ring || !mask || !last_sel || !q || !k_new || !v_new || !out || (L_p + sink > 0 && !prefix))
+        return fail(DSA_ERR_ARG, "state and input/output pointers must be non-NULL");
+    if (!aligned16(prefix) || !aligned16(ring) || !aligned16(q) || !aligned16(k_new) || !aligned16(v_new) ||
+        !aligned16(out) || ((uintptr_t)mask & 3u) || ((uintptr_t)last_sel & 3u))
+        return fail(DSA_ERR_ARG, "data pointers must be 16-byte aligned (mask and last_sel 4-byte aligned)");
     h.prefix = prefix;
     h.ring = ring;
-    Plan pl = make_plan(&h, t);
-    // Fewer splits if the automatic choice does not fit the static scratch.
-    int fit = 0;
-    while (fit < pl.nsplit && noalloc_scratch_bytes(heads, fit + 1, head_dim) <= kNoAllocScratchBytes) ++fit;
-    if (fit < pl.nsplit) {
-        h.forced_split = fit > 0 ? fit : 1;
-        pl = make_plan(&h, t);
-        if (fit == 0 || noalloc_scratch_bytes(heads, pl.nsplit, head_dim) > kNoAllocScratchBytes)
-            return fail(DSA_ERR_ARG,
-                        "dsa_decode_step_noalloc: %d streams with %d splits need %zu bytes of scratch, more than the "
-                        "static %zu bytes; use the handle API (dsa_create / dsa_decode_step) for this size",
-                        heads, pl.nsplit, noalloc_scratch_bytes(heads, pl.nsplit, head_dim), kNoAllocScratchBytes);
-    }
     rc = encode_ring_map(&h);
     if (rc != DSA_OK) return rc;
 
@@ -1127,5 +1144,21 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.early = 0;  // caller-owned state: the previous kernel may have written it
     e = launch_step(dtype, head_dim, pl.shape, p, h.ring_map, pl.grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return DSA_OK;
+}
+
+extern "C" int dsa_decode_step_noalloc_status(void *stream)
+{
+    void *scratch = nullptr;
+    int sms = 0;
+    int rc = noalloc_setup(&scratch, &sms);
+    if (rc != DSA_OK) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    int word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, scratch, sizeof word, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "status copy from the static scratch");
+    if (word & dsa::ST_TIMEOUT) return fail(DSA_ERR_TIMEOUT, "a bounded wait in the decode kernel gave up");
+    if (word & dsa::ST_CHECK) return fail(DSA_ERR_DEVICE_CHECK, "device consistency check failed (skip mask count)");
     return DSA_OK;
 }

@@ -15,9 +15,10 @@
 // persistent grid of one CTA per SM (stream-K): a CTA takes a contiguous run
 // of k-blocks, which may end inside one tile and begin inside another.  A
 // tile finished by one CTA is written directly; a tile shared by several
-// CTAs has each CTA write an fp32 partial, and the last to finish (a counter
-// per tile) sums the partials in segment order (deterministic) and writes
-// the tile.
+// CTAs is summed by the CTA that holds the tile's first k-block (for which
+// it is the last piece of its run): the others write fp32 partials and
+// count themselves done on the tile's counter, and that CTA waits for the
+// count, adds the partials in k order (deterministic) and writes the tile.
 //
 // CTA of 10 warps: warp 0 issues the TMA loads of W and x tiles (128-byte
 // swizzle) into a ring of shared-memory stages, warp 1 issues tcgen05.mma

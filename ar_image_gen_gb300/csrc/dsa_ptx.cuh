@@ -110,19 +110,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared (LDGSTS, L1 bypassed).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-// Arrives on `bar` once all earlier cp.async copies of this thread have
-// landed; the arrival counts toward the barrier's expected count.
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;

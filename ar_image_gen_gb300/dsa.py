@@ -44,8 +44,8 @@ STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_ARG", -2: "DSA_ERR_STATE", -3: "DSA_ER
 EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa_destroy", "dsa_get_step",
            "dsa_get_skip_mask", "dsa_get_last_selection", "dsa_sync_status", "dsa_last_error",
            "dsa_state_bytes", "dsa_plan_step", "dsa_set_kv_scales", "dsa_set_splits", "dsa_set_pipeline",
-           "dsa_set_wait_limit", "dsa_debug_copy_state",
-           "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc", "dsa_diag_trace", "dsa_set_graph_mode",
+           "dsa_set_wait_limit", "dsa_debug_copy_state", "dsa_debug_set_step",
+           "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc", "dsa_decode_step_noalloc_status", "dsa_diag_trace", "dsa_set_graph_mode",
            "dsa_sync_step",
            "dsa_proj_create", "dsa_proj_destroy", "dsa_qkv_rope", "dsa_decode_step_fused", "dsa_proj_sync_status",
            "dsa_proj_set_wait_limit", "dsa_pol_create", "dsa_pol_destroy", "dsa_pol_prefill", "dsa_pol_decode_step",
@@ -78,12 +78,14 @@ _L.dsa_plan_step.argtypes = [_P, _I, ctypes.POINTER(dsa_step_plan)]
 _L.dsa_set_splits.argtypes = [_P, _I]
 _L.dsa_set_kv_scales.argtypes = [_P, _P, _P]
 _L.dsa_debug_copy_state.argtypes = [_P, _P, _P]
+_L.dsa_debug_set_step.argtypes = [_P, _I, _P]
 _L.dsa_set_pipeline.argtypes = [_P, _I]
 _L.dsa_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
 _L.dsa_debug_fail_alloc_after.argtypes = [_I]
 _L.dsa_set_graph_mode.argtypes = [_P, _I]
 _L.dsa_sync_step.argtypes = [_P, _P]
 _L.dsa_decode_step_noalloc.argtypes = [_I] * 8 + [_P] * 9
+_L.dsa_decode_step_noalloc_status.argtypes = [_P]
 _L.dsa_diag_trace.argtypes = [_I] * 5 + [_P] * 3 + [_I] + [_P] * 6
 _L.dsa_proj_create.argtypes = [_I] * 4 + [ctypes.POINTER(_P)]
 _L.dsa_proj_destroy.argtypes = [_P]
@@ -213,6 +215,10 @@ def dsa_debug_copy_state(h, host_prefix: np.ndarray | None, host_ring: np.ndarra
                                    None if host_ring is None else host_ring.ctypes.data)
 
 
+def dsa_debug_set_step(h, t, stream=None) -> int:
+    return _L.dsa_debug_set_step(h, t, _stream(stream))
+
+
 def dsa_set_splits(h, nsplit) -> int:
     return _L.dsa_set_splits(h, nsplit)
 
@@ -242,6 +248,10 @@ def dsa_decode_step_noalloc(heads, head_dim, L_p, N_r, N_att, sink, dtype, t, pr
     return _L.dsa_decode_step_noalloc(heads, head_dim, L_p, N_r, N_att, sink, dtype, t, _ptr(prefix), _ptr(ring),
                                       _ptr(mask), _ptr(last_sel), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
                                       _stream(stream))
+
+
+def dsa_decode_step_noalloc_status(stream=None) -> int:
+    return _L.dsa_decode_step_noalloc_status(_stream(stream))
 
 
 def dsa_diag_trace(heads, head_dim, L_p, L_dec, dtype, Q, Kp, Kd, dist: np.ndarray, step_mass, mass_mean: np.ndarray,
@@ -465,6 +475,10 @@ class DSA:
     def sync_status(self, stream=None) -> int:
         return dsa_sync_status(self.h, stream)
 
+    def state_bytes(self) -> int:
+        """Device bytes of the handle's KV state (prefix, ring, skip mask)."""
+        return dsa_state_bytes(self.heads, self.head_dim, self.L_p, self.N_r, self.sink, self.dtype_code)
+
     def plan(self, t: int | None = None) -> dsa_step_plan:
         code, p = dsa_plan_step(self.h, self.t if t is None else t)
         _check(code, "dsa_plan_step")
@@ -484,6 +498,11 @@ class DSA:
 
     def set_splits(self, nsplit: int):
         _check(dsa_set_splits(self.h, nsplit), "dsa_set_splits")
+
+    def debug_set_step(self, t: int, stream=None):
+        """N_att == N_r handles only, right after prefill: jump to step t
+        (the skipped-over decode entries read as zero rows)."""
+        _check(dsa_debug_set_step(self.h, t, stream), "dsa_debug_set_step")
 
     def set_pipeline(self, pipeline: int):
         _check(dsa_set_pipeline(self.h, pipeline), "dsa_set_pipeline")

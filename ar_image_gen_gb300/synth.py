@@ -121,6 +121,8 @@ WORKLOADS = {
     "sweep512-sink4-s95": _wl("sweep512-sink4-s95", 2, 32, 32, 128, "bf16", 64, 32, 512, 95, 64, sink=4),
     # Lumina-mGPT-7B 1024x1024-shaped (4096 tokens)
     "lumina-s90-b16": _wl("lumina-s90-b16", 3, 32, 32, 128, "bf16", 64, 64, 2048, 90, 16),
+    "lumina-s90-b32": _wl("lumina-s90-b32", 3, 32, 32, 128, "bf16", 64, 64, 2048, 90, 32),
+    "lumina-s90-b54": _wl("lumina-s90-b54", 3, 32, 32, 128, "bf16", 64, 64, 2048, 90, 54),
     "lumina-s95-b16": _wl("lumina-s95-b16", 3, 32, 32, 128, "bf16", 64, 64, 2048, 95, 16),
     "lumina-s95-b32": _wl("lumina-s95-b32", 3, 32, 32, 128, "bf16", 64, 64, 2048, 95, 32),
     "lumina-s95-b54": _wl("lumina-s95-b54", 3, 32, 32, 128, "bf16", 64, 64, 2048, 95, 54),

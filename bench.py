@@ -1,16 +1,19 @@
 """Throughput of diagonal-aware sparse decode attention on GB300.
 
 A bench step is one decode step of the whole hot path for every layer of the
-workload: 30 (or 32) per-layer handles, each one fused kernel launch over
-batch x heads streams (append + evict, index set from the skip bitmask,
-gather, split-K softmax.V, fused argmin).  The metric counts stream-steps
-(sequence x layer x head) per second.
+workload: 32 per-layer handles, each one fused kernel launch (plus a small
+merge launch when streams are split) over batch x heads streams (append +
+evict, index set from the skip bitmask, gather, split-K softmax.V, fused
+argmin).  The metric counts stream-steps (sequence x layer x head) per second.
 
-Default workload: the Janus-Pro-7B-shaped attention stack (30 layers x 32
-heads x head_dim 128, bf16 KV, L_p 64, 24x24 grid = 576 decode tokens,
-N_r 288, 95 % sparsity -> N_att 29) at batch 96, in the phase-3 steady state
-(t >= N_r).  Inputs are seeded synthetic traces resident in HBM; each step
-touches 30 distinct layers' KV (about 4.4 GB), far more than the 129 MB L2.
+Default workload: the high-resolution stress stack (32 layers x 32 heads x
+head_dim 128, bf16 KV, L_p 96, 90x90 grid = 8100 decode tokens, N_r 4050,
+95 % sparsity -> N_att 405) at batch 64, about 139 GB of KV resident in HBM,
+in the phase-3 steady state (t >= N_r).  Inputs are seeded synthetic traces
+resident in HBM; each step reads every layer's KV (about 17 GB), far more
+than the 129 MB L2.  The same line carries the dense setting of the same
+kernel at the largest batch whose 32 layers of dense KV fit on the device,
+and the Janus-Pro-7B-shaped stack at batch 96 as an extra key.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -210,16 +213,24 @@ def workload_config(wl, phase: str) -> dict:
 
 class OracleArm:
     """The C oracle (fp64, as it stands) on `n` streams of layer 0 of the
-    workload, brought untimed to the phase-3 steady state."""
+    workload; steps stay inside the trace (0 .. L_dec - 1): past its last
+    step the sample is prefilled again and brought back, untimed, to the
+    step it is timed from."""
 
     def __init__(self, wl, n: int, device: str):
         from ar_image_gen_gb300.synth import TraceGen
-        from oracle.oracle import OracleBatch, max_threads
+        from oracle.oracle import max_threads
 
         self.wl = wl
         self.gen = TraceGen(wl.with_batch(max(1, (n + wl.heads - 1) // wl.heads)), layer=0, device=device)
         self.n = min(n, self.gen.S)
         self.threads = max_threads()
+        self.restart()
+
+    def restart(self):
+        from oracle.oracle import OracleBatch
+
+        wl = self.wl
         ks = vs = None
         if wl.dtype == "fp8e4m3":
             ks, vs = (x[: self.n] for x in self.gen.kv_scales())
@@ -229,37 +240,67 @@ class OracleArm:
         self.t = 0
 
     def inputs(self):
-        t = min(self.t, self.wl.L_dec - 1)
-        return [x[: self.n].double().cpu().numpy() for x in self.gen.step(t)]
+        return [x[: self.n].double().cpu().numpy() for x in self.gen.step(self.t)]
 
     def advance(self, t_end: int):
         while self.t < t_end:
             self.orc.step(*self.inputs(), threads=self.threads)
             self.t += 1
 
-    def timed_step(self) -> float:
-        """One decode step of the sample; returns its seconds (input
-        generation excluded)."""
+    def timed_step(self, t_from: int) -> tuple[float, int]:
+        """One decode step of the sample (from step t_from again once the
+        trace is exhausted); returns its seconds (input generation and any
+        restart excluded) and the step it ran."""
+        if self.t >= self.wl.L_dec:
+            self.restart()
+            self.advance(t_from)
         q, k, v = self.inputs()
         t0 = time.perf_counter()
         self.orc.step(q, k, v, threads=self.threads)
         el = time.perf_counter() - t0
         self.t += 1
-        return el
+        return el, self.t - 1
+
+
+def cpu_sample_streams(wl) -> int:
+    """Streams of the oracle sample: as many as keep its untimed approach to
+    the steady state (steps 0 .. N_r + sink - 1) near 1.5e8 row visits
+    (a few seconds on the host cores), at least 32."""
+    t0 = wl.N_r + wl.sink
+    rows = sum(wl.L_p + min(t + 1, wl.N_att) for t in range(t0))
+    return int(min(wl.streams, max(32, 1.5e8 // max(rows, 1))))
+
+
+def step_ranges(steps: list[int]) -> str:
+    """'a..b, c..d' for the runs of consecutive steps in `steps`."""
+    runs, start, prev = [], None, None
+    for t in steps:
+        if start is None:
+            start = prev = t
+        elif t == prev + 1:
+            prev = t
+        else:
+            runs.append((start, prev))
+            start = prev = t
+    if start is not None:
+        runs.append((start, prev))
+    return ", ".join(f"{a}..{b}" for a, b in runs)
 
 
 def oracle_baseline(wl, n_streams: int = 0, budget_s: float = 10.0, device: str = "cuda") -> dict:
     """Stream-steps/s of the oracle on phase-3 steps of a sample of layer 0,
     timed until about `budget_s` seconds of oracle work have run."""
-    arm = OracleArm(wl, n_streams or wl.streams, device)
+    arm = OracleArm(wl, n_streams or cpu_sample_streams(wl), device)
     t0 = wl.N_r + wl.sink
     arm.advance(t0)
-    spent, steps = 0.0, 0
-    while spent < budget_s and steps < 4 * wl.L_dec:
-        spent += arm.timed_step()
-        steps += 1
+    spent, ran = 0.0, []
+    while spent < budget_s:
+        el, t = arm.timed_step(t0)
+        spent += el
+        ran.append(t)
+    steps = len(ran)
     return {"value": arm.n * steps / spent, "unit": UNIT, "cores": arm.threads, "kind": "oracle",
-            "sample": f"{arm.n} streams of layer 0, phase-3 steps {t0}..{t0 + steps - 1} "
+            "sample": f"{arm.n} streams of layer 0, phase-3 steps {step_ranges(ran)} of the {wl.L_dec}-step trace "
                       f"({arm.n * steps} stream-steps in {spent:.1f} s of oracle time, fp64 C oracle, "
                       f"input generation excluded)"}
 
@@ -281,18 +322,23 @@ class Stack:
         self.handles = []
         self.gens = []
         self.outs = []
-        for layer in range(wl.layers):
-            gen = TraceGen(wl, layer=layer, device=device)
-            h = DSA(wl.streams, wl.head_dim, wl.L_p, wl.N_r, wl.N_att, wl.sink, wl.dtype)
-            if wl.dtype == "fp8e4m3":
-                h.set_kv_scales(*gen.kv_scales())
-            Kp, Vp = gen.prompt()
-            h.prefill(Kp, Vp)
-            self.handles.append(h)
-            self.gens.append(gen)
-            self.outs.append(torch.empty((wl.streams, wl.head_dim), dtype=Kp.dtype, device=device))
         self.pool_steps = pool_steps
         self.pool = None
+        try:
+            for layer in range(wl.layers):
+                gen = TraceGen(wl, layer=layer, device=device)
+                h = DSA(wl.streams, wl.head_dim, wl.L_p, wl.N_r, wl.N_att, wl.sink, wl.dtype)
+                self.handles.append(h)
+                if wl.dtype == "fp8e4m3":
+                    h.set_kv_scales(*gen.kv_scales())
+                Kp, Vp = gen.prompt()
+                h.prefill(Kp, Vp)
+                self.gens.append(gen)
+                self.outs.append(torch.empty((wl.streams, wl.head_dim), dtype=Kp.dtype, device=device))
+                del Kp, Vp
+        except BaseException:
+            self.close()
+            raise
 
     def advance(self, t_end: int, generate: bool = True):
         """Decode steps t = current .. t_end - 1 with freshly drawn inputs."""
@@ -320,6 +366,8 @@ class Stack:
         for h in self.handles:
             h.close()
         self.handles = []
+        self.pool = None
+        self.outs = []
 
 
 def time_steps(stack, steps: int, per_launch: bool):
@@ -490,11 +538,121 @@ def time_e2e(stack, steps: int):
     return max(start.elapsed_time(end), wall), h2d, d2h
 
 
+def kernels_per_step(stack, t: int) -> int:
+    """Kernel launches of one decode step of every layer at step t: the
+    decode kernel, plus the merge kernel where streams are split."""
+    p = stack.handles[0].plan(t)
+    return stack.wl.layers * (2 if p.nsplit > 1 else 1)
+
+
+def dense_stack(wl, pool_steps: int):
+    """The dense setting (N_r = N_att = L_dec) of the workload at the largest
+    batch, from the workload's own down, whose layers all fit on the device.
+    Returns (stack, batches tried that did not fit)."""
+    import torch
+
+    from ar_image_gen_gb300.dsa import DSA_ERR_OOM, DSAError
+
+    tried, b = [], wl.batch
+    while b >= 1:
+        st = None
+        try:
+            st = Stack(wl.dense().with_batch(b), pool_steps=pool_steps)
+            st.make_pool(0)
+            return st, tried
+        except (DSAError, torch.cuda.OutOfMemoryError) as e:
+            if isinstance(e, DSAError) and e.code != DSA_ERR_OOM:
+                raise
+            if st is not None:
+                st.close()
+            del st
+            torch.cuda.empty_cache()
+            tried.append(b)
+            b = b - 8 if b > 16 else b // 2
+    raise RuntimeError("no batch of the dense setting fits on the device")
+
+
+def time_dense(wl, args, peak: float, last_sparse_ms: float) -> dict:
+    """The 0 % sparsity setting of the same kernel at the largest batch that
+    fits: the last `dense_steps` steps of the trace (every layer, back to
+    back) and the last step alone.  The handles jump to the first timed step
+    (dsa_debug_set_step: the entries before it are zero rows, which move the
+    same bytes through the same launches as real ones)."""
+    import torch
+
+    dstack, tried = dense_stack(wl, args.pool)
+    dwl = dstack.wl
+    d_steps = max(2, min(args.dense_steps, dwl.L_dec - 1))
+    t_first = dwl.L_dec - 1 - d_steps
+    for h in dstack.handles:
+        h.debug_set_step(t_first)
+    time_steps(dstack, 1, per_launch=False)  # warm-up step t_first
+    t_first += 1
+    d_steps -= 1
+    d_ms, _, _ = time_steps(dstack, d_steps, per_launch=False)
+    d_bytes = sum(dstack.handles[0].plan(t_first + i).algo_bytes for i in range(d_steps))
+    last_dense_ms = _last_step_ms(dstack)
+    dplan_last = dstack.handles[0].plan(dwl.L_dec - 1)
+    status = max((h.sync_status() for h in dstack.handles), key=abs)
+    kv_gb = sum(1 for _ in dstack.handles) * dstack.handles[0].state_bytes() / 1e9
+    dstack.close()
+    del dstack
+    torch.cuda.empty_cache()
+    res = {
+        "workload": f"{dwl.name}: N_r = N_att = L_dec = {dwl.L_dec}, batch {dwl.batch} (largest that fits; "
+                    f"{kv_gb:.1f} GB of KV over {dwl.layers} layers), steps {t_first}..{t_first + d_steps - 1}",
+        "batch": dwl.batch, "batches_that_did_not_fit": tried, "kv_gb": kv_gb,
+        "value": dwl.streams * dwl.layers * d_steps / (d_ms / 1e3), "unit": UNIT,
+        "hbm_gbs": d_bytes * dwl.layers / (d_ms / 1e3) / 1e9,
+        "frac": d_bytes * dwl.layers / (d_ms / 1e3) / 1e9 / peak,
+        "last_step_ms": last_dense_ms,
+        "last_step_gbs": dplan_last.algo_bytes * dwl.layers / (last_dense_ms / 1e3) / 1e9,
+        "device_status": status,
+    }
+    if dwl.batch == wl.batch:
+        res["last_step_speedup_sparse_vs_dense"] = last_dense_ms / last_sparse_ms
+    else:
+        res["last_step_speedup_sparse_vs_dense_per_stream"] = (last_dense_ms / dwl.batch) / (last_sparse_ms / wl.batch)
+    return res
+
+
+def time_extra(key: str, args, ws: int, peak: float) -> dict:
+    """Another workload's sparse steady state (all its layers), timed like the
+    main line: stream-steps/s and the decode kernel's roofline fraction."""
+    import torch
+
+    from ar_image_gen_gb300.synth import WORKLOADS
+
+    wl = WORKLOADS[key]
+    if args.kv == "fp8":
+        wl = wl.fp8()
+    stack = Stack(wl, pool_steps=args.pool)
+    t_start = wl.N_r + wl.sink
+    stack.advance(t_start)
+    stack.make_pool(t_start)
+    plan = stack.handles[0].plan(t_start)
+    time_steps(stack, args.warmup, per_launch=False)
+    barrier(ws)
+    steps = max(20, args.steps)
+    el_ms, _, launches = time_steps(stack, steps, per_launch=False)
+    el_ms = max_over_ranks(el_ms, ws)
+    per_launch_ms = el_ms / launches
+    achieved = plan.algo_bytes / (per_launch_ms / 1e3) / 1e9
+    status = max((h.sync_status() for h in stack.handles), key=abs)
+    stack.close()
+    del stack
+    torch.cuda.empty_cache()
+    return {"workload": workload_config(wl, f"phase-3 steady state from t = {t_start}")["workload"],
+            "value": wl.streams * wl.layers * steps * ws / (el_ms / 1e3), "unit": UNIT, "steps": steps,
+            "ms_per_step": el_ms / steps, "launch_ms": per_launch_ms, "algo_bytes_per_launch": plan.algo_bytes,
+            "achieved_gbs": achieved, "frac": achieved / peak, "traffic": profiled_traffic(wl.name),
+            "pipeline": plan.pipeline, "nsplit": plan.nsplit, "device_status": status}
+
+
 def run_ours(args, rank: int, ws: int) -> dict | None:
     import torch
 
     from __graft_entry__ import build
-    from ar_image_gen_gb300.synth import WORKLOADS
 
     build()
     torch.cuda.init()
@@ -504,6 +662,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
     except Exception:
         pass
+    peak, peak_kind = measured_peak()
 
     # --- sparse setting, phase-3 steady state
     stack = Stack(wl, pool_steps=args.pool)
@@ -525,15 +684,16 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
             el_ms, _, launches = time_steps(stack, args.steps, per_launch=False)
         clocks = dict(clk.summary(), first_run_rejected=why)
     el_ms = max_over_ranks(el_ms, ws)
-    # The timed region launches only the decode kernel, back to back (each
-    # launch may overlap the previous one's tail): its average duration is
-    # the region's time over the launches.  A second pass with events around
-    # every launch gives the duration of a launch that cannot overlap.
+    # The timed region launches only the decode kernel (and, where streams
+    # are split, its merge kernel), back to back (each launch may overlap the
+    # previous one's tail): its average duration is the region's time over
+    # the decode launches.  A second pass with events around every launch
+    # gives the duration of a launch that cannot overlap.
     per_launch_ms = el_ms / launches
+    gpu_launches = kernels_per_step(stack, t_start) * args.steps
     _, isolated_ms, _ = time_steps(stack, max(4, min(args.steps, 50)), per_launch=True)
     stream_steps = wl.streams * wl.layers * args.steps * ws
     value = stream_steps / (el_ms / 1e3)
-    peak, peak_kind = measured_peak()
     achieved = plan.algo_bytes / (per_launch_ms / 1e3) / 1e9
     whole = plan.algo_bytes * wl.layers * args.steps * ws / (el_ms / 1e3) / 1e9
     traffic = profiled_traffic(wl.name)
@@ -545,10 +705,10 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     graph = None
     if args.graph:
         graph = time_graph(stack, max(4, min(args.steps, 200)), ws)
-        graph["frac"] = plan.algo_bytes / (graph["launch_ms"] / 1e3) / 1e9 / measured_peak()[0]
+        graph["frac"] = plan.algo_bytes / (graph["launch_ms"] / 1e3) / 1e9 / peak
 
     # --- end to end through the public API with host buffers
-    e2e_steps = max(3, min(args.steps // 4, 100))
+    e2e_steps = max(50, min(args.steps, 200))
     e2e_ms, h2d, d2h = time_e2e(stack, e2e_steps)
     e2e_ms = max_over_ranks(e2e_ms, ws)
     e2e_value = wl.streams * wl.layers * e2e_steps * ws / (e2e_ms / 1e3)
@@ -557,42 +717,24 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     stack.advance(wl.L_dec - 1, generate=False)
     last_sparse_ms = _last_step_ms(stack)
     status = max((h.sync_status() for h in stack.handles), key=abs)
-    # the whole trace, all phases, three runs
+    # the whole trace, all phases: three runs where a run is short, else one
     trace = None
     if not args.no_trace:
-        trace = time_trace(stack, 3)
-        trace["frac"] = trace["hbm_gbs"] / measured_peak()[0]
+        est_s = sum(stack.handles[0].plan(t).algo_bytes for t in range(wl.L_dec)) * wl.layers / (0.8 * peak * 1e9)
+        trace = time_trace(stack, 3 if est_s < 20 else 1)
+        trace["frac"] = trace["hbm_gbs"] / peak
         status = max([status] + [h.sync_status() for h in stack.handles], key=abs)
     stack.close()
     del stack
     torch.cuda.empty_cache()
 
     # --- dense setting (0 % sparsity) of the same kernel: N_r = N_att = L_dec
-    dense = None
-    if not args.no_dense:
-        dwl = wl.dense()
-        dstack = Stack(dwl, pool_steps=args.pool)
-        dstack.make_pool(0)
-        d_steps = max(2, min(args.dense_steps, dwl.L_dec - 1))
-        dstack.advance(dwl.L_dec - 1 - d_steps, generate=False)
-        dplan_first = dstack.handles[0].plan()
-        d_ms, _, _ = time_steps(dstack, d_steps, per_launch=False)
-        d_bytes = sum(dstack.handles[0].plan(dplan_first.t_inner + i).algo_bytes for i in range(d_steps))
-        last_dense_ms = _last_step_ms(dstack)
-        dplan_last = dstack.handles[0].plan(dwl.L_dec - 1)
-        dense = {
-            "workload": f"{dwl.name}: N_r = N_att = L_dec = {dwl.L_dec}, steps {dplan_first.t_inner}.."
-                        f"{dplan_first.t_inner + d_steps - 1}",
-            "value": dwl.streams * dwl.layers * d_steps / (d_ms / 1e3), "unit": UNIT,
-            "hbm_gbs": d_bytes * dwl.layers / (d_ms / 1e3) / 1e9,
-            "frac": d_bytes * dwl.layers / (d_ms / 1e3) / 1e9 / peak,
-            "last_step_gbs": dplan_last.algo_bytes * dwl.layers / (last_dense_ms / 1e3) / 1e9,
-        }
-        dstack.close()
-        del dstack
-        torch.cuda.empty_cache()
-        dense["last_step_ms"] = last_dense_ms
-        dense["last_step_speedup_sparse_vs_dense"] = last_dense_ms / last_sparse_ms
+    dense = None if args.no_dense else time_dense(wl, args, peak, last_sparse_ms)
+
+    # --- other workloads' steady state, as extra keys
+    extra = {}
+    for key in ([] if args.no_extra else [k for k in args.extra.split(",") if k and k != args.workload]):
+        extra[key] = time_extra(key, args, ws, peak)
 
     if rank != 0:
         return None
@@ -608,18 +750,22 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algo_bytes_per_launch": plan.algo_bytes, "launch_ms": per_launch_ms,
+                     "launch_ms_note": "timed region / decode launches (merge launches of split streams included)",
                      "isolated_launch_ms": isolated_ms,
                      "grid": plan.grid, "nsplit": plan.nsplit, "pipeline": plan.pipeline},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
-        "gpu_launches": launches,
+        "gpu_launches": gpu_launches,
         "clocks": clocks,
         "last_step": {"sparse_ms": last_sparse_ms},
         "trace": trace,
         "graph": graph,
         "dense": dense,
+        "extra": extra,
         "device_status": status,
     }
+    if dense is not None:
+        res["config"]["dense_batch"] = dense["batch"]
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = oracle_baseline(wl, budget_s=args.cpu_budget)
     if args.layers:
@@ -657,15 +803,19 @@ def run_reference(args, rank: int, ws: int) -> dict | None:
     build_oracle()
     wl = _workload(args)
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    arm = OracleArm(wl, args.ref_streams, device)
+    arm = OracleArm(wl, args.ref_streams or cpu_sample_streams(wl), device)
     t0 = wl.N_r + wl.sink
     arm.advance(t0)
     for _ in range(args.warmup):
-        arm.timed_step()
-    spent = sum(arm.timed_step() for _ in range(args.steps))
+        arm.timed_step(t0)
+    spent, ran = 0.0, []
+    for _ in range(args.steps):
+        el, t = arm.timed_step(t0)
+        spent += el
+        ran.append(t)
     value = arm.n * args.steps / spent
     sample = (f"each step: one phase-3 decode step of {arm.n} streams of layer 0 "
-              f"(steps {t0 + args.warmup}..{t0 + args.warmup + args.steps - 1}), fp64 C oracle, "
+              f"(steps {step_ranges(ran)} of the {wl.L_dec}-step trace), fp64 C oracle, "
               f"input generation excluded")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
@@ -693,7 +843,8 @@ def _workload(args):
 
 
 SWEEP = ["janus-b32", "janus-b96", "sweep512-s50", "sweep512-s75", "sweep512-s90", "sweep512-s95",
-         "sweep512-sink4-s95", "lumina-s90-b16", "lumina-s95-b16", "lumina-s95-b32", "lumina-s95-b54", "stress-s95"]
+         "sweep512-sink4-s95", "lumina-s90-b16", "lumina-s90-b32", "lumina-s90-b54", "lumina-s95-b16", "lumina-s95-b32",
+         "lumina-s95-b54", "stress-s95"]
 
 
 def run_sweep(args) -> None:
@@ -974,7 +1125,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="janus-b96")
+    ap.add_argument("--workload", default="stress-s95")
+    ap.add_argument("--extra", default="janus-b96", help="comma-separated workloads timed as extra keys")
+    ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--pool", type=int, default=8, help="distinct input steps kept in HBM and cycled")
     ap.add_argument("--dense-steps", type=int, default=16)
     ap.add_argument("--no-dense", action="store_true")
@@ -982,7 +1135,8 @@ def main(argv=None):
     ap.add_argument("--no-trace", action="store_true", help="skip the whole-trace timing")
     ap.add_argument("--graph", action="store_true", help="also time the steady state replayed from a CUDA graph")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--ref-streams", type=int, default=256, help="streams per step of the reference arm")
+    ap.add_argument("--ref-streams", type=int, default=0,
+                    help="streams per step of the reference arm (0: as many as keep its untimed approach short)")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
     ap.add_argument("--kv", choices=["native", "fp8"], default="native",
                     help="fp8: store the KV state as FP8 E4M3 (q, k, v, out stay bf16)")

@@ -207,19 +207,33 @@ int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out);
  *   q, k_new, v_new, out  as for dsa_decode_step.
  * The split partials and a status word live in a static 4 MiB device array
  * of this library (every GPU that loads the library holds it until the
- * process exits).  Workloads whose splits would need more (about 7,900
- * streams at head_dim 128 without splits, fewer with splits) are rejected
- * with DSA_ERR_ARG and a message.  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress): make that
- * first call before any stream capture.  Every call shares the array and
- * clears its status word when it starts, so calls that overlap on the GPU
- * (other streams, other threads) race: order them on one stream.
- * Device-side errors (a bounded wait that gave up) are not reported by this
- * entry point.  Asynchronous on `stream`.
+ * process exits).  Streams that run as one work item each (the usual case
+ * beyond about a thousand streams) need only the status word; split streams
+ * need 528 bytes per work item at head_dim 128 (272 at 64), so a step is
+ * refused with DSA_ERR_ARG and a message when its streams x work items
+ * exceed about 7,900 (15,400 at head_dim 64).  That check comes before the
+ * pointers are looked at.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress): make that first call before any
+ * stream capture.  Every call shares the array and clears its status word
+ * when it starts, so calls that overlap on the GPU (other streams, other
+ * threads) race: order them on one stream.  Device-side errors (a bounded
+ * wait that gave up, a skip-mask count that disagrees with the step) are
+ * recorded in that status word: dsa_decode_step_noalloc_status reads it.
+ * Asynchronous on `stream`.
  */
 int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int dtype, int t,
                             void *prefix, void *ring, uint32_t *mask, int32_t *last_sel, const void *q,
                             const void *k_new, const void *v_new, void *out, void *stream);
+
+/*
+ * dsa_decode_step_noalloc_status -- the device status of the last
+ * dsa_decode_step_noalloc call on the current device: waits for `stream`
+ * (pass the stream of that call) and returns DSA_OK, DSA_ERR_TIMEOUT or
+ * DSA_ERR_DEVICE_CHECK (DSA_ERR_CUDA if the copy failed).  Valid until the
+ * next dsa_decode_step_noalloc call on the device, which clears the word.
+ * Allocates nothing.  The paper has no counterpart.
+ */
+int dsa_decode_step_noalloc_status(void *stream);
 
 /*
  * dsa_set_kv_scales -- per-stream scales of a DSA_FP8_E4M3 handle.  The
@@ -260,6 +274,22 @@ int dsa_set_pipeline(dsa_handle h, int pipeline);
  * DSA_FP8_E4M3).  Either pointer may be NULL.  Used by the tests to check
  * stored values bit for bit. */
 int dsa_debug_copy_state(dsa_handle h, void *host_prefix, void *host_ring);
+
+/*
+ * dsa_debug_set_step -- move a freshly prefilled handle (step 0) to step t
+ * without decoding the steps before it.  Only for handles that never
+ * select (N_att == N_r: the dense and sliding-window settings, whose skip
+ * sets stay empty), so the state at step t is the prompt plus the decode
+ * entries alone.  The entries the jump passes over are zero rows (every
+ * ring slot and the sink rows of the prefix are cleared; a zero K row
+ * scores 0 and a zero V row adds nothing), so the next step attends the
+ * prompt plus min(t + 1, N_r) decode rows as a real step t would: the same
+ * rows, bytes and launch.  Lets a benchmark time the last steps of a long
+ * dense trace without running all the steps before them.  Asynchronous on
+ * `stream`.  DSA_ERR_STATE if the handle is not at step 0 after
+ * dsa_prefill, or is in graph mode; DSA_ERR_ARG if N_att != N_r or t < 0.
+ */
+int dsa_debug_set_step(dsa_handle h, int t, void *stream);
 
 /* Poll limit of the bounded waits inside the decode kernel (default: none;
  * every wait still gives up after about one second).  A limit of 0 makes

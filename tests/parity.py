@@ -82,21 +82,23 @@ def run_parity(wl: Workload, steps: int | None = None, sample: list[int] | None 
         ks, vs = ks[sample], vs[sample]
     orc = OracleBatch(len(sample), d, wl.L_p, wl.N_r, wl.N_att, wl.sink, k_scales=ks, v_scales=vs)
 
+    # The sampled streams are taken from host copies (device-to-host copies,
+    # no device kernels besides the library's own).
     Kp, Vp = gen.prompt()
     Kp_d, Vp_d = Kp.to(device), Vp.to(device)
     h.prefill(Kp_d, Vp_d)
-    orc.prefill(Kp_d[idx.to(device)].double().cpu().numpy(), Vp_d[idx.to(device)].double().cpu().numpy())
+    orc.prefill(Kp.cpu()[idx].double().numpy(), Vp.cpu()[idx].double().numpy())
     out = torch.empty((S, d), dtype=Kp_d.dtype, device=device)
-    idx_d = idx.to(device)
     for t in range(steps):
-        q, k, v = (x.to(device) for x in gen.step(t))
+        qkv = gen.step(t)
+        q, k, v = (x.to(device) for x in qkv)
         h.decode_step(q, k, v, out)
         sel = h.last_selection()  # synchronizes
         tin = t - wl.sink
         picks = np.array([tin - sel[s] if sel[s] >= 0 else -1 for s in sample], dtype=np.int32)
-        ref, infos = orc.step(q[idx_d].double().cpu().numpy(), k[idx_d].double().cpu().numpy(),
-                              v[idx_d].double().cpu().numpy(), picks=picks, threads=threads)
-        got = out[idx_d].double().cpu().numpy()
+        qh, kh, vh = (x.cpu()[idx].double().numpy() for x in qkv)
+        ref, infos = orc.step(qh, kh, vh, picks=picks, threads=threads)
+        got = out.cpu()[idx].double().numpy()
         err = np.abs(got - ref)
         excess = err - (ATOL + RTOL * np.abs(ref))
         rep.max_err = max(rep.max_err, float(err.max()))

@@ -71,6 +71,7 @@ def test_calls_on_a_null_handle_fail_cleanly(dsa):
     assert dsa.dsa_get_step(null)[0] == dsa.DSA_ERR_STATE
     assert dsa.dsa_sync_status(null) == dsa.DSA_ERR_STATE
     assert dsa.dsa_plan_step(null, 0)[0] == dsa.DSA_ERR_STATE
+    assert dsa.dsa_debug_set_step(null, 5) == dsa.DSA_ERR_STATE
 
 
 def test_state_bytes_is_the_kv_bound(dsa):

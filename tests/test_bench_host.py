@@ -76,6 +76,11 @@ def test_workload_table_matches_the_sparsity_rule():
     assert WORKLOADS["janus-b96"].N_att == 29 and WORKLOADS["janus-b96"].streams == 3072
     assert [WORKLOADS[f"sweep512-s{s}"].N_att for s in (0, 50, 75, 90, 95)] == [512, 512, 256, 102, 51]
     assert (WORKLOADS["lumina-s90-b16"].N_att, WORKLOADS["lumina-s95-b16"].N_att) == (410, 205)
+    # Lumina-mGPT-shaped: 90 % and 95 % sparsity at batch 16, 32 and 54
+    for s, n in ((90, 410), (95, 205)):
+        for b in (16, 32, 54):
+            wl = WORKLOADS[f"lumina-s{s}-b{b}"]
+            assert (wl.N_att, wl.batch, wl.N_r, wl.L_dec, wl.layers) == (n, b, 2048, 4096, 32)
     assert WORKLOADS["stress-s95"].N_att == 405 and WORKLOADS["stress-s95"].L_dec == 8100
     assert n_att_for(1000, 0, 2000) == 1000
     d = WORKLOADS["janus-b96"].dense()
@@ -105,3 +110,37 @@ def test_clock_sampler_parses_nvidia_smi_lines():
     s = c.summary()
     assert s["samples"] == 2 and s["sm_max_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
     assert s["sm_mhz"] == (2070 + 1980) / 2
+
+
+def test_step_ranges_names_runs_of_steps():
+    import bench
+
+    assert bench.step_ranges([5, 6, 7, 2, 3, 9]) == "5..7, 2..3, 9..9"
+    assert bench.step_ranges([]) == ""
+
+
+def test_oracle_sample_stays_inside_the_trace():
+    """The CPU baseline times phase-3 steps only and never steps past the
+    trace's last step: once the sample reaches L_dec it is prefilled again
+    and brought back to N_r (untimed)."""
+    import re
+
+    import bench
+    from ar_image_gen_gb300.synth import WORKLOADS
+
+    wl = WORKLOADS["tiny"]
+    res = bench.oracle_baseline(wl, n_streams=4, budget_s=0.3, device="cpu")
+    runs = re.search(r"phase-3 steps (.*) of the 64-step trace", res["sample"]).group(1).split(", ")
+    assert len(runs) >= 2  # the sample wrapped around at least once
+    for r in runs:
+        a, b = (int(x) for x in r.split(".."))
+        assert wl.N_r <= a <= b <= wl.L_dec - 1
+    assert res["value"] > 0 and res["cores"] >= 1
+
+
+def test_cpu_sample_is_bounded():
+    import bench
+    from ar_image_gen_gb300.synth import WORKLOADS
+
+    assert bench.cpu_sample_streams(WORKLOADS["janus-b96"]) == 3072
+    assert 32 <= bench.cpu_sample_streams(WORKLOADS["stress-s95"]) <= 128

@@ -40,6 +40,9 @@ FULL = {
     "sweep512-s95": (24, 16),
     "sweep512-sink4-s95": (24, 16),
     "lumina-s90-b16": (16, 32),
+    "lumina-s90-b32": (16, 32),
+    "lumina-s90-b54": (16, 32),
+    "lumina-s95-b16": (16, 32),
     "lumina-s95-b32": (16, 32),
     "lumina-s95-b54": (16, 32),
     "stress-s95": (12, 64),

@@ -224,3 +224,68 @@ def test_interleaved_handles_on_one_stream(splits):
     for gen, h, orc, out in layers:
         assert h.sync_status() == 0
         h.close()
+
+
+@pytest.mark.parametrize("sink,N_r", [(0, 90), (0, 40), (4, 40)])
+def test_step_jump_equals_decoding_zero_rows(sink, N_r):
+    """dsa_debug_set_step on a handle that never selects (N_att == N_r): the
+    jump to step t0 leaves the state a decode of zero rows up to t0 would
+    leave, so later steps match the oracle fed zero k / v rows for steps
+    0 .. t0 - 1.  N_r = 90 keeps every entry (dense); N_r = 40 evicts, so
+    the zero rows leave the window as real steps replace them; with sinks
+    the jumped-over sink rows are zero too."""
+    import numpy as np
+
+    from ar_image_gen_gb300.dsa import DSA
+    from ar_image_gen_gb300.synth import TraceGen
+    from oracle.oracle import OracleBatch
+
+    wl = small("jump", 24, N_r, N_r, sink=sink, grid=9, heads=5)
+    S, d, t0 = wl.streams, wl.head_dim, 30
+    gen = TraceGen(wl, device="cuda")
+    K, V = gen.prompt()
+    h = DSA(S, d, wl.L_p, wl.N_r, wl.N_att, sink, "bf16")
+    h.prefill(K, V)
+    h.debug_set_step(t0)
+    assert h.t == t0
+    orc = OracleBatch(S, d, wl.L_p, wl.N_r, wl.N_att, sink)
+    orc.prefill(K.double().cpu().numpy(), V.double().cpu().numpy())
+    zero = np.zeros((S, d))
+    for _ in range(t0):
+        orc.step(zero, zero, zero)
+    out = torch.empty((S, d), dtype=torch.bfloat16, device="cuda")
+    for t in range(t0, wl.L_dec):
+        q, k, v = gen.step(t)
+        h.decode_step(q, k, v, out)
+        ref, _ = orc.step(q.double().cpu().numpy(), k.double().cpu().numpy(), v.double().cpu().numpy())
+        got = out.double().cpu().numpy()
+        assert (np.abs(got - ref) <= 2e-3 + 1e-2 * np.abs(ref)).all(), f"t={t}"
+    assert h.sync_status() == 0
+    h.close()
+
+
+def test_step_jump_is_refused_where_it_does_not_apply():
+    from ar_image_gen_gb300 import dsa
+    from ar_image_gen_gb300.dsa import DSA, DSAError
+
+    wl = small("jumpno", 8, 40, 9, grid=8, heads=2)
+    K = torch.zeros((2, 8, 128), dtype=torch.bfloat16, device="cuda")
+    h = DSA(2, 128, 8, 40, 9, 0, "bf16")  # selects: N_att < N_r
+    h.prefill(K, K)
+    with pytest.raises(DSAError) as e:
+        h.debug_set_step(10)
+    assert e.value.code == dsa.DSA_ERR_ARG
+    h.close()
+    h = DSA(2, 128, 8, 40, 40, 0, "bf16")
+    with pytest.raises(DSAError) as e:  # before prefill
+        h.debug_set_step(10)
+    assert e.value.code == dsa.DSA_ERR_STATE
+    h.prefill(K, K)
+    q = torch.zeros((2, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    h.decode_step(q, q, q, out)
+    with pytest.raises(DSAError) as e:  # not at step 0
+        h.debug_set_step(10)
+    assert e.value.code == dsa.DSA_ERR_STATE
+    assert h.sync_status() == 0
+    h.close()

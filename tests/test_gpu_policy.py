@@ -41,30 +41,35 @@ class Report:
         return not self.failures
 
 
-def run_policy(wl: Workload, policy: str, steps: int, sample=None, check_every: int = 1, shape: int = 0) -> Report:
+def run_policy(wl: Workload, policy: str, steps: int, sample=None, check_every: int = 1, shape: int = 0,
+               gen_device: str = "cuda") -> Report:
+    """Runs `steps` steps of `policy` on the GPU and the sampled streams on
+    the oracle.  Inputs are drawn on `gen_device`; the oracle's share is
+    taken from host copies."""
     from ar_image_gen_gb300.dsa import DSA_OK, Policy
 
-    gen = TraceGen(wl, device="cuda")
+    gen = TraceGen(wl, device=gen_device)
     S, d = gen.S, wl.head_dim
     sample = list(range(S)) if sample is None else list(sample)
-    idx = torch.tensor(sample, device="cuda")
+    idx = torch.tensor(sample)
     h = Policy(S, d, wl.L_p, wl.N_att, policy, wl.dtype)
     if shape:
         h.set_shape(shape)
     Kp, Vp = gen.prompt()
-    h.prefill(Kp, Vp)
+    h.prefill(Kp.to("cuda"), Vp.to("cuda"))
     orc = [PolicyStream(d, wl.L_p, wl.N_att, policy) for _ in sample]
-    Kh, Vh = Kp[idx].double().cpu().numpy(), Vp[idx].double().cpu().numpy()
+    Kh, Vh = Kp.cpu()[idx].double().numpy(), Vp.cpu()[idx].double().numpy()
     for i, o in enumerate(orc):
         o.prefill(Kh[i], Vh[i])
     out = torch.empty((S, d), dtype=Kp.dtype, device="cuda")
     rep = Report()
     for t in range(steps):
-        q, k, v = gen.step(t)
+        qkv = gen.step(t)
+        q, k, v = (x.to("cuda") for x in qkv)
         h.decode_step(q, k, v, out)
         ev = h.last_eviction()  # synchronizes
-        qh, kh, vh = (x[idx].double().cpu().numpy() for x in (q, k, v))
-        got = out[idx].double().cpu().numpy()
+        qh, kh, vh = (x.cpu()[idx].double().numpy() for x in qkv)
+        got = out.cpu()[idx].double().numpy()
         for i, s in enumerate(sample):
             ref, info = orc[i].step(qh[i], kh[i], vh[i], pick=int(ev[s]))
             err = np.abs(got[i] - ref)
