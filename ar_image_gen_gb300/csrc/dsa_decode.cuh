@@ -230,29 +230,21 @@ struct Elem<__nv_bfloat16> {
 // scale.  The kernel keeps the scales out of the inner loops: logits are
 // q . code (times the K scale, applied once per logit with the softmax
 // scale) and P.V accumulates p * code (times the V scale at the end).
-// q is rounded to f16 once per item, codes widen exactly to f16, and
-// products accumulate in fp32 (mixed-precision FMA).
-//
-// Widening by bit moves instead of a conversion instruction: a code with
-// sign s, exponent field e (4 bits) and mantissa m (3 bits), read as the
-// f16 bits s << 15 | e << 10 | m << 7, is the code's value times 2^-8 --
-// 2^(e-15) (1 + m/8) against 2^(e-7) (1 + m/8) for normal codes, and
-// 2^-14 m/8 against 2^-6 m/8 for subnormal ones (e = 0 in both formats).
-// The factor 2^8 (kWiden) goes into the K scale of each logit and the V
-// scale of each output; powers of two scale without rounding, so results
-// are those of the codes' exact f16 values.  (The NaN codes 0x7F / 0xFF
-// would read as finite values; the stored inputs are finite.)
+// q is rounded to f16 once per item (exact: every bf16 value in the f16
+// range is an f16 value), each pair of codes widens exactly to an f16 pair
+// with one conversion instruction (every E4M3 value is an f16 value), and
+// products accumulate in fp32 (mixed-precision FMA: f16 x f16 products are
+// exact in fp32).  Stored codes are finite (satfinite), so no NaN code is
+// ever widened.
 __device__ __forceinline__ uint32_t f16x2_bits(__half2 h) { return *reinterpret_cast<const uint32_t *>(&h); }
 
-// f16x2 (value * 2^-8) of codes 1 and 3 of the four codes in w (byte i = code i).
-__device__ __forceinline__ uint32_t e4m3_odd_f16x2(uint32_t w)
+// The two E4M3 codes in the low 16 bits of w as an f16 pair (code 0 in the
+// low half).
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w)
 {
-    return (w & 0x80008000u) | ((w >> 1) & 0x3F803F80u);
-}
-// f16x2 (value * 2^-8) of codes 0 and 2 of the four codes in w.
-__device__ __forceinline__ uint32_t e4m3_even_f16x2(uint32_t w)
-{
-    return ((w << 8) & 0x80008000u) | ((w << 7) & 0x3F803F80u);
+    uint32_t r;
+    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(r) : "r"(w));
+    return r;
 }
 
 // acc0 += lo(a) * lo(b), acc1 += hi(a) * hi(b) for f16x2 a, b in fp32.
@@ -271,42 +263,33 @@ struct Elem<__nv_fp8_e4m3> {
     using Vec = uint2;                  // 8 codes
     static constexpr bool SCALED = true;
     static constexpr int VEC = 8;
-    static constexpr float kWiden = 256.f;  // code value / widened f16 value
-    // 8 q elements as f16 pairs in the order the widened codes come in:
-    // (0, 2), (1, 3), (4, 6), (5, 7)
-    struct Q { uint32_t h[4]; };
+    static constexpr float kWiden = 1.f;  // widened values are the codes' values
+    struct Q { uint32_t h[4]; };          // 8 q elements as f16 pairs (0, 1), (2, 3), (4, 5), (6, 7)
     static __device__ __forceinline__ Q load_q(const uint4 &v)  // 8 bf16
     {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(w[i] << 16);
-            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
         Q q;
-        q.h[0] = f16x2_bits(__floats2half2_rn(f[0], f[2]));
-        q.h[1] = f16x2_bits(__floats2half2_rn(f[1], f[3]));
-        q.h[2] = f16x2_bits(__floats2half2_rn(f[4], f[6]));
-        q.h[3] = f16x2_bits(__floats2half2_rn(f[5], f[7]));
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            q.h[i] = f16x2_bits(__floats2half2_rn(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u)));
         return q;
     }
-    // q . code * 2^-8 (partial sums)
+    // q . code (partial sums)
     static __device__ __forceinline__ void dot(const Q &q, const uint2 &k, float &s0, float &s1)
     {
-        fma2_f16_f32(s0, s1, e4m3_even_f16x2(k.x), q.h[0]);
-        fma2_f16_f32(s0, s1, e4m3_odd_f16x2(k.x), q.h[1]);
-        fma2_f16_f32(s0, s1, e4m3_even_f16x2(k.y), q.h[2]);
-        fma2_f16_f32(s0, s1, e4m3_odd_f16x2(k.y), q.h[3]);
+        fma2_f16_f32(s0, s1, e4m3x2_f16x2(k.x), q.h[0]);
+        fma2_f16_f32(s0, s1, e4m3x2_f16x2(k.x >> 16), q.h[1]);
+        fma2_f16_f32(s0, s1, e4m3x2_f16x2(k.y), q.h[2]);
+        fma2_f16_f32(s0, s1, e4m3x2_f16x2(k.y >> 16), q.h[3]);
     }
-    // acc[0..7] += p * code * 2^-8 (p rounded to f16, products in fp32)
+    // acc[0..7] += p * code (p rounded to f16, products in fp32)
     static __device__ __forceinline__ void axpy(float p, const uint2 &v, float *acc)
     {
         const uint32_t pp = f16x2_bits(__float2half2_rn(p));
-        fma2_f16_f32(acc[0], acc[2], e4m3_even_f16x2(v.x), pp);
-        fma2_f16_f32(acc[1], acc[3], e4m3_odd_f16x2(v.x), pp);
-        fma2_f16_f32(acc[4], acc[6], e4m3_even_f16x2(v.y), pp);
-        fma2_f16_f32(acc[5], acc[7], e4m3_odd_f16x2(v.y), pp);
+        fma2_f16_f32(acc[0], acc[1], e4m3x2_f16x2(v.x), pp);
+        fma2_f16_f32(acc[2], acc[3], e4m3x2_f16x2(v.x >> 16), pp);
+        fma2_f16_f32(acc[4], acc[5], e4m3x2_f16x2(v.y), pp);
+        fma2_f16_f32(acc[6], acc[7], e4m3x2_f16x2(v.y >> 16), pp);
     }
     static __device__ __forceinline__ __nv_bfloat16 narrow(float x) { return __float2bfloat16_rn(x); }
     static __device__ __forceinline__ uint4 pack(const float *a, float scale)
@@ -408,7 +391,7 @@ __device__ __forceinline__ bool better(float v, int r, float bv, int br)
 // through its own nbuf shared-memory stages (stage shape SH), reads q and the current token
 // straight into registers, and ends with a warp-shuffle combine.
 template <typename T, int D, int SH>
-__global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const DecodeParams p,
+__global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) decode_kernel(const DecodeParams p,
                                                                           const __grid_constant__ CUtensorMap tmap)
 {
     using C = KCfg<T, D, SH>;
@@ -731,29 +714,34 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
             }
             const unsigned char *st = ws + b * C::STAGE_BYTES;
             const int u0 = j * C::SROWS;
-            const int nv = min(C::SROWS, nrows - u0);  // valid rows of the stage
+            const int nv = min(C::SROWS, nrows - u0);  // valid rows of the stage (>= 1)
+            // Rows past nv (only in an item's last stage) read row 0 of the
+            // stage instead, so every row read holds loaded data; their logit
+            // is -inf and their softmax weight 0.  No branch per row.
             float sc[C::NIT];
 #pragma unroll
             for (int it = 0; it < C::NIT; ++it) {
                 const int row = it * C::RPW + g;
                 const bool valid = row < nv;
+                const Vec *kr = reinterpret_cast<const Vec *>(st + (valid ? row : 0) * C::ROW);
                 float s0 = 0.f, s1 = 0.f;
-                if (valid) {
-                    const Vec *kr = reinterpret_cast<const Vec *>(st + row * C::ROW);
-                    EL::dot(q0, kr[cl], s0, s1);
-                    EL::dot(q1, kr[cl + C::LPR], s0, s1);
-                }
+                EL::dot(q0, kr[cl], s0, s1);
+                EL::dot(q1, kr[cl + C::LPR], s0, s1);
                 float x = s0 + s1;
 #pragma unroll
                 for (int o = C::LPR / 2; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-                x *= xs;
-                sc[it] = valid ? x : -INFINITY;
-                if (p.select && valid && u0 + row >= npre) {
-                    const int k = kr0 + (u0 + row - npre);
-                    const int r = lst[k - klo];
-                    if (better(x, r, minv, minr)) {
-                        minv = x;
-                        minr = r;
+                sc[it] = valid ? x * xs : -INFINITY;
+            }
+            if (p.select) {  // a8: argmin over the stage's attended decode rows
+#pragma unroll
+                for (int it = 0; it < C::NIT; ++it) {
+                    const int row = it * C::RPW + g;
+                    if (row < nv && u0 + row >= npre) {
+                        const int r = lst[kr0 + (u0 + row - npre) - klo];
+                        if (better(sc[it], r, minv, minr)) {
+                            minv = sc[it];
+                            minr = r;
+                        }
                     }
                 }
             }
@@ -772,13 +760,11 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS) decode_kernel(const D
 #pragma unroll
             for (int it = 0; it < C::NIT; ++it) {
                 const int row = it * C::RPW + g;
-                if (row < nv) {
-                    const float pj = ex2(sc[it] - m);
-                    l += pj;
-                    const Vec *vr = reinterpret_cast<const Vec *>(st + row * C::ROW + C::KROW);
-                    EL::axpy(pj, vr[cl], acc);
-                    EL::axpy(pj, vr[cl + C::LPR], acc + C::VEC);
-                }
+                const float pj = ex2(sc[it] - m);  // 0 for rows past nv
+                l += pj;
+                const Vec *vr = reinterpret_cast<const Vec *>(st + (row < nv ? row : 0) * C::ROW + C::KROW);
+                EL::axpy(pj, vr[cl], acc);
+                EL::axpy(pj, vr[cl + C::LPR], acc + C::VEC);
             }
             __syncwarp();
             top_up(con_seq);  // refill the freed buffer

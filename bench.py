@@ -40,8 +40,7 @@ if ROOT not in sys.path:
 METRIC = "sparse decode attn steps/s (batch·layers·heads) and HBM GB/s vs peak @95%"
 UNIT = "stream-steps/s"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["ar_image_gen_gb300/csrc/dsa_decode.cuh", "ar_image_gen_gb300/csrc/dsa_ptx.cuh",
-                  "ar_image_gen_gb300/csrc/dsa_api.cu"]
+KERNEL_SOURCES = ["ar_image_gen_gb300/csrc/dsa_decode.cuh", "ar_image_gen_gb300/csrc/dsa_ptx.cuh"]
 
 
 def code_tokens(src: str) -> str:
@@ -53,8 +52,9 @@ def code_tokens(src: str) -> str:
 
 
 def kernel_source_hash() -> str:
-    """Identity of the decode kernel's code (comments and layout excluded):
-    profile figures stored under profiles/ apply while it is unchanged."""
+    """Identity of the decode kernel's device code (comments and layout
+    excluded): profile figures stored under profiles/ apply while it and the
+    launch plan they were taken with are unchanged."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
@@ -81,9 +81,10 @@ def measured_bf16_tflops() -> float:
         return 1900.0
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, plan=None):
     """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, or None when the kernel changed since the capture."""
+    summary, or None when the kernel's code or the launch plan (pipeline,
+    work items per stream, grid) changed since the capture."""
     path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}.json")
     try:
         with open(path) as f:
@@ -92,6 +93,10 @@ def profiled_traffic(workload: str):
         return None
     if prof.get("kernel_source_hash") != kernel_source_hash():
         return None
+    if plan is not None:
+        for key in ("pipeline", "nsplit", "grid"):
+            if prof.get(key) != getattr(plan, key):
+                return None
     return prof.get("dram_bytes_per_launch")
 
 
@@ -645,7 +650,7 @@ def time_extra(key: str, args, ws: int, peak: float) -> dict:
     return {"workload": workload_config(wl, f"phase-3 steady state from t = {t_start}")["workload"],
             "value": wl.streams * wl.layers * steps * ws / (el_ms / 1e3), "unit": UNIT, "steps": steps,
             "ms_per_step": el_ms / steps, "launch_ms": per_launch_ms, "algo_bytes_per_launch": plan.algo_bytes,
-            "achieved_gbs": achieved, "frac": achieved / peak, "traffic": profiled_traffic(wl.name),
+            "achieved_gbs": achieved, "frac": achieved / peak, "traffic": profiled_traffic(wl.name, plan),
             "pipeline": plan.pipeline, "nsplit": plan.nsplit, "device_status": status}
 
 
@@ -696,7 +701,7 @@ def run_ours(args, rank: int, ws: int) -> dict | None:
     value = stream_steps / (el_ms / 1e3)
     achieved = plan.algo_bytes / (per_launch_ms / 1e3) / 1e9
     whole = plan.algo_bytes * wl.layers * args.steps * ws / (el_ms / 1e3) / 1e9
-    traffic = profiled_traffic(wl.name)
+    traffic = profiled_traffic(wl.name, plan)
 
     # --- the same steady state replayed from a CUDA graph (graph mode: the
     # step lives on the device; one capture of all layers, replayed per step;
