@@ -122,6 +122,8 @@ struct dsa_ctx {
     int *status;
     float *scales;         // FP8 storage: [4, S] K scale, V scale, their fp32 inverses (else NULL)
     int *step_dev;         // graph mode: [0] the step t on the device, [1] CTAs finished (allocated on first use)
+    uint16_t *glist;       // [S, LS] attended relative offsets of the steady state (NULL when nothing is skipped)
+    int LS;
     int graph_mode;
     CUtensorMap ring_map;  // 2-D view of the ring: [S * R rows, 2 * D], one-row box
 };
@@ -341,6 +343,7 @@ void free_ctx(dsa_ctx *h)
     cudaFree(h->status);
     cudaFree(h->scales);
     cudaFree(h->step_dev);
+    cudaFree(h->glist);
     h->magic = 0;
     forget_handle(h);
     delete h;
@@ -626,6 +629,10 @@ int dsa_create_ex(int heads, int head_dim, int L_p, int N_r, int N_att, int sink
     if (rc == DSA_OK) rc = dev_alloc((void **)&h->status, 16, "status word");
     if (rc == DSA_OK && dtype == DSA_FP8_E4M3) rc = dev_alloc((void **)&h->scales, S * 4 * sizeof(float), "FP8 scales");
     if (rc == DSA_OK && dtype == DSA_FP8_E4M3) rc = upload_scales(h, nullptr, nullptr);
+    // The steady state's attended offsets (A per stream): stored at the last
+    // step before it, read afterwards.
+    h->LS = (h->A + 1) & ~1;
+    if (rc == DSA_OK && h->A < h->R) rc = dev_alloc((void **)&h->glist, S * h->LS * sizeof(uint16_t), "offset list");
     if (rc == DSA_OK) rc = ensure_partials(h, max_splits(h));
     if (rc == DSA_OK) rc = encode_ring_map(h);
     if (rc != DSA_OK) {
@@ -711,6 +718,26 @@ int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out)
 
 namespace {
 
+// How a step lists the attended offsets.  From the last step before the
+// steady state on (t' >= R - 1, no more selections) the relative-offset mask
+// never changes, so neither do the attended offsets: that step lists them
+// from the mask and stores them (1), later steps read the stored list (2),
+// provided every item's slice fits the kernel's prefetch registers;
+// otherwise, and before, the mask is scanned (0).
+int list_mode(const dsa_ctx *h, const Plan &pl)
+{
+    if (!h->glist || pl.sinkmode || pl.tin < h->R - 1) return 0;
+    if (pl.tin == h->R - 1) return 1;
+    for (int c = 0; c < pl.nsplit; ++c) {
+        const int lo = c * pl.chunk;
+        const int hi = lo + pl.chunk < pl.n ? lo + pl.chunk : pl.n;
+        const int klo = (lo > pl.P ? lo : pl.P) - pl.P;
+        const int khi = (hi > pl.P ? hi : pl.P) - pl.P;
+        if (khi - (klo & ~1) > dsa::kListSliceMax) return 0;
+    }
+    return 2;
+}
+
 // Host checks of a decode step that come before any launch.
 int check_step(dsa_handle h, const void *q, const void *k_new, const void *v_new, void *out)
 {
@@ -777,6 +804,10 @@ int launch_decode_step(dsa_handle h, const void *q, const void *k_new, const voi
     p.wait_limit = h->wait_limit;
     p.step_dev = h->graph_mode ? h->step_dev : nullptr;
     p.sink = h->sink;
+
+    p.glist = h->glist;
+    p.LS = h->LS;
+    p.list_mode = list_mode(h, pl);
 
     const bool other = note_launch(st, h);
     p.early = (other || after_proj) ? 1 : 0;
@@ -1142,6 +1173,9 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.step_dev = nullptr;
     p.sink = sink;
     p.early = 0;  // caller-owned state: the previous kernel may have written it
+    p.glist = nullptr;  // no stored list: the offsets are listed from the mask every step
+    p.LS = 0;
+    p.list_mode = 0;
     e = launch_step(dtype, head_dim, pl.shape, p, h.ring_map, pl.grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return DSA_OK;

@@ -111,6 +111,10 @@ struct DecodeParams {
     int sink;             // t - t' (graph mode derives t' mod R from [0])
     int early;            // 1: the previous grid in the stream does not write this state, so
                           // the mask, prefix and ring may be read before the grid dependency wait
+    uint16_t *glist;      // [S, LS] attended relative offsets, ascending (steady state), or NULL
+    int LS;               // entries per stream of glist (even)
+    int list_mode;        // 0: list from the mask; 1: list from the mask and store it to glist;
+                          // 2: read the list from glist (the mask no longer changes)
     float qscale;         // log2(e) / sqrt(D), applied to q.k
     const float *kscale;  // [S] FP8 storage: K scale, V scale and their fp32 inverses
     const float *vscale;  //     (NULL for bf16 / fp32 storage)
@@ -325,6 +329,10 @@ struct Elem<__nv_fp8_e4m3> {
 #endif
 
 constexpr int kPipes = 2;      // stage shapes
+constexpr int kMaskRegs = 8;   // mask words (or stored-list pairs) per lane kept in registers
+// Longest slice of the stored offset list one item may read, counted from
+// its first rank rounded down to even: 32 lanes x kMaskRegs pairs.
+constexpr int kListSliceMax = 2 * 32 * kMaskRegs;
 constexpr int kMaxNbuf = 3;    // stages per warp: 2 or 3, per launch (DecodeParams::nbuf)
 // Launch pipelines: shape pi & 1 with 2 + (pi >> 1) stages per warp.
 constexpr int kPipelines = kPipes * (kMaxNbuf - 1);
@@ -356,7 +364,7 @@ struct KCfg {
     static constexpr int SROWS = STAGE_BYTES / ROW;  // entries per stage
     static constexpr int NIT = SROWS / RPW;          // warp instructions per stage
     static constexpr int CHUNK_MAX = Pipe<SH>::CHUNK_MAX;  // decode ranks per work item
-    static constexpr int MAXW = 8;                   // mask words per lane kept in registers
+    static constexpr int MAXW = kMaskRegs;           // mask words per lane kept in registers
     // Shared memory of one warp with nbuf stages: the stages, their barriers
     // (room for kMaxNbuf) and the two item lists; 128-byte aligned.
     static constexpr __host__ __device__ int off_bar(int nbuf) { return nbuf * STAGE_BYTES; }
@@ -422,9 +430,29 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
     const int GW = gridDim.x * C::WARPS;
     const int first_item = blockIdx.x * C::WARPS + warp;
 
+    // The next item's mask words or, when the list is read (list_mode 2),
+    // its slice of the stored list as pairs of offsets: word i of a lane
+    // holds entries (klo & ~1) + 2 (lane + 32 i) + {0, 1} (the host keeps
+    // every slice within 2 * 32 * MAXW entries).
     uint32_t words[C::MAXW];
+    uint32_t w0n = 0;  // list_mode 2: the next item's mask word 0 (bit 0: its current token is skipped)
     auto load_words = [&](int item) {
-        const uint32_t *row = p.mask + (size_t)(item / p.nsplit) * p.MW;
+        const int s = item / p.nsplit;
+        if (p.list_mode == 2) {
+            const int lo = (item - s * p.nsplit) * p.chunk;
+            const int klo = max(lo, p.P) - p.P;
+            const int khi = max(min(lo + p.chunk, p.n), p.P) - p.P;
+            const uint32_t *src = reinterpret_cast<const uint32_t *>(p.glist + (size_t)s * p.LS);
+            const int e0 = klo & ~1;
+#pragma unroll
+            for (int i = 0; i < C::MAXW; ++i) {
+                const int e = e0 + 2 * (lane + 32 * i);
+                words[i] = e < khi ? __ldcg(src + (e >> 1)) : 0u;
+            }
+            w0n = __ldcg(p.mask + (size_t)s * p.MW);
+            return;
+        }
+        const uint32_t *row = p.mask + (size_t)s * p.MW;
 #pragma unroll
         for (int i = 0; i < C::MAXW; ++i) {
             const int w = lane * wpl + i;
@@ -450,7 +478,8 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
     // Graph mode: the step comes from device memory (advanced by the last CTA
     // of the previous launch of this state, which has completed here).
     const int tin_mod = p.step_dev ? (__ldcg(p.step_dev) - p.sink) % p.R : p.tin_mod;
-    if (first_item < p.nitems && inreg && nwords > 0) load_words(first_item);
+    const bool prefetch = p.list_mode == 2 || (inreg && nwords > 0);  // load_words serves the listing
+    if (first_item < p.nitems && prefetch) load_words(first_item);
 
     bool aborted = false;
     int issued = 0, consumed = 0;  // stages issued / consumed by this warp over all its items
@@ -463,24 +492,49 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
     // across item boundaries.  Items are numbered by seq (0, 1, ... for
     // this warp); item seq's offsets are listed in list buffer seq & 1, so
     // the issuer may run at most one item ahead of the consumer.
+    // An item's prompt-only stages need no offsets: they are issued first
+    // (iss_state 1), and the offsets are listed (iss_state 2) when the first
+    // stage with ring rows is due or the consumer reaches the item, so the
+    // listing overlaps the first copies.
     int iss_item = first_item, iss_seq = 0, iss_j = 0;
-    bool iss_ready = false;
-    int I_s = 0, I_lo = 0, I_npre = 0, I_kr0 = 0, I_klo = 0, I_nrows = 0, I_nst = 0;
+    int iss_state = 0;  // 0: not set up; 1: prompt stages may be issued; 2: offsets listed
+    int I_s = 0, I_lo = 0, I_npre = 0, I_kr0 = 0, I_klo = 0, I_khi = 0, I_nrows = 0, I_nst = 0;
     uint32_t self_skip_bits = 0;  // bit (seq & 1): the item's current token is itself skipped
 
-    // a4: list the attended offsets of ranks [klo, khi) of the issuer's item
-    auto setup_item = [&]() {
-        const int item = iss_item;
-        const int s = item / p.nsplit;
-        const int c = item - s * p.nsplit;
-        const int lo = c * p.chunk;
+    auto setup_basic = [&]() {
+        const int s = iss_item / p.nsplit;
+        const int lo = (iss_item - s * p.nsplit) * p.chunk;
         const int hi = min(lo + p.chunk, p.n);
-        const int klo = max(lo, p.P) - p.P;
-        const int khi = max(hi, p.P) - p.P;
+        I_s = s;
+        I_lo = lo;
+        I_klo = max(lo, p.P) - p.P;
+        I_khi = max(hi, p.P) - p.P;
+        I_npre = max(min(hi, p.P) - lo, 0);
+        I_nrows = I_npre;  // until the offsets are listed
+        iss_state = 1;
+    };
+
+    // a4: list the attended offsets of ranks [klo, khi) of the issuer's item
+    auto setup_list = [&]() {
+        const int item = iss_item;
+        const int s = I_s;
+        const int klo = I_klo;
+        const int khi = I_khi;
         uint16_t *lst = list + (iss_seq & 1) * C::CHUNK_MAX;
         const uint32_t *mrow = p.mask + (size_t)s * p.MW;
         bool self_skip = false;
-        if (nwords > 0) {
+        if (p.list_mode == 2) {
+            // the stored list: entries e of the prefetched pairs within [klo, khi)
+            const int e0 = klo & ~1;
+#pragma unroll
+            for (int i = 0; i < C::MAXW; ++i) {
+                const int e = e0 + 2 * (lane + 32 * i);
+                if (e >= klo && e < khi) lst[e - klo] = (uint16_t)(words[i] & 0xffffu);
+                if (e + 1 >= klo && e + 1 < khi) lst[e + 1 - klo] = (uint16_t)(words[i] >> 16);
+            }
+            self_skip = (w0n & 1u) != 0;
+            if (item + GW < p.nitems) load_words(item + GW);  // prefetch for the next item
+        } else if (nwords > 0) {
             int mine = 0;
             if (inreg) {
 #pragma unroll
@@ -540,14 +594,10 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
         __syncwarp();
         const bool has_cur = (klo == 0 && khi > 0 && !self_skip);
         self_skip_bits = (self_skip_bits & ~(1u << (iss_seq & 1))) | ((self_skip ? 1u : 0u) << (iss_seq & 1));
-        I_s = s;
-        I_lo = lo;
-        I_klo = klo;
-        I_npre = max(min(hi, p.P) - lo, 0);
         I_kr0 = has_cur ? klo + 1 : klo;
         I_nrows = I_npre + max(khi - I_kr0, 0);
         I_nst = (I_nrows + C::SROWS - 1) / C::SROWS;
-        iss_ready = true;
+        iss_state = 2;
     };
 
     // a5: issue stage iss_j of the issuer's item into buffer ib (= issued mod nbuf)
@@ -611,18 +661,19 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
     // ahead of the consumer's item con_seq).
     auto issue_next = [&](int con_seq) {
         while (iss_item < p.nitems) {
-            if (!iss_ready) {
+            if (iss_state == 0) {
                 if (iss_seq > con_seq + 1) return;
-                setup_item();
+                setup_basic();
             }
-            if (iss_j < I_nst) {
+            if (iss_state == 1 && (iss_j + 1) * C::SROWS > I_npre) setup_list();  // the stage needs offsets
+            if (iss_state == 1 || iss_j < I_nst) {
                 issue_stage();
                 return;
             }
             iss_item += GW;
             ++iss_seq;
             iss_j = 0;
-            iss_ready = false;
+            iss_state = 0;
         }
     };
 
@@ -650,9 +701,12 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
             iss_item += GW;
             ++iss_seq;
             iss_j = 0;
-            iss_ready = false;
+            iss_state = 0;
         }
-        if (iss_seq == con_seq && !iss_ready) setup_item();
+        if (iss_seq == con_seq && iss_state < 2) {
+            if (iss_state == 0) setup_basic();
+            setup_list();
+        }
         top_up(con_seq);
         const int s = item / p.nsplit;
         const int c = item - s * p.nsplit;
@@ -662,6 +716,10 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
         const int khi = max(hi, p.P) - p.P;
         const bool self_skip = (self_skip_bits >> (con_seq & 1)) & 1u;
         const uint16_t *lst = list + (con_seq & 1) * C::CHUNK_MAX;
+        if (p.list_mode == 1) {  // the last step before the steady state: store the list
+            uint16_t *dst = p.glist + (size_t)s * p.LS + klo;
+            for (int i = lane; i < khi - klo; i += 32) dst[i] = lst[i];
+        }
         const typename EL::Q q0 = EL::load_q(qn0), q1 = EL::load_q(qn1);
         if (item + GW < p.nitems) load_q(item + GW);  // prefetch the next item's q
 
