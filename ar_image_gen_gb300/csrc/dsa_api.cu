@@ -755,7 +755,7 @@ int check_step(dsa_handle h, const void *q, const void *k_new, const void *v_new
 // handle's state and lets its dependents start only after the kernel before
 // it has completed, so the state may be read before the grid dependency wait.
 int launch_decode_step(dsa_handle h, const void *q, const void *k_new, const void *v_new, void *out,
-                       cudaStream_t st, bool after_proj)
+                       cudaStream_t st, bool after_proj, int kvstride = 0, bool appended = false)
 {
     const Plan pl = make_plan(h, h->t);
     if ((long long)pl.nsplit * h->S > INT_MAX) return fail(DSA_ERR_ARG, "grid too large");
@@ -808,6 +808,8 @@ int launch_decode_step(dsa_handle h, const void *q, const void *k_new, const voi
     p.glist = h->glist;
     p.LS = h->LS;
     p.list_mode = list_mode(h, pl);
+    p.kvstride = kvstride > 0 ? kvstride : h->D;
+    p.appended = appended ? 1 : 0;
 
     const bool other = note_launch(st, h);
     p.early = (other || after_proj) ? 1 : 0;
@@ -844,8 +846,30 @@ int dsa_decode_step_fused(dsa_handle h, dsa_proj pr, const void *x, const void *
     dsa_detail::proj_staging(pr, &q, &k, &v);
     rc = check_step(h, q, k, v, out);
     if (rc != DSA_OK) return rc;
+    if (h->graph_mode)
+        return fail(DSA_ERR_STATE, "dsa_decode_step_fused takes host-counted steps: switch graph mode off first");
     if ((long long)h->L_p + h->t > INT_MAX) return fail(DSA_ERR_STATE, "position out of range");
     cudaStream_t st = (cudaStream_t)stream;
+    if (h->dtype == DSA_BF16) {
+        // The projection's epilogue writes k and v of the newest token straight
+        // into the slot it takes at this step (ring slot t' mod R, or prefix
+        // row L_p + t during the sink fill), K row then V row of each entry;
+        // the decode kernel reads them there and appends nothing.
+        const size_t row = 2 * (size_t)h->D;  // elements of a K|V entry
+        __nv_bfloat16 *kdst;
+        long long stride;
+        if (h->t < h->sink) {
+            kdst = static_cast<__nv_bfloat16 *>(h->prefix) + (size_t)(h->L_p + h->t) * row;
+            stride = (long long)h->Lcap * row;
+        } else {
+            kdst = static_cast<__nv_bfloat16 *>(h->ring) + (size_t)((h->t - h->sink) % h->R) * row;
+            stride = (long long)h->R * row;
+        }
+        if (stride > INT_MAX) return fail(DSA_ERR_ARG, "decode state rows too long for the fused step");
+        rc = dsa_detail::proj_launch(pr, x, W, h->L_p + h->t, q, kdst, kdst + h->D, st, (int)stride, (int)stride);
+        if (rc != DSA_OK) return rc;
+        return launch_decode_step(h, q, kdst, kdst + h->D, out, st, true, (int)stride, true);
+    }
     rc = dsa_detail::proj_launch(pr, x, W, h->L_p + h->t, q, k, v, st);
     if (rc != DSA_OK) return rc;
     return launch_decode_step(h, q, k, v, out, st, true);
@@ -1176,6 +1200,8 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.glist = nullptr;  // no stored list: the offsets are listed from the mask every step
     p.LS = 0;
     p.list_mode = 0;
+    p.kvstride = head_dim;
+    p.appended = 0;
     e = launch_step(dtype, head_dim, pl.shape, p, h.ring_map, pl.grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return DSA_OK;

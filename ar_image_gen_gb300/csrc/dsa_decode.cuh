@@ -8,7 +8,9 @@
 // item, one warp performs:
 //   a2  append: the current token, read into registers, is stored to ring
 //       slot t' mod R (the slot of the entry evicted at this step) or,
-//       during the sink fill, to prefix row L_p + t;
+//       during the sink fill, to prefix row L_p + t (in the fused layer step
+//       with bf16 storage the projection has written it there already, and
+//       the kernel reads it from that slot);
 //   a4  index set: the attended relative offsets r in [0, min(t'+1, R)) whose
 //       skip bit is clear, listed by a warp scan over the mask words;
 //   a5  gather + logits: the prompt rows (bulk copies) and the attended ring
@@ -115,6 +117,8 @@ struct DecodeParams {
     int LS;               // entries per stream of glist (even)
     int list_mode;        // 0: list from the mask; 1: list from the mask and store it to glist;
                           // 2: read the list from glist (the mask no longer changes)
+    int kvstride;         // elements between streams' rows of knew / vnew (D for [S, D] inputs)
+    int appended;         // 1: knew / vnew already are the current token's stored rows (its slot): no append
     float qscale;         // log2(e) / sqrt(D), applied to q.k
     const float *kscale;  // [S] FP8 storage: K scale, V scale and their fp32 inverses
     const float *vscale;  //     (NULL for bf16 / fp32 storage)
@@ -731,15 +735,15 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
         const float kinv = EL::SCALED ? __ldg(p.kinv + s) : 1.f;
         const float vinv = EL::SCALED ? __ldg(p.vinv + s) : 1.f;
         const float xs = EL::SCALED ? p.qscale * (__ldg(p.kscale + s) * EL::kWiden) : p.qscale;
-        const IO *kio = reinterpret_cast<const IO *>(p.knew) + (size_t)s * D;
-        const IO *vio = reinterpret_cast<const IO *>(p.vnew) + (size_t)s * D;
+        const IO *kio = reinterpret_cast<const IO *>(p.knew) + (size_t)s * p.kvstride;
+        const IO *vio = reinterpret_cast<const IO *>(p.vnew) + (size_t)s * p.kvstride;
         Vec kc0, kc1, vc0, vc1;
         if (has_cur) {  // the current token goes straight to registers, in its stored form
             kc0 = EL::load_kv(kio, cl, kinv);
             kc1 = EL::load_kv(kio, cl + C::LPR, kinv);
             vc0 = EL::load_kv(vio, cl, vinv);
             vc1 = EL::load_kv(vio, cl + C::LPR, vinv);
-        } else if (self_skip && c == 0) {
+        } else if (self_skip && c == 0 && !p.appended) {
             // a2 for a token that is not attended: it is in no stage; store it.
             constexpr int NV = D / C::VEC;
             Vec *dst = reinterpret_cast<Vec *>(cur_dst);
@@ -854,11 +858,13 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
                 l += pj;
                 EL::axpy(pj, vc0, acc);
                 EL::axpy(pj, vc1, acc + C::VEC);
-                Vec *dst = reinterpret_cast<Vec *>(cur_dst);
-                dst[cl] = kc0;
-                dst[cl + C::LPR] = kc1;
-                dst[2 * C::LPR + cl] = vc0;
-                dst[3 * C::LPR + cl] = vc1;
+                if (!p.appended) {
+                    Vec *dst = reinterpret_cast<Vec *>(cur_dst);
+                    dst[cl] = kc0;
+                    dst[cl + C::LPR] = kc1;
+                    dst[2 * C::LPR + cl] = vc0;
+                    dst[3 * C::LPR + cl] = vc1;
+                }
             }
         }
 

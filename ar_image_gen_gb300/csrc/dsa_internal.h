@@ -23,10 +23,13 @@ __attribute__((visibility("hidden"))) int dev_alloc(void **p, size_t bytes, cons
 __attribute__((visibility("hidden"))) bool note_launch(cudaStream_t st, const void *handle);
 __attribute__((visibility("hidden"))) void forget_handle(const void *handle);
 
-// The QKV projection (dsa_proj.cu) as the fused decode step uses it.
+// The QKV projection (dsa_proj.cu) as the fused decode step uses it.  k and
+// v rows of stream s are written at k + s * kstride and v + s * vstride
+// (elements; 0: head_dim, i.e. [batch * heads, head_dim] tensors).
 __attribute__((visibility("hidden"))) int proj_shape(const dsa_proj_ctx *p, int *batch, int *heads, int *head_dim);
 __attribute__((visibility("hidden"))) void proj_staging(const dsa_proj_ctx *p, void **q, void **k, void **v);
 __attribute__((visibility("hidden"))) int proj_launch(dsa_proj_ctx *p, const void *x, const void *W, int pos, void *q,
-                                                      void *k, void *v, cudaStream_t st);
+                                                      void *k, void *v, cudaStream_t st, int kstride = 0,
+                                                      int vstride = 0);
 
 }  // namespace dsa_detail

@@ -63,11 +63,15 @@ constexpr int kExtraBars = 4;            // acc_full, acc_empty, drain, red_full
 constexpr uint32_t kBulkPiece = 32768;  // bytes per bulk copy of a partial
 
 struct ProjParams {
-    __nv_bfloat16 *q, *k, *v;  // [B, HD] each
+    // Row of stream s = b * H + h of q, k, v: q + s * D, k + s * kstride,
+    // v + s * vstride (a stride of D: [B, HD] tensors; the fused decode step
+    // points k and v at the decode state's slot of the newest token instead).
+    __nv_bfloat16 *q, *k, *v;
+    int kstride, vstride;
     float *part;               // [grid][npad / 16][4][128] float4 partials of shared tiles
     int *counters;             // [tiles] published pieces per shared tile
     int *status;
-    int B, npad, HD, D, tiles, kblocks, stages, tmem_cols;
+    int B, H, npad, HD, D, tiles, kblocks, stages, tmem_cols;
     int pos;
     uint32_t wait_limit;
     double inv_freq[64];       // 10000^(-2j/D), j < D/2
@@ -187,8 +191,8 @@ __device__ __forceinline__ void rope_cs(int pos, double inv_freq, float &c, floa
 // one row as one 16-byte vector.  The 128 threads of one epilogue group
 // (gt = 0..127, named barrier `bar`) call it together.
 __device__ __forceinline__ void finish_cols(float (&y)[32], int ncol, int c0, int f, int gt, uint32_t bar, bool rope,
-                                            bool upper, float cs, float sn, __nv_bfloat16 *xch, __nv_bfloat16 *dst,
-                                            const ProjParams &p)
+                                            bool upper, float cs, float sn, __nv_bfloat16 *xch, __nv_bfloat16 *base,
+                                            int stride, int f0, const ProjParams &p)
 {
     if (rope) {
 #pragma unroll
@@ -204,10 +208,12 @@ __device__ __forceinline__ void finish_cols(float (&y)[32], int ncol, int c0, in
         if (j < ncol) xch[j * kBM + f] = __float2bfloat16_rn(y[j]);
     named_bar_sync(bar, kGroupThreads);
     const int g = gt & 15, r = gt >> 4;  // 8 features [8 g, 8 g + 8) of rows r, r + 8, ...
+    const int fe = f0 + 8 * g;            // feature fe of token b: element fe % D of stream b * H + fe / D
+    __nv_bfloat16 *const dst = base + (size_t)(fe / p.D) * stride + fe % p.D;
     for (int j = r; j < ncol; j += 8) {
         const int b = c0 + j;
         if (b < p.B)
-            *reinterpret_cast<uint4 *>(dst + (size_t)b * p.HD + 8 * g) =
+            *reinterpret_cast<uint4 *>(dst + (size_t)b * p.H * stride) =
                 *reinterpret_cast<const uint4 *>(xch + j * kBM + 8 * g);
     }
     named_bar_sync(bar, kGroupThreads);  // xch is rewritten by the next call
@@ -274,7 +280,8 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
         const int part = sg.tile * kBM / p.HD;
         const int f0 = sg.tile * kBM - part * p.HD;
         const bool rope = part < 2;
-        __nv_bfloat16 *dst = (part == 0 ? p.q : (part == 1 ? p.k : p.v)) + f0;
+        __nv_bfloat16 *const dbase = part == 0 ? p.q : (part == 1 ? p.k : p.v);
+        const int dstride = part == 0 ? p.D : (part == 1 ? p.kstride : p.vstride);
         float cs = 1.f, sn = 0.f;
         if (rope) rope_cs(p.pos, p.inv_freq[jr], cs, sn);
         // One thread waits; the others learn the outcome at the barrier.
@@ -366,7 +373,7 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
                 for (int i = 0; i < 8; ++i)
                     if (4 * i < ncol) add4(y, i, v[i]);
             }
-            finish_cols(y, ncol, c0, f, gt, gbar, rope, upper, cs, sn, xch, dst, p);
+            finish_cols(y, ncol, c0, f, gt, gbar, rope, upper, cs, sn, xch, dbase, dstride, f0, p);
         });
         named_bar_sync(kEpiBar, kEpiThreads);  // both groups are done with this piece
         if (nother > 0 && et == 0) atomicExch(p.counters + sg.tile, 0);
@@ -658,7 +665,8 @@ void proj_staging(const dsa_proj_ctx *p, void **q, void **k, void **v)
     *v = p->staging + 2 * n;
 }
 
-int proj_launch(dsa_proj_ctx *pr, const void *x, const void *W, int pos, void *q, void *k, void *v, cudaStream_t st)
+int proj_launch(dsa_proj_ctx *pr, const void *x, const void *W, int pos, void *q, void *k, void *v, cudaStream_t st,
+                int kstride, int vstride)
 {
     if (!valid(pr)) return fail(DSA_ERR_STATE, "invalid projection context");
     if (!x || !W || !q || !k || !v) return fail(DSA_ERR_ARG, "x, W, q, k and v must be non-NULL");
@@ -674,6 +682,9 @@ int proj_launch(dsa_proj_ctx *pr, const void *x, const void *W, int pos, void *q
     p.q = static_cast<__nv_bfloat16 *>(q);
     p.k = static_cast<__nv_bfloat16 *>(k);
     p.v = static_cast<__nv_bfloat16 *>(v);
+    p.kstride = kstride > 0 ? kstride : pr->D;
+    p.vstride = vstride > 0 ? vstride : pr->D;
+    p.H = pr->H;
     p.part = pr->part;
     p.counters = pr->counters;
     p.status = pr->status;

@@ -78,13 +78,20 @@ int dsa_qkv_rope(dsa_proj p, const void *x, const void *W, int pos, void *q, voi
 /*
  * dsa_decode_step_fused -- one decode step of handle h whose q, k_new and
  * v_new come from the projection of x by W at position L_p + t (t = h's
- * step counter): the projection kernel writes them to p's staging buffers
- * and the decode kernel (dsa_decode_step) reads them there.
+ * step counter).  The projection kernel writes q to p's staging buffer and,
+ * for a DSA_BF16 handle, k_new and v_new straight into the decode state at
+ * the slot the newest token takes at this step (its ring slot, or its
+ * prefix row during the sink fill), where the decode kernel reads them and
+ * appends nothing; for a DSA_FP8_E4M3 handle (whose state holds E4M3 codes)
+ * they go to p's staging buffers and the decode kernel stores them.  The
+ * results equal dsa_qkv_rope followed by dsa_decode_step bit for bit.
  *
  * h must be a DSA_BF16 or DSA_FP8_E4M3 handle with heads = batch * heads of
- * p and the same head_dim.  x, W, out as in dsa_qkv_rope / dsa_decode_step.
- * Asynchronous on `stream`; advances t.  Errors: as dsa_decode_step and
- * dsa_qkv_rope, DSA_ERR_ARG when h and p do not match.
+ * p and the same head_dim, not in graph mode (the position and the slot are
+ * taken from the host's step counter).  x, W, out as in dsa_qkv_rope /
+ * dsa_decode_step.  Asynchronous on `stream`; advances t.  Errors: as
+ * dsa_decode_step and dsa_qkv_rope, DSA_ERR_ARG when h and p do not match,
+ * DSA_ERR_STATE in graph mode.
  */
 int dsa_decode_step_fused(dsa_handle h, dsa_proj p, const void *x, const void *W, void *out, void *stream);
 

@@ -122,10 +122,12 @@ def test_timeout_is_reported_and_the_context_recovers():
 
 def run_fused(wl: Workload, hidden: int, steps: int, sample, kv_scales=None):
     """Steps a fused handle (projection + decode) and a twin handle fed with
-    dsa_qkv_rope's outputs; checks the two agree bit for bit, the projection
-    against its oracle, and the sampled streams' attention against the decode
-    oracle (outputs within tolerance, selections and skip masks exact up to
-    accepted near ties)."""
+    dsa_qkv_rope's outputs; checks the two agree bit for bit (outputs,
+    selections, and the stored prefix and ring: with bf16 storage the fused
+    step's projection writes the newest token into its slot itself), the
+    projection against its oracle, and the sampled streams' attention
+    against the decode oracle (outputs within tolerance, selections and skip
+    masks exact up to accepted near ties)."""
     from ar_image_gen_gb300.dsa import DSA, DSA_OK, Proj
 
     gen = ProjGen(wl, device="cuda", hidden=hidden)
@@ -162,6 +164,9 @@ def run_fused(wl: Workload, hidden: int, steps: int, sample, kv_scales=None):
         assert torch.equal(out_f, out_t), f"fused and two-call outputs differ at t={t}"
         sel_f, sel_t = fused.last_selection(), twin.last_selection()
         assert np.array_equal(sel_f, sel_t)
+        if (S <= 64 and t % 25 == 24) or t == steps - 1:
+            for a, b in zip(fused.copy_state(), twin.copy_state()):
+                assert np.array_equal(a, b), f"stored state differs at t={t}"
         if t % 16 == 0 or t == steps - 1:
             ref = oracle_qkv_rope(x.double().cpu().numpy(), Wd, wl.heads, d, pos)
             for g, r in zip((q, k, v), ref):
@@ -223,3 +228,32 @@ def test_fused_step_lumina_b32_through_phase3():
     (2100 steps), fused vs two-call bit-exact and sampled oracle parity."""
     wl = Workload("lumina-s95-b32", 1, 32, 128, "bf16", 64, 64, 2048, 205, 0, 32, 20260920)
     assert run_fused(wl, hidden=4096, steps=2100, sample=list(range(0, 1024, 171))) > 0
+
+
+def test_fused_step_refuses_graph_mode():
+    """The fused step counts steps on the host (the projection's position and
+    the newest token's slot come from it), so a handle in graph mode is
+    refused before anything is launched."""
+    from ar_image_gen_gb300.dsa import DSA, DSA_ERR_STATE, DSAError, Proj
+
+    wl = wl_for(2, 128, 1, L_p=8, N_r=12, N_att=4, grid=5)
+    S, d = wl.streams, wl.head_dim
+    h = DSA(S, d, wl.L_p, wl.N_r, wl.N_att, 0, "bf16")
+    pr = Proj(wl.batch, wl.heads, d, 128)
+    K = torch.zeros((S, wl.L_p, d), dtype=torch.bfloat16, device="cuda")
+    h.prefill(K, K)
+    q = torch.zeros((S, d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    for _ in range(wl.N_r):
+        h.decode_step(q, q, q, out)
+    h.set_graph_mode(True)
+    x = torch.zeros((wl.batch, 128), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((3 * wl.heads * d, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(DSAError) as e:
+        h.decode_step_fused(pr, x, W, out)
+    assert e.value.code == DSA_ERR_STATE
+    h.sync_step()
+    h.set_graph_mode(False)
+    assert h.sync_status() == 0
+    h.close()
+    pr.close()
