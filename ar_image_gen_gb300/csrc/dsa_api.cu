@@ -755,7 +755,7 @@ int check_step(dsa_handle h, const void *q, const void *k_new, const void *v_new
 // handle's state and lets its dependents start only after the kernel before
 // it has completed, so the state may be read before the grid dependency wait.
 int launch_decode_step(dsa_handle h, const void *q, const void *k_new, const void *v_new, void *out,
-                       cudaStream_t st, bool after_proj, int kvstride = 0, bool appended = false)
+                       cudaStream_t st, bool after_proj, bool appended = false)
 {
     const Plan pl = make_plan(h, h->t);
     if ((long long)pl.nsplit * h->S > INT_MAX) return fail(DSA_ERR_ARG, "grid too large");
@@ -808,7 +808,6 @@ int launch_decode_step(dsa_handle h, const void *q, const void *k_new, const voi
     p.glist = h->glist;
     p.LS = h->LS;
     p.list_mode = list_mode(h, pl);
-    p.kvstride = kvstride > 0 ? kvstride : h->D;
     p.appended = appended ? 1 : 0;
 
     const bool other = note_launch(st, h);
@@ -842,37 +841,36 @@ int dsa_decode_step_fused(dsa_handle h, dsa_proj pr, const void *x, const void *
     if ((long long)batch * heads != h->S || hd != h->D)
         return fail(DSA_ERR_ARG, "handle (%d streams of %d) and projection (%d x %d heads of %d) do not match", h->S,
                     h->D, batch, heads, hd);
-    void *q = nullptr, *k = nullptr, *v = nullptr;
-    dsa_detail::proj_staging(pr, &q, &k, &v);
-    rc = check_step(h, q, k, v, out);
+    void *q = nullptr;  // k_new and v_new are written to the decode state (below)
+    dsa_detail::proj_staging(pr, &q);
+    rc = check_step(h, q, q, q, out);
     if (rc != DSA_OK) return rc;
     if (h->graph_mode)
         return fail(DSA_ERR_STATE, "dsa_decode_step_fused takes host-counted steps: switch graph mode off first");
     if ((long long)h->L_p + h->t > INT_MAX) return fail(DSA_ERR_STATE, "position out of range");
     cudaStream_t st = (cudaStream_t)stream;
-    if (h->dtype == DSA_BF16) {
-        // The projection's epilogue writes k and v of the newest token straight
-        // into the slot it takes at this step (ring slot t' mod R, or prefix
-        // row L_p + t during the sink fill), K row then V row of each entry;
-        // the decode kernel reads them there and appends nothing.
-        const size_t row = 2 * (size_t)h->D;  // elements of a K|V entry
-        __nv_bfloat16 *kdst;
-        long long stride;
-        if (h->t < h->sink) {
-            kdst = static_cast<__nv_bfloat16 *>(h->prefix) + (size_t)(h->L_p + h->t) * row;
-            stride = (long long)h->Lcap * row;
-        } else {
-            kdst = static_cast<__nv_bfloat16 *>(h->ring) + (size_t)((h->t - h->sink) % h->R) * row;
-            stride = (long long)h->R * row;
-        }
-        if (stride > INT_MAX) return fail(DSA_ERR_ARG, "decode state rows too long for the fused step");
-        rc = dsa_detail::proj_launch(pr, x, W, h->L_p + h->t, q, kdst, kdst + h->D, st, (int)stride, (int)stride);
-        if (rc != DSA_OK) return rc;
-        return launch_decode_step(h, q, kdst, kdst + h->D, out, st, true, (int)stride, true);
+    // The projection's epilogue writes k and v of the newest token straight
+    // into the slot it takes at this step (ring slot t' mod R, or prefix row
+    // L_p + t during the sink fill), K row then V row of each entry, in the
+    // stored form (E4M3 codes with the stream's inverse scales for FP8
+    // storage); the decode kernel reads them there and appends nothing.
+    const size_t row = 2 * (size_t)h->D * elem_bytes(h->dtype);  // bytes of a K|V entry
+    unsigned char *kdst;
+    long long stride;  // bytes (= elements) between streams' entries, in stored elements
+    if (h->t < h->sink) {
+        kdst = static_cast<unsigned char *>(h->prefix) + (size_t)(h->L_p + h->t) * row;
+        stride = (long long)h->Lcap * 2 * h->D;
+    } else {
+        kdst = static_cast<unsigned char *>(h->ring) + (size_t)((h->t - h->sink) % h->R) * row;
+        stride = (long long)h->R * 2 * h->D;
     }
-    rc = dsa_detail::proj_launch(pr, x, W, h->L_p + h->t, q, k, v, st);
+    if (stride > INT_MAX) return fail(DSA_ERR_ARG, "decode state rows too long for the fused step");
+    unsigned char *vdst = kdst + (size_t)h->D * elem_bytes(h->dtype);
+    const float *kinv = h->scales ? h->scales + 2 * (size_t)h->S : nullptr;
+    const float *vinv = h->scales ? h->scales + 3 * (size_t)h->S : nullptr;
+    rc = dsa_detail::proj_launch(pr, x, W, h->L_p + h->t, q, kdst, vdst, st, (int)stride, (int)stride, kinv, vinv);
     if (rc != DSA_OK) return rc;
-    return launch_decode_step(h, q, k, v, out, st, true);
+    return launch_decode_step(h, q, kdst, vdst, out, st, true, true);
 }
 
 int dsa_get_step(dsa_handle h, int *t)
@@ -1200,7 +1198,6 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.glist = nullptr;  // no stored list: the offsets are listed from the mask every step
     p.LS = 0;
     p.list_mode = 0;
-    p.kvstride = head_dim;
     p.appended = 0;
     e = launch_step(dtype, head_dim, pl.shape, p, h.ring_map, pl.grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");

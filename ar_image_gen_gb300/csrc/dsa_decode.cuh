@@ -9,8 +9,8 @@
 //   a2  append: the current token, read into registers, is stored to ring
 //       slot t' mod R (the slot of the entry evicted at this step) or,
 //       during the sink fill, to prefix row L_p + t (in the fused layer step
-//       with bf16 storage the projection has written it there already, and
-//       the kernel reads it from that slot);
+//       the projection has stored it there already, and the kernel reads it
+//       from that slot);
 //   a4  index set: the attended relative offsets r in [0, min(t'+1, R)) whose
 //       skip bit is clear, listed by a warp scan over the mask words;
 //   a5  gather + logits: the prompt rows (bulk copies) and the attended ring
@@ -117,8 +117,7 @@ struct DecodeParams {
     int LS;               // entries per stream of glist (even)
     int list_mode;        // 0: list from the mask; 1: list from the mask and store it to glist;
                           // 2: read the list from glist (the mask no longer changes)
-    int kvstride;         // elements between streams' rows of knew / vnew (D for [S, D] inputs)
-    int appended;         // 1: knew / vnew already are the current token's stored rows (its slot): no append
+    int appended;         // 1: the current token is already stored in its slot (read there, no append)
     float qscale;         // log2(e) / sqrt(D), applied to q.k
     const float *kscale;  // [S] FP8 storage: K scale, V scale and their fp32 inverses
     const float *vscale;  //     (NULL for bf16 / fp32 storage)
@@ -265,6 +264,20 @@ __device__ __forceinline__ void fma2_f16_f32(float &acc0, float &acc1, uint32_t 
         : "r"(a), "r"(b));
 }
 
+// E4M3 codes of 8 bf16 elements (x holds them as pairs, element 0 in the low
+// half of x.x): each is the code nearest to fp32(element) * inv, satfinite.
+__device__ __forceinline__ uint2 e4m3_codes(const uint4 &x, float inv)
+{
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = make_float2(__uint_as_float(w[i] << 16) * inv, __uint_as_float(w[i] & 0xffff0000u) * inv);
+        c[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
 template <>
 struct Elem<__nv_fp8_e4m3> {
     using IO = __nv_bfloat16;
@@ -307,15 +320,7 @@ struct Elem<__nv_fp8_e4m3> {
     // Codes of the 8 bf16 elements of vector `vec` of an input row.
     static __device__ __forceinline__ Vec load_kv(const IO *row, int vec, float inv)
     {
-        const uint4 x = __ldg(reinterpret_cast<const uint4 *>(row) + vec);
-        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-        uint32_t c[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = make_float2(__uint_as_float(w[i] << 16) * inv, __uint_as_float(w[i] & 0xffff0000u) * inv);
-            c[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
-        }
-        return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+        return e4m3_codes(__ldg(reinterpret_cast<const uint4 *>(row) + vec), inv);
     }
 };
 
@@ -735,10 +740,16 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
         const float kinv = EL::SCALED ? __ldg(p.kinv + s) : 1.f;
         const float vinv = EL::SCALED ? __ldg(p.vinv + s) : 1.f;
         const float xs = EL::SCALED ? p.qscale * (__ldg(p.kscale + s) * EL::kWiden) : p.qscale;
-        const IO *kio = reinterpret_cast<const IO *>(p.knew) + (size_t)s * p.kvstride;
-        const IO *vio = reinterpret_cast<const IO *>(p.vnew) + (size_t)s * p.kvstride;
+        const IO *kio = reinterpret_cast<const IO *>(p.knew) + (size_t)s * D;
+        const IO *vio = reinterpret_cast<const IO *>(p.vnew) + (size_t)s * D;
         Vec kc0, kc1, vc0, vc1;
-        if (has_cur) {  // the current token goes straight to registers, in its stored form
+        if (has_cur && p.appended) {  // already stored in its slot (fused step): read its stored form there
+            const Vec *cur = reinterpret_cast<const Vec *>(cur_dst);
+            kc0 = cur[cl];
+            kc1 = cur[cl + C::LPR];
+            vc0 = cur[2 * C::LPR + cl];
+            vc1 = cur[3 * C::LPR + cl];
+        } else if (has_cur) {  // the current token goes straight to registers, in its stored form
             kc0 = EL::load_kv(kio, cl, kinv);
             kc1 = EL::load_kv(kio, cl + C::LPR, kinv);
             vc0 = EL::load_kv(vio, cl, vinv);

@@ -25,11 +25,13 @@ __attribute__((visibility("hidden"))) void forget_handle(const void *handle);
 
 // The QKV projection (dsa_proj.cu) as the fused decode step uses it.  k and
 // v rows of stream s are written at k + s * kstride and v + s * vstride
-// (elements; 0: head_dim, i.e. [batch * heads, head_dim] tensors).
+// (elements; 0: head_dim, i.e. [batch * heads, head_dim] tensors), as bf16,
+// or as E4M3 codes of fp32(value) * kinv[s] (vinv[s]) when those are given.
 __attribute__((visibility("hidden"))) int proj_shape(const dsa_proj_ctx *p, int *batch, int *heads, int *head_dim);
-__attribute__((visibility("hidden"))) void proj_staging(const dsa_proj_ctx *p, void **q, void **k, void **v);
+__attribute__((visibility("hidden"))) void proj_staging(const dsa_proj_ctx *p, void **q);
 __attribute__((visibility("hidden"))) int proj_launch(dsa_proj_ctx *p, const void *x, const void *W, int pos, void *q,
                                                       void *k, void *v, cudaStream_t st, int kstride = 0,
-                                                      int vstride = 0);
+                                                      int vstride = 0, const float *kinv = nullptr,
+                                                      const float *vinv = nullptr);
 
 }  // namespace dsa_detail

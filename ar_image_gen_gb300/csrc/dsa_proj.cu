@@ -64,10 +64,13 @@ constexpr uint32_t kBulkPiece = 32768;  // bytes per bulk copy of a partial
 
 struct ProjParams {
     // Row of stream s = b * H + h of q, k, v: q + s * D, k + s * kstride,
-    // v + s * vstride (a stride of D: [B, HD] tensors; the fused decode step
-    // points k and v at the decode state's slot of the newest token instead).
+    // v + s * vstride elements (a stride of D: [B, HD] tensors; the fused
+    // decode step points k and v at the decode state's slot of the newest
+    // token instead).  With kinv / vinv set, k and v are stored as E4M3 codes
+    // (one byte each) of fp32(value) * inv[s] instead of bf16.
     __nv_bfloat16 *q, *k, *v;
     int kstride, vstride;
+    const float *kinv, *vinv;
     float *part;               // [grid][npad / 16][4][128] float4 partials of shared tiles
     int *counters;             // [tiles] published pieces per shared tile
     int *status;
@@ -192,7 +195,7 @@ __device__ __forceinline__ void rope_cs(int pos, double inv_freq, float &c, floa
 // (gt = 0..127, named barrier `bar`) call it together.
 __device__ __forceinline__ void finish_cols(float (&y)[32], int ncol, int c0, int f, int gt, uint32_t bar, bool rope,
                                             bool upper, float cs, float sn, __nv_bfloat16 *xch, __nv_bfloat16 *base,
-                                            int stride, int f0, const ProjParams &p)
+                                            int stride, int f0, const float *inv, const ProjParams &p)
 {
     if (rope) {
 #pragma unroll
@@ -209,12 +212,18 @@ __device__ __forceinline__ void finish_cols(float (&y)[32], int ncol, int c0, in
     named_bar_sync(bar, kGroupThreads);
     const int g = gt & 15, r = gt >> 4;  // 8 features [8 g, 8 g + 8) of rows r, r + 8, ...
     const int fe = f0 + 8 * g;            // feature fe of token b: element fe % D of stream b * H + fe / D
-    __nv_bfloat16 *const dst = base + (size_t)(fe / p.D) * stride + fe % p.D;
+    const size_t off = (size_t)(fe / p.D) * stride + fe % p.D;
     for (int j = r; j < ncol; j += 8) {
         const int b = c0 + j;
-        if (b < p.B)
-            *reinterpret_cast<uint4 *>(dst + (size_t)b * p.H * stride) =
-                *reinterpret_cast<const uint4 *>(xch + j * kBM + 8 * g);
+        if (b >= p.B) continue;
+        const uint4 x = *reinterpret_cast<const uint4 *>(xch + j * kBM + 8 * g);
+        if (inv) {  // E4M3 codes of the bf16 values, as the decode state stores them
+            const size_t sidx = (size_t)b * p.H + fe / p.D;
+            *reinterpret_cast<uint2 *>(reinterpret_cast<unsigned char *>(base) + (size_t)b * p.H * stride + off) =
+                e4m3_codes(x, __ldg(inv + sidx));
+        } else {
+            *reinterpret_cast<uint4 *>(base + (size_t)b * p.H * stride + off) = x;
+        }
     }
     named_bar_sync(bar, kGroupThreads);  // xch is rewritten by the next call
 }
@@ -282,6 +291,7 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
         const bool rope = part < 2;
         __nv_bfloat16 *const dbase = part == 0 ? p.q : (part == 1 ? p.k : p.v);
         const int dstride = part == 0 ? p.D : (part == 1 ? p.kstride : p.vstride);
+        const float *dinv = part == 0 ? nullptr : (part == 1 ? p.kinv : p.vinv);
         float cs = 1.f, sn = 0.f;
         if (rope) rope_cs(p.pos, p.inv_freq[jr], cs, sn);
         // One thread waits; the others learn the outcome at the barrier.
@@ -373,7 +383,7 @@ __device__ __forceinline__ void epilogue(const ProjParams &p, int c, int U, int 
                 for (int i = 0; i < 8; ++i)
                     if (4 * i < ncol) add4(y, i, v[i]);
             }
-            finish_cols(y, ncol, c0, f, gt, gbar, rope, upper, cs, sn, xch, dbase, dstride, f0, p);
+            finish_cols(y, ncol, c0, f, gt, gbar, rope, upper, cs, sn, xch, dbase, dstride, f0, dinv, p);
         });
         named_bar_sync(kEpiBar, kEpiThreads);  // both groups are done with this piece
         if (nother > 0 && et == 0) atomicExch(p.counters + sg.tile, 0);
@@ -624,7 +634,7 @@ struct dsa_proj_ctx {
     float *part;
     int *counters;
     int *status;
-    __nv_bfloat16 *staging;  // [3][B * HD]: q, k, v of dsa_decode_step_fused
+    __nv_bfloat16 *staging;  // [B * HD]: q of dsa_decode_step_fused (k and v go to the decode state)
     uint32_t wait_limit;
     double inv_freq[64];
 };
@@ -657,16 +667,10 @@ int proj_shape(const dsa_proj_ctx *p, int *batch, int *heads, int *head_dim)
     return DSA_OK;
 }
 
-void proj_staging(const dsa_proj_ctx *p, void **q, void **k, void **v)
-{
-    const size_t n = (size_t)p->B * p->HD;
-    *q = p->staging;
-    *k = p->staging + n;
-    *v = p->staging + 2 * n;
-}
+void proj_staging(const dsa_proj_ctx *p, void **q) { *q = p->staging; }
 
 int proj_launch(dsa_proj_ctx *pr, const void *x, const void *W, int pos, void *q, void *k, void *v, cudaStream_t st,
-                int kstride, int vstride)
+                int kstride, int vstride, const float *kinv, const float *vinv)
 {
     if (!valid(pr)) return fail(DSA_ERR_STATE, "invalid projection context");
     if (!x || !W || !q || !k || !v) return fail(DSA_ERR_ARG, "x, W, q, k and v must be non-NULL");
@@ -684,6 +688,8 @@ int proj_launch(dsa_proj_ctx *pr, const void *x, const void *W, int pos, void *q
     p.v = static_cast<__nv_bfloat16 *>(v);
     p.kstride = kstride > 0 ? kstride : pr->D;
     p.vstride = vstride > 0 ? vstride : pr->D;
+    p.kinv = kinv;
+    p.vinv = vinv;
     p.H = pr->H;
     p.part = pr->part;
     p.counters = pr->counters;
@@ -776,7 +782,7 @@ int dsa_proj_create(int batch, int heads, int head_dim, int hidden, dsa_proj *ou
                        "projection partials");
     if (rc == DSA_OK) rc = dev_alloc((void **)&p->counters, sizeof(int) * (size_t)p->tiles, "projection counters");
     if (rc == DSA_OK) rc = dev_alloc((void **)&p->status, 16, "projection status");
-    if (rc == DSA_OK) rc = dev_alloc((void **)&p->staging, sizeof(__nv_bfloat16) * 3 * n, "q, k, v staging");
+    if (rc == DSA_OK) rc = dev_alloc((void **)&p->staging, sizeof(__nv_bfloat16) * n, "q staging");
     if (rc != DSA_OK) {
         free_proj(p);  // keeps the allocation's error message
         return rc;

@@ -932,8 +932,18 @@ def run_fused(args) -> None:
     projs = [Proj(wl.batch, wl.heads, wl.head_dim, g.hidden) for g in pgens]
     xpool = [[g.x(t_start + i) for g in pgens] for i in range(args.pool)]
     hidden, HD, B = pgens[0].hidden, wl.heads * wl.head_dim, wl.batch
+    # the projection alone (dsa_qkv_rope): W and x read, q, k, v written (bf16)
     proj_bytes = 3 * HD * hidden * 2 + B * hidden * 2 + 3 * B * HD * 2
     proj_flops = 2.0 * B * hidden * 3 * HD
+    # the fused layer step: the projection writes q (bf16) and the newest entry
+    # in its stored form straight into the decode state; the decode kernel
+    # reads q, the attended rows (the newest entry among them) and writes out
+    e = 1 if wl.dtype == "fp8e4m3" else 2
+    d = wl.head_dim
+    pl0 = stack.handles[0].plan(t_start)
+    rows = pl0.n_prefix + pl0.n_decode
+    fused_bytes = (3 * HD * hidden * 2 + B * hidden * 2
+                   + wl.streams * (2 * d + 2 * d * e + 2 * d * e * rows + 2 * d + 2 * d))
     stream = torch.cuda.current_stream()
     q, k, v = (torch.empty((wl.streams, wl.head_dim), dtype=torch.bfloat16, device="cuda") for _ in range(3))
 
@@ -990,9 +1000,9 @@ def run_fused(args) -> None:
         "config": workload_config(wl, f"phase-3 steady state from t = {t_start}; hidden {hidden}"),
         "fused": {"value": n_fused / (el_fused / 1e3), "unit": UNIT, "ms_per_step": el_fused / steps,
                   "ms_per_layer": el_fused / (steps * wl.layers),
-                  "hbm_gbs": (proj_bytes + plan.algo_bytes) * wl.layers * steps / (el_fused / 1e3) / 1e9,
-                  "frac": (proj_bytes + plan.algo_bytes) * wl.layers * steps / (el_fused / 1e3) / 1e9 / peak,
-                  "algo_bytes_per_layer": proj_bytes + plan.algo_bytes, "launches_per_layer": 2 if plan.nsplit == 1 else 3},
+                  "hbm_gbs": fused_bytes * wl.layers * steps / (el_fused / 1e3) / 1e9,
+                  "frac": fused_bytes * wl.layers * steps / (el_fused / 1e3) / 1e9 / peak,
+                  "algo_bytes_per_layer": fused_bytes, "launches_per_layer": 2 if plan.nsplit == 1 else 3},
         "projection": {"kernel": "dsa_proj_k::qkv_rope_kernel", "bound": "hbm", "launch_ms": per_proj,
                        "isolated_launch_ms": iso, "algo_bytes_per_launch": proj_bytes,
                        "achieved": proj_bytes / (per_proj / 1e3) / 1e9, "peak": peak, "unit": "GB/s",

@@ -47,7 +47,7 @@ typedef struct dsa_proj_ctx *dsa_proj; /* opaque; library-owned */
  * (an even head count at head_dim 64); hidden a positive multiple of 64.
  * Allocates on the current device: the split-reduction scratch (SMs x
  * batch (rounded up to 16) x 128 floats plus one counter per 128 output
- * features) and bf16 staging for one step's q, k, v (3 x batch x
+ * features) and bf16 staging for one step's q (batch x
  * heads x head_dim), used by dsa_decode_step_fused.  Errors: DSA_ERR_ARG,
  * DSA_ERR_OOM, DSA_ERR_CUDA.
  */
@@ -78,13 +78,13 @@ int dsa_qkv_rope(dsa_proj p, const void *x, const void *W, int pos, void *q, voi
 /*
  * dsa_decode_step_fused -- one decode step of handle h whose q, k_new and
  * v_new come from the projection of x by W at position L_p + t (t = h's
- * step counter).  The projection kernel writes q to p's staging buffer and,
- * for a DSA_BF16 handle, k_new and v_new straight into the decode state at
- * the slot the newest token takes at this step (its ring slot, or its
- * prefix row during the sink fill), where the decode kernel reads them and
- * appends nothing; for a DSA_FP8_E4M3 handle (whose state holds E4M3 codes)
- * they go to p's staging buffers and the decode kernel stores them.  The
- * results equal dsa_qkv_rope followed by dsa_decode_step bit for bit.
+ * step counter).  The projection kernel writes q to p's staging buffer and
+ * k_new, v_new straight into the decode state, in its stored form (bf16, or
+ * for a DSA_FP8_E4M3 handle the E4M3 codes of fp32(value) / scale with the
+ * stream's scales), at the slot the newest token takes at this step (its
+ * ring slot, or its prefix row during the sink fill); the decode kernel
+ * reads the token there and appends nothing.  The results equal
+ * dsa_qkv_rope followed by dsa_decode_step bit for bit.
  *
  * h must be a DSA_BF16 or DSA_FP8_E4M3 handle with heads = batch * heads of
  * p and the same head_dim, not in graph mode (the position and the slot are
