@@ -271,20 +271,28 @@ Plan make_plan(const dsa_ctx *h, int t)
             if (launch_cost(q, h->dtype) < launch_cost(p, h->dtype)) p = q;
         }
         // A third stage per warp (two CTAs per SM, 8 warps) pays where the
-        // two-stage plan splits streams to fill one round of warps and three
-        // stages let every stream stay one work item in one round: no split
-        // partials, no merge launch (janus-b32 13.4 -> 11.6 us, lumina-s95-b32
-        // 29.7 -> 27.3 us on GB300).  Where it costs rounds it loses (two-round
-        // launches gained nothing or lost up to 4 %), and with FP8 rows, whose
-        // warps are bound by their own arithmetic, it always loses.
-        if (h->dtype != DSA_FP8_E4M3 && p.nsplit > 1 && p.rounds == 1 && h->forced_split == 0) {
+        // two-stage plan fits its streams in one round of items and three
+        // stages need no more rounds and fewer pieces per stream: fewer split
+        // partials and merge work, deeper pipelines.  Measured on GB300
+        // (us per launch, two stages -> three): janus-b32 13.4 -> 11.6,
+        // lumina-s95-b32 29.7 -> 27.3 (unsplit), lumina-s95-b16 17.8 -> 16.8
+        // (three pieces -> two); where three stages cost a round they lose.
+        // FP8 rows (half the bytes per row) take three stages only unsplit,
+        // and also from a two-stage plan of several rounds that splits:
+        // janus-b32 9.2 -> 8.5, lumina-s95-b32 19.5 -> 17.9, sweep512-s75
+        // 38.6 -> 36.8; FP8 lumina-s95-b16 in two pieces lost (13.4 -> 14.5).
+        const bool fp8 = h->dtype == DSA_FP8_E4M3;
+        const bool try3 = h->forced_split == 0 &&
+                          (p.rounds == 1 ? (p.nsplit > 1 || fp8) : (fp8 && p.nsplit > 1));
+        if (try3) {
             Plan best{};
             bool have = false;
             for (int pi = 2; pi < dsa::kPipelines; ++pi) {
                 if (h->ctas_per_sm[pi] < 1) continue;
                 Plan q = p;
                 shape_plan(h, pi, q);
-                if (q.nsplit != 1 || q.rounds > p.rounds) continue;
+                if (q.rounds > p.rounds) continue;
+                if (fp8 ? q.nsplit != 1 : q.nsplit >= p.nsplit) continue;
                 if (!have || launch_cost(q, h->dtype) < launch_cost(best, h->dtype)) best = q;
                 have = true;
             }

@@ -137,16 +137,22 @@ def test_pipeline_choice_is_reported():
     p = h.plan(400)
     assert (p.pipeline, p.nsplit) == (3, 1), (p.pipeline, p.nsplit)
     h.close()
-    # a longer stream (164 rows) that FP8 rows would also split in two
-    # (32-row stages): three stages for bf16 rows, not for FP8 rows, whose
-    # warps are bound by their own arithmetic
-    h = DSA(6 * sms, 128, 64, 288, 100, 0, "bf16")
-    p = h.plan(400)
-    assert (p.pipeline, p.nsplit) == (3, 1), (p.pipeline, p.nsplit)
+    # a longer stream (164 rows), split in two by the two-stage plans for
+    # bf16 and FP8 rows alike, stays one item with three stages
+    for dtype in ("bf16", "fp8e4m3"):
+        h = DSA(6 * sms, 128, 64, 288, 100, 0, dtype)
+        p = h.plan(400)
+        assert (p.pipeline, p.nsplit) == (3, 1), (dtype, p.pipeline, p.nsplit)
+        h.close()
+    # 512 streams of 269 rows: three stages in two pieces (one round) for
+    # bf16 rows; FP8 rows keep the two-stage plan's pieces
+    h = DSA(512, 128, 64, 2048, 205, 0, "bf16")
+    p = h.plan(3000)
+    assert p.pipeline in (3, 4) and p.nsplit == 2, (p.pipeline, p.nsplit)
     h.close()
-    h = DSA(6 * sms, 128, 64, 288, 100, 0, "fp8e4m3")
-    p = h.plan(400)
-    assert p.pipeline in (1, 2) and p.nsplit == 2, (p.pipeline, p.nsplit)
+    h = DSA(512, 128, 64, 2048, 205, 0, "fp8e4m3")
+    p = h.plan(3000)
+    assert p.pipeline in (1, 2) and p.nsplit > 1, (p.pipeline, p.nsplit)
     h.close()
 
 
