@@ -20,6 +20,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// 3-D tiled TMA load of one box at element coordinates (x, y, z); boxes
+// reaching outside the tensor (negative or past-the-end y included) read
+// zeros there.  x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 // 5-D tiled TMA load of one box at coordinates (c0 .. c4), with an L2
 // eviction-priority hint; c0 * element size must be a multiple of 16 bytes.
 __device__ __forceinline__ void tma_load_5d_hint(uint32_t dst, const void *tmap, int c0, int c1, int c2, int c3, int c4,

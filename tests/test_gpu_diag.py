@@ -1,9 +1,10 @@
 """The attention diagnostics (include/dsa_diag.h) on the GPU against the
 oracle's fp64 statement of them (section 3.4, Fig. 8 and Fig. 10).
 
-Logits and weights are fp32 on the GPU (bf16 products exact, fp32 sums over
-at most 128 terms), so masses and cosines agree with fp64 to a few 1e-6;
-the bound used is 2e-5 absolute.
+Logits and weights are fp32 on the GPU (bf16 logits on the tensor cores, fp32
+ones on FMAs; bf16 products exact, fp32 sums over at most 128 terms), so
+masses and cosines agree with fp64 to a few 1e-6; the bound used is 2e-5
+absolute.
 """
 import numpy as np
 import pytest
@@ -52,6 +53,11 @@ CASES = {
     "f32-d64": (Workload("dg2", 1, 3, 64, "f32", 9, 8, 64, 64, 0, 1, 4), [1, 7, 8, 9, 30, 63]),
     "no-prompt": (Workload("dg3", 1, 2, 128, "bf16", 0, 7, 49, 49, 0, 1, 5), [1, 7]),
     "janus-layer": (Workload("dg4", 1, 32, 128, "bf16", 64, 24, 576, 576, 0, 1, 6), [1, 23, 24, 25, 48]),
+    # bf16 logits run on the tensor cores in 128 x 128 tiles: a prompt longer
+    # than one key tile, key tiles that straddle prompt and decoded keys,
+    # and a ragged last query tile (289 = 2 x 128 + 33)
+    "bf16-d64-long-prompt": (Workload("dg6", 1, 3, 64, "bf16", 200, 17, 289, 289, 0, 1, 8), [1, 16, 17, 18, 100]),
+    "bf16-d128-ragged": (Workload("dg7", 1, 2, 128, "bf16", 37, 12, 144, 144, 0, 1, 9), [1, 11, 12, 13, 143]),
 }
 
 
