@@ -144,6 +144,16 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// A stored vector (16 or 8 bytes) held in, and taken back from, a uint4.
+__device__ __forceinline__ uint4 to_u4(const uint4 &v) { return v; }
+__device__ __forceinline__ uint4 to_u4(const uint2 &v) { return make_uint4(v.x, v.y, 0u, 0u); }
+template <typename V>
+__device__ __forceinline__ V from_u4(const uint4 &x);
+template <>
+__device__ __forceinline__ uint4 from_u4<uint4>(const uint4 &x) { return x; }
+template <>
+__device__ __forceinline__ uint2 from_u4<uint2>(const uint4 &x) { return make_uint2(x.x, x.y); }
+
 // Per element type: the query fragment a lane keeps, the q.k partial dot
 // product of one 16-byte vector, and acc += p * v for one 16-byte vector.
 template <typename T>
@@ -154,7 +164,6 @@ struct Elem<float> {
     using IO = float;                   // type of q, k_new, v_new, prompt K / V and out
     using Vec = uint4;                  // one stored vector of a K or V row
     static constexpr bool SCALED = false;
-    static constexpr float kWiden = 1.f;  // value of a stored element / the value the math reads
     static constexpr int VEC = 4;       // elements per Vec
     struct Q { float x[4]; };
     static __device__ __forceinline__ Q load_q(const uint4 &v)
@@ -178,7 +187,9 @@ struct Elem<float> {
         return make_uint4(__float_as_uint(a[0] * scale), __float_as_uint(a[1] * scale), __float_as_uint(a[2] * scale),
                           __float_as_uint(a[3] * scale));
     }
-    // Stored form of vector `vec` of an input row (unchanged).
+    // Stored form of 16 loaded bytes of an input row (unchanged), and of
+    // vector `vec` of an input row.
+    static __device__ __forceinline__ Vec from_raw(const uint4 &x, float) { return x; }
     static __device__ __forceinline__ Vec load_kv(const IO *row, int vec, float)
     {
         return __ldg(reinterpret_cast<const Vec *>(row) + vec);
@@ -190,7 +201,6 @@ struct Elem<__nv_bfloat16> {
     using IO = __nv_bfloat16;
     using Vec = uint4;
     static constexpr bool SCALED = false;
-    static constexpr float kWiden = 1.f;
     static constexpr int VEC = 8;
     struct Q { uint4 raw; };  // q stays packed bf16: the dot uses mixed-precision FMAs
     static __device__ __forceinline__ Q load_q(const uint4 &v) { return Q{v}; }
@@ -225,6 +235,7 @@ struct Elem<__nv_bfloat16> {
         }
         return make_uint4(w[0], w[1], w[2], w[3]);
     }
+    static __device__ __forceinline__ Vec from_raw(const uint4 &x, float) { return x; }
     static __device__ __forceinline__ Vec load_kv(const IO *row, int vec, float)
     {
         return __ldg(reinterpret_cast<const Vec *>(row) + vec);
@@ -284,7 +295,6 @@ struct Elem<__nv_fp8_e4m3> {
     using Vec = uint2;                  // 8 codes
     static constexpr bool SCALED = true;
     static constexpr int VEC = 8;
-    static constexpr float kWiden = 1.f;  // widened values are the codes' values
     struct Q { uint32_t h[4]; };          // 8 q elements as f16 pairs (0, 1), (2, 3), (4, 5), (6, 7)
     static __device__ __forceinline__ Q load_q(const uint4 &v)  // 8 bf16
     {
@@ -318,6 +328,7 @@ struct Elem<__nv_fp8_e4m3> {
         return Elem<__nv_bfloat16>::pack(a, scale);
     }
     // Codes of the 8 bf16 elements of vector `vec` of an input row.
+    static __device__ __forceinline__ Vec from_raw(const uint4 &x, float inv) { return e4m3_codes(x, inv); }
     static __device__ __forceinline__ Vec load_kv(const IO *row, int vec, float inv)
     {
         return e4m3_codes(__ldg(reinterpret_cast<const uint4 *>(row) + vec), inv);
@@ -729,9 +740,6 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
             uint16_t *dst = p.glist + (size_t)s * p.LS + klo;
             for (int i = lane; i < khi - klo; i += 32) dst[i] = lst[i];
         }
-        const typename EL::Q q0 = EL::load_q(qn0), q1 = EL::load_q(qn1);
-        if (item + GW < p.nitems) load_q(item + GW);  // prefetch the next item's q
-
         // rank 0 is the current token (offset 0) unless it is itself skipped
         const bool has_cur = (klo == 0 && khi > 0 && !self_skip);
         T *const cur_dst = p.sinkmode ? reinterpret_cast<T *>(p.prefix) + ((size_t)s * p.Lcap + p.P) * 2 * D
@@ -739,21 +747,27 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
         // FP8 storage: per-stream scales (1 otherwise)
         const float kinv = EL::SCALED ? __ldg(p.kinv + s) : 1.f;
         const float vinv = EL::SCALED ? __ldg(p.vinv + s) : 1.f;
-        const float xs = EL::SCALED ? p.qscale * (__ldg(p.kscale + s) * EL::kWiden) : p.qscale;
+        const float xs = EL::SCALED ? p.qscale * __ldg(p.kscale + s) : p.qscale;
         const IO *kio = reinterpret_cast<const IO *>(p.knew) + (size_t)s * D;
         const IO *vio = reinterpret_cast<const IO *>(p.vnew) + (size_t)s * D;
-        Vec kc0, kc1, vc0, vc1;
-        if (has_cur && p.appended) {  // already stored in its slot (fused step): read its stored form there
+        // The current token goes straight to registers: its k_new / v_new
+        // vectors (or, already stored in its slot by the fused step, its
+        // stored vectors) are loaded here and turned into the stored form
+        // after the stage loop, so the loads overlap the wait for q and the
+        // stages.
+        uint4 kn0 = make_uint4(0, 0, 0, 0), kn1 = kn0, vn0 = kn0, vn1 = kn0;
+        if (has_cur && p.appended) {
             const Vec *cur = reinterpret_cast<const Vec *>(cur_dst);
-            kc0 = cur[cl];
-            kc1 = cur[cl + C::LPR];
-            vc0 = cur[2 * C::LPR + cl];
-            vc1 = cur[3 * C::LPR + cl];
-        } else if (has_cur) {  // the current token goes straight to registers, in its stored form
-            kc0 = EL::load_kv(kio, cl, kinv);
-            kc1 = EL::load_kv(kio, cl + C::LPR, kinv);
-            vc0 = EL::load_kv(vio, cl, vinv);
-            vc1 = EL::load_kv(vio, cl + C::LPR, vinv);
+            kn0 = to_u4(cur[cl]);
+            kn1 = to_u4(cur[cl + C::LPR]);
+            vn0 = to_u4(cur[2 * C::LPR + cl]);
+            vn1 = to_u4(cur[3 * C::LPR + cl]);
+        } else if (has_cur) {
+            const uint4 *k4 = reinterpret_cast<const uint4 *>(kio), *v4 = reinterpret_cast<const uint4 *>(vio);
+            kn0 = __ldg(k4 + cl);
+            kn1 = __ldg(k4 + cl + C::LPR);
+            vn0 = __ldg(v4 + cl);
+            vn1 = __ldg(v4 + cl + C::LPR);
         } else if (self_skip && c == 0 && !p.appended) {
             // a2 for a token that is not attended: it is in no stage; store it.
             constexpr int NV = D / C::VEC;
@@ -761,6 +775,8 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
             for (int i = lane; i < 2 * NV; i += 32)
                 dst[i] = (i < NV) ? EL::load_kv(kio, i, kinv) : EL::load_kv(vio, i - NV, vinv);
         }
+        const typename EL::Q q0 = EL::load_q(qn0), q1 = EL::load_q(qn1);
+        if (item + GW < p.nitems) load_q(item + GW);  // prefetch the next item's q
         const int npre = max(min(hi, p.P) - lo, 0);
         const int kr0 = has_cur ? klo + 1 : klo;
         const int nrows = npre + max(khi - kr0, 0);
@@ -846,6 +862,18 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
 
         // ---- the current token (a2 append, logit, softmax.V), from registers
         if (has_cur) {
+            Vec kc0, kc1, vc0, vc1;
+            if (p.appended) {
+                kc0 = from_u4<Vec>(kn0);
+                kc1 = from_u4<Vec>(kn1);
+                vc0 = from_u4<Vec>(vn0);
+                vc1 = from_u4<Vec>(vn1);
+            } else {
+                kc0 = EL::from_raw(kn0, kinv);
+                kc1 = EL::from_raw(kn1, kinv);
+                vc0 = EL::from_raw(vn0, vinv);
+                vc1 = EL::from_raw(vn1, vinv);
+            }
             float s0 = 0.f, s1 = 0.f;
             EL::dot(q0, kc0, s0, s1);
             EL::dot(q1, kc1, s0, s1);
@@ -894,7 +922,7 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
         }
         if (p.nsplit == 1) {
             if (g == 0) {
-                const float inv = (EL::SCALED ? __ldg(p.vscale + s) * EL::kWiden : 1.f) / l;
+                const float inv = (EL::SCALED ? __ldg(p.vscale + s) : 1.f) / l;
                 uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<IO *>(p.out) + (size_t)s * D);
                 o[cl] = EL::pack(acc, inv);
                 o[cl + C::LPR] = EL::pack(acc + C::VEC, inv);
@@ -976,7 +1004,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) merge_kernel(const DecodePar
         }
     }
     typename EL::IO *o = reinterpret_cast<typename EL::IO *>(p.out) + (size_t)s * D + lane * DPL;
-    const float inv = (EL::SCALED ? __ldg(p.vscale + s) * EL::kWiden : 1.f) / Lx;
+    const float inv = (EL::SCALED ? __ldg(p.vscale + s) : 1.f) / Lx;
 #pragma unroll
     for (int e = 0; e < DPL; ++e) o[e] = EL::narrow(O[e] * inv);
     if (p.select) {
