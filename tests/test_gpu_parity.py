@@ -295,3 +295,18 @@ def test_step_jump_is_refused_where_it_does_not_apply():
     assert e.value.code == dsa.DSA_ERR_STATE
     assert h.sync_status() == 0
     h.close()
+
+
+def test_steady_state_with_a_list_slice_too_long_to_prefetch():
+    """1024 rows per stream (a one-row prompt and 1023 attended decode rows)
+    in two pieces of 512 (8 KB stages forced): the second piece's decode
+    ranks start at 511 (odd), so its slice of the stored offset list,
+    counted from the even rank below, is 513 entries, one more than the
+    kernel prefetches, and the plan lists those steps' offsets from the
+    skip mask as before the steady state.  Every step through selection,
+    the step that stores the list and 60 steady-state steps against the
+    oracle."""
+    wl = small("longslice", 1, 1100, 1023, grid=35, heads=2, d=64)
+    rep = run_parity(wl, steps=1160, splits=2, pipeline=1, mask_every=100)
+    assert rep.ok, rep.summary()
+    assert rep.selections == 2 * (1100 - 1023)
