@@ -177,13 +177,15 @@ int auto_splits(const dsa_ctx *h, int n, int pi)
     return ns > need ? ns : need;
 }
 
-// Items, grid and cost of launch pipeline pi for a step of n rows per stream.
-void shape_plan(const dsa_ctx *h, int pi, Plan &p)
+// Items, grid and stage count of launch pipeline pi for a step of n rows per
+// stream, with the pieces per stream the split knob forces, else the fewest
+// an item's row limit allows (fewest) or the automatic count above.
+void shape_plan(const dsa_ctx *h, int pi, Plan &p, bool fewest = false)
 {
     const int sh = pi & 1;
     const int rows = stage_rows(h->dtype, h->D, sh);
     const int cap = chunk_cap(h->dtype, h->D, sh);
-    int ns = h->forced_split > 0 ? h->forced_split : auto_splits(h, p.n, pi);
+    int ns = h->forced_split > 0 ? h->forced_split : (fewest ? 1 : auto_splits(h, p.n, pi));
     const int need = (p.n + cap - 1) / cap;
     if (ns < need) ns = need;
     if (ns > p.n) ns = p.n;
@@ -209,31 +211,44 @@ void shape_plan(const dsa_ctx *h, int pi, Plan &p)
     p.stages = p.rounds * ((item_rows + rows - 1) / rows);
 }
 
-// Cost model of a launch, in loaded copy latencies: a launch is bound either
-// by HBM bandwidth (its bytes over the HBM rate) or by the stages each warp
-// waits on in sequence (rounds x stages per item, one loaded copy latency
-// each).  Measured on GB300 (152 SMs): one loaded latency is about 1.6 us
-// and HBM streams about 6.7 TB/s, so a launch is bandwidth bound once it
-// moves more than about kBytesPerLatency per stage it runs in sequence.
-// With bf16 / fp32 rows the 6 KB stages of shape 1 stream about 5 % slower
-// than shape 0 when bandwidth bound (more stage waits per byte); with FP8
-// rows the warps are bound by their own arithmetic rather than by HBM, and
-// the third more warps of shape 1 stream about 5 % faster.
-constexpr double kBytesPerLatency = 10.5e6;
-constexpr double kShapeRate[dsa::kPipes] = {1.0, 0.95};
-constexpr double kShapeRateFp8[dsa::kPipes] = {1.0, 1.05};
+// Cost model of a launch, in microseconds: a launch is bound either by HBM
+// bandwidth (its bytes at the rate its pipeline streams) or by the stages
+// each warp waits on in sequence (rounds x stages per item, one loaded copy
+// latency each); splitting streams adds the partial writes and the merge
+// launch.  The rates, stage latencies and split cost are fitted per pipeline
+// (least squares on the relative error) to launch times measured on GB300
+// (152 SMs) for every pipeline, with the automatic and with the fewest
+// pieces per stream, over 13 decode workloads (S from 1024 to 3072 streams,
+// 300 to 3500 rows per stream), separately for 2-byte and for 1-byte rows:
+// with FP8 rows the warps are bound by their own widening arithmetic as much
+// as by HBM, so the rates are lower and each stage takes longer.  A plan
+// chosen by this model took 1 % (bf16) and 0.5 % (FP8) longer in total than
+// the fastest measured plan of each workload.  fp32 rows take the 2-byte
+// fit (bandwidth bound at twice the bytes).
+struct CostFit {
+    double gbs[dsa::kPipelines];       // streaming rate, GB/s
+    double us_stage[dsa::kPipelines];  // one stage in sequence, us
+    double split_us;                   // partials + merge of a split step, us
+};
+constexpr CostFit kFit16 = {{6355, 6404, 6737, 6492}, {0.858, 1.022, 0.839, 0.817}, 2.29};
+constexpr CostFit kFitFp8 = {{5891, 5284, 5183, 4724}, {1.813, 1.300, 1.506, 1.458}, 2.71};
 
 double launch_cost(const Plan &p, int dtype)
 {
-    const double rate = dtype == DSA_FP8_E4M3 ? kShapeRateFp8[p.shape] : kShapeRate[p.shape];
-    const double bw = (double)p.bytes / (kBytesPerLatency * rate);
-    return bw > (double)p.stages ? bw : (double)p.stages;
+    const CostFit &f = dtype == DSA_FP8_E4M3 ? kFitFp8 : kFit16;
+    const double bw = (double)p.bytes / (f.gbs[p.pipe] * 1e3);
+    const double lat = f.us_stage[p.pipe] * (double)p.stages;
+    return (bw > lat ? bw : lat) + (p.nsplit > 1 ? f.split_us : 0.0);
 }
 
-// The pipeline shape of a step: the one the cost model above finishes first
-// (shape 0 on a tie).  Both shapes hold about the same bytes in flight per
-// SM; shape 1 wins where its extra warps take the streams in fewer rounds,
-// shape 0 where the launch is bandwidth bound either way.
+// The plan of a step: every launch pipeline the device can hold (or the one
+// the pipeline knob forces), each with the automatic and with the fewest
+// pieces per stream (or the count the split knob forces), and the one the
+// cost model above finishes first (the earlier candidate on a tie).  Three
+// stages per warp win where their deeper pipelines take the streams in as
+// few rounds as two stages do; shape 1's extra warps win where they save a
+// round; unsplit items win where the split would leave the launch
+// bandwidth bound anyway.
 Plan make_plan(const dsa_ctx *h, int t)
 {
     Plan p{};
@@ -261,45 +276,23 @@ Plan make_plan(const dsa_ctx *h, int t)
     // K and V rows read (current token through k_new/v_new) + q, k_new, v_new
     // read + new entry written + out written.
     p.bytes = (unsigned long long)h->S * (2 * De * (unsigned long long)(p.n - 1) + 4 * Di + 2 * De);
-    if (h->forced_pipe > 0) {
-        shape_plan(h, h->forced_pipe - 1, p);
-    } else {
-        shape_plan(h, 0, p);
-        if (h->ctas_per_sm[1] > 0) {
+    Plan best{};
+    double best_cost = 0.0;
+    bool have = false;
+    for (int pi = 0; pi < dsa::kPipelines; ++pi) {
+        if (h->forced_pipe > 0 ? pi != h->forced_pipe - 1 : h->ctas_per_sm[pi] < 1) continue;
+        for (int fewest = 0; fewest < (h->forced_split > 0 ? 1 : 2); ++fewest) {
             Plan q = p;
-            shape_plan(h, 1, q);
-            if (launch_cost(q, h->dtype) < launch_cost(p, h->dtype)) p = q;
-        }
-        // A third stage per warp (two CTAs per SM, 8 warps) pays where the
-        // two-stage plan fits its streams in one round of items and three
-        // stages need no more rounds and fewer pieces per stream: fewer split
-        // partials and merge work, deeper pipelines.  Measured on GB300
-        // (us per launch, two stages -> three): janus-b32 13.4 -> 11.6,
-        // lumina-s95-b32 29.7 -> 27.3 (unsplit), lumina-s95-b16 17.8 -> 16.8
-        // (three pieces -> two); where three stages cost a round they lose.
-        // FP8 rows (half the bytes per row) take three stages only unsplit,
-        // and also from a two-stage plan of several rounds that splits:
-        // janus-b32 9.2 -> 8.5, lumina-s95-b32 19.5 -> 17.9, sweep512-s75
-        // 38.6 -> 36.8; FP8 lumina-s95-b16 in two pieces lost (13.4 -> 14.5).
-        const bool fp8 = h->dtype == DSA_FP8_E4M3;
-        const bool try3 = h->forced_split == 0 &&
-                          (p.rounds == 1 ? (p.nsplit > 1 || fp8) : (fp8 && p.nsplit > 1));
-        if (try3) {
-            Plan best{};
-            bool have = false;
-            for (int pi = 2; pi < dsa::kPipelines; ++pi) {
-                if (h->ctas_per_sm[pi] < 1) continue;
-                Plan q = p;
-                shape_plan(h, pi, q);
-                if (q.rounds > p.rounds) continue;
-                if (fp8 ? q.nsplit != 1 : q.nsplit >= p.nsplit) continue;
-                if (!have || launch_cost(q, h->dtype) < launch_cost(best, h->dtype)) best = q;
+            shape_plan(h, pi, q, fewest != 0);
+            const double c = launch_cost(q, h->dtype);
+            if (!have || c < best_cost) {
+                best = q;
+                best_cost = c;
                 have = true;
             }
-            if (have) p = best;
         }
     }
-    return p;
+    return best;
 }
 
 // The most work items per stream any step takes (steps from N_att - 1 on

@@ -110,32 +110,43 @@ def test_small_parity_each_pipeline(name, pipeline):
 
 
 def test_pipeline_choice_is_reported():
-    """The automatic plan takes shape 2 where shape 1 would need a second
-    round of items (more streams than shape 1's resident warps, a launch
-    bound by copy latency) and shape 1 where both run two rounds of a short
-    stream and the launch is bandwidth bound."""
+    """The automatic plan, from the launch cost model fitted to measured
+    launch times: the steady-state plans of the workloads where the earlier
+    rule-based choice was measurably slower, small cases where the three-stage
+    pipelines keep streams unsplit, and the pipeline knob."""
     from ar_image_gen_gb300.dsa import DSA
+    from ar_image_gen_gb300.synth import WORKLOADS
+
+    def steady(name, dtype):
+        wl = WORKLOADS[name]
+        h = DSA(wl.streams, wl.head_dim, wl.L_p, wl.N_r, wl.N_att, wl.sink, dtype)
+        p = h.plan(wl.L_dec - 1)
+        h.close()
+        return p.pipeline, p.nsplit
+
+    # stress-s95, bf16: unsplit (about 84 us per launch on GB300) rather than
+    # shape 1 in two pieces (91 us)
+    pipe, ns = steady("stress-s95", "bf16")
+    assert ns == 1 and pipe in (1, 3), (pipe, ns)
+    # sweep512-s75, bf16: three stages unsplit (54 us) rather than shape 1 in
+    # two pieces (61 us)
+    assert steady("sweep512-s75", "bf16") == (3, 1)
+    # lumina-s90-b54, FP8 rows: two stages of shape 0 unsplit (36 us) rather
+    # than three stages (52 us)
+    assert steady("lumina-s90-b54", "fp8e4m3") == (1, 1)
 
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # one round in shape 2 (16 warps per SM), two in shape 1 (12 per SM)
-    h = DSA(14 * sms, 128, 64, 512, 51, 0, "bf16")
-    p = h.plan(600)
-    assert (p.pipeline, p.nsplit) == (2, 1), (p.pipeline, p.nsplit)
-    h.close()
-    # two rounds in either shape of a 93-row stream: fewer, larger stages win
-    h = DSA(20 * sms, 128, 64, 288, 29, 0, "bf16")
-    p = h.plan(400)
-    assert (p.pipeline, p.nsplit) == (1, 1), (p.pipeline, p.nsplit)
-    h.set_pipeline(2)
-    assert h.plan(400).pipeline == 2
-    h.set_pipeline(0)
-    assert h.plan(400).pipeline == 1
-    h.close()
     # streams that would be split in two to fill the two-stage grid fit one
     # round of the three-stage grid (8 warps per SM) unsplit: no merge launch
     h = DSA(6 * sms, 128, 64, 288, 29, 0, "bf16")
     p = h.plan(400)
     assert (p.pipeline, p.nsplit) == (3, 1), (p.pipeline, p.nsplit)
+    h.set_pipeline(2)
+    assert h.plan(400).pipeline == 2
+    h.set_pipeline(0)
+    assert h.plan(400).pipeline == 3
+    h.set_splits(3)
+    assert h.plan(400).nsplit == 3
     h.close()
     # a longer stream (164 rows), split in two by the two-stage plans for
     # bf16 and FP8 rows alike, stays one item with three stages
@@ -145,7 +156,8 @@ def test_pipeline_choice_is_reported():
         assert (p.pipeline, p.nsplit) == (3, 1), (dtype, p.pipeline, p.nsplit)
         h.close()
     # 512 streams of 269 rows: three stages in two pieces (one round) for
-    # bf16 rows; FP8 rows keep the two-stage plan's pieces
+    # bf16 rows; FP8 rows, bound by their stage waits, take the two-stage
+    # plan's shorter pieces
     h = DSA(512, 128, 64, 2048, 205, 0, "bf16")
     p = h.plan(3000)
     assert p.pipeline in (3, 4) and p.nsplit == 2, (p.pipeline, p.nsplit)
