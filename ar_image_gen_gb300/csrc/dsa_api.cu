@@ -218,20 +218,21 @@ void shape_plan(const dsa_ctx *h, int pi, Plan &p, bool fewest = false)
 // launch.  The rates, stage latencies and split cost are fitted per pipeline
 // (least squares on the relative error) to launch times measured on GB300
 // (152 SMs) for every pipeline, with the automatic and with the fewest
-// pieces per stream, over 13 decode workloads (S from 1024 to 3072 streams,
-// 300 to 3500 rows per stream), separately for 2-byte and for 1-byte rows:
-// with FP8 rows the warps are bound by their own widening arithmetic as much
-// as by HBM, so the rates are lower and each stage takes longer.  A plan
-// chosen by this model took 1 % (bf16) and 0.5 % (FP8) longer in total than
-// the fastest measured plan of each workload.  fp32 rows take the 2-byte
-// fit (bandwidth bound at twice the bytes).
+// pieces per stream, over 20 decode launches (13 sparse steady states and 7
+// dense settings: 512 to 3072 streams of 93 to 8196 rows), separately for
+// 2-byte and for 1-byte rows: FP8 stages hold twice the rows of a bf16
+// stage and take longer, their warps being bound by their own widening
+// arithmetic as much as by HBM.  Over those launches the plans this model
+// picks took 1.7 % (bf16) and 0.2 % (FP8) longer in total than the fastest
+// measured plan of each.  fp32 rows take the 2-byte fit (bandwidth bound at
+// twice the bytes).
 struct CostFit {
     double gbs[dsa::kPipelines];       // streaming rate, GB/s
     double us_stage[dsa::kPipelines];  // one stage in sequence, us
     double split_us;                   // partials + merge of a split step, us
 };
-constexpr CostFit kFit16 = {{6355, 6404, 6737, 6492}, {0.858, 1.022, 0.839, 0.817}, 2.29};
-constexpr CostFit kFitFp8 = {{5891, 5284, 5183, 4724}, {1.813, 1.300, 1.506, 1.458}, 2.71};
+constexpr CostFit kFit16 = {{6533, 6535, 6740, 6655}, {0.846, 0.999, 0.827, 0.433}, 2.32};
+constexpr CostFit kFitFp8 = {{6286, 5864, 6736, 6219}, {1.644, 1.108, 1.420, 1.321}, 2.64};
 
 double launch_cost(const Plan &p, int dtype)
 {

@@ -256,13 +256,15 @@ struct Elem<__nv_bfloat16> {
 // ever widened.
 __device__ __forceinline__ uint32_t f16x2_bits(__half2 h) { return *reinterpret_cast<const uint32_t *>(&h); }
 
-// The two E4M3 codes in the low 16 bits of w as an f16 pair (code 0 in the
-// low half).
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t w)
+// The four E4M3 codes of w as two f16 pairs: codes 0, 1 in lo and 2, 3 in
+// hi (the lower code in the low half of each).  The word is split into its
+// 16-bit halves as operands of the two conversions (no shift).
+__device__ __forceinline__ void e4m3x4_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
-    uint32_t r;
-    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(r) : "r"(w));
-    return r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 // acc0 += lo(a) * lo(b), acc1 += hi(a) * hi(b) for f16x2 a, b in fp32.
@@ -308,19 +310,25 @@ struct Elem<__nv_fp8_e4m3> {
     // q . code (partial sums)
     static __device__ __forceinline__ void dot(const Q &q, const uint2 &k, float &s0, float &s1)
     {
-        fma2_f16_f32(s0, s1, e4m3x2_f16x2(k.x), q.h[0]);
-        fma2_f16_f32(s0, s1, e4m3x2_f16x2(k.x >> 16), q.h[1]);
-        fma2_f16_f32(s0, s1, e4m3x2_f16x2(k.y), q.h[2]);
-        fma2_f16_f32(s0, s1, e4m3x2_f16x2(k.y >> 16), q.h[3]);
+        uint32_t c01, c23, c45, c67;
+        e4m3x4_f16x4(k.x, c01, c23);
+        e4m3x4_f16x4(k.y, c45, c67);
+        fma2_f16_f32(s0, s1, c01, q.h[0]);
+        fma2_f16_f32(s0, s1, c23, q.h[1]);
+        fma2_f16_f32(s0, s1, c45, q.h[2]);
+        fma2_f16_f32(s0, s1, c67, q.h[3]);
     }
     // acc[0..7] += p * code (p rounded to f16, products in fp32)
     static __device__ __forceinline__ void axpy(float p, const uint2 &v, float *acc)
     {
         const uint32_t pp = f16x2_bits(__float2half2_rn(p));
-        fma2_f16_f32(acc[0], acc[1], e4m3x2_f16x2(v.x), pp);
-        fma2_f16_f32(acc[2], acc[3], e4m3x2_f16x2(v.x >> 16), pp);
-        fma2_f16_f32(acc[4], acc[5], e4m3x2_f16x2(v.y), pp);
-        fma2_f16_f32(acc[6], acc[7], e4m3x2_f16x2(v.y >> 16), pp);
+        uint32_t c01, c23, c45, c67;
+        e4m3x4_f16x4(v.x, c01, c23);
+        e4m3x4_f16x4(v.y, c45, c67);
+        fma2_f16_f32(acc[0], acc[1], c01, pp);
+        fma2_f16_f32(acc[2], acc[3], c23, pp);
+        fma2_f16_f32(acc[4], acc[5], c45, pp);
+        fma2_f16_f32(acc[6], acc[7], c67, pp);
     }
     static __device__ __forceinline__ __nv_bfloat16 narrow(float x) { return __float2bfloat16_rn(x); }
     static __device__ __forceinline__ uint4 pack(const float *a, float scale)

@@ -991,6 +991,18 @@ def run_fused(args) -> None:
     _, evs = timed(proj_steps, max(3, min(steps, 20)), True)
     iso = statistics.fmean(a.elapsed_time(b) for a, b in evs)
     per_proj = el_proj / (steps * wl.layers)
+
+    # for context: the library GEMM of the same shapes (torch.matmul on
+    # cuBLAS, x W^T without RoPE), back to back over the layers
+    def lib_steps(n):
+        for i in range(n):
+            xs = xpool[i % args.pool]
+            for layer in range(wl.layers):
+                torch.matmul(xs[layer], Ws[layer].t())
+
+    lib_steps(args.warmup)
+    el_lib, _ = timed(lib_steps, steps)
+    per_lib = el_lib / (steps * wl.layers)
     status = max([h.sync_status() for h in stack.handles] + [p.sync_status() for p in projs], key=abs)
     # the oracle's projection (numpy fp64) on one layer, for scale
     x0 = xpool[0][0].double().cpu().numpy()
@@ -1012,7 +1024,9 @@ def run_fused(args) -> None:
                        "achieved": proj_bytes / (per_proj / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                        "peak_kind": f"{peak_kind} hbm_gbs", "frac": proj_bytes / (per_proj / 1e3) / 1e9 / peak,
                        "tflops": proj_flops / (per_proj / 1e3) / 1e12,
-                       "tensor_frac_of_bf16_peak": proj_flops / (per_proj / 1e3) / 1e12 / measured_bf16_tflops()},
+                       "tensor_frac_of_bf16_peak": proj_flops / (per_proj / 1e3) / 1e12 / measured_bf16_tflops(),
+                       "library_gemm_ms": per_lib,
+                       "library_gemm_note": "torch.matmul (cuBLAS) of x by W^T, same shapes, no RoPE, back to back"},
         "clocks": clk.summary(), "steps": steps, "warmup": args.warmup,
         "cpu_baseline": {"seconds_per_layer_projection": cpu_s, "kind": "oracle", "cores": "numpy BLAS",
                          "sample": "layer 0, one step, fp64 x W^T and RoPE"},

@@ -112,8 +112,9 @@ def test_small_parity_each_pipeline(name, pipeline):
 def test_pipeline_choice_is_reported():
     """The automatic plan, from the launch cost model fitted to measured
     launch times: the steady-state plans of the workloads where the earlier
-    rule-based choice was measurably slower, small cases where the three-stage
-    pipelines keep streams unsplit, and the pipeline knob."""
+    rule-based choice was measurably slower, the dense setting of stress-s95,
+    small cases where the three-stage pipelines keep streams unsplit, and
+    the pipeline knob."""
     from ar_image_gen_gb300.dsa import DSA
     from ar_image_gen_gb300.synth import WORKLOADS
 
@@ -134,6 +135,14 @@ def test_pipeline_choice_is_reported():
     # lumina-s90-b54, FP8 rows: two stages of shape 0 unsplit (36 us) rather
     # than three stages (52 us)
     assert steady("lumina-s90-b54", "fp8e4m3") == (1, 1)
+    # stress-s95's dense setting (2048 streams of about 8190 rows), FP8 rows:
+    # three stages in 16-17 pieces (645 us) rather than two stages of shape 0
+    # (806 us)
+    wl = WORKLOADS["stress-s95"].dense()
+    h = DSA(wl.streams, wl.head_dim, wl.L_p, wl.N_r, wl.N_att, wl.sink, "fp8e4m3")
+    p = h.plan(wl.L_dec - 1)
+    h.close()
+    assert p.pipeline == 3 and p.nsplit == 17, (p.pipeline, p.nsplit)
 
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     # streams that would be split in two to fill the two-stage grid fit one
@@ -148,13 +157,16 @@ def test_pipeline_choice_is_reported():
     h.set_splits(3)
     assert h.plan(400).nsplit == 3
     h.close()
-    # a longer stream (164 rows), split in two by the two-stage plans for
-    # bf16 and FP8 rows alike, stays one item with three stages
-    for dtype in ("bf16", "fp8e4m3"):
-        h = DSA(6 * sms, 128, 64, 288, 100, 0, dtype)
-        p = h.plan(400)
-        assert (p.pipeline, p.nsplit) == (3, 1), (dtype, p.pipeline, p.nsplit)
-        h.close()
+    # a longer stream (164 rows), which the automatic two-stage plans split
+    # in two, stays one item: three stages for bf16 rows; FP8 rows (half the
+    # stages) in the fewest pieces of any pipeline
+    h = DSA(6 * sms, 128, 64, 288, 100, 0, "bf16")
+    p = h.plan(400)
+    assert (p.pipeline, p.nsplit) == (3, 1), (p.pipeline, p.nsplit)
+    h.close()
+    h = DSA(6 * sms, 128, 64, 288, 100, 0, "fp8e4m3")
+    assert h.plan(400).nsplit == 1
+    h.close()
     # 512 streams of 269 rows: three stages in two pieces (one round) for
     # bf16 rows; FP8 rows, bound by their stage waits, take the two-stage
     # plan's shorter pieces
