@@ -112,6 +112,8 @@ struct dsa_ctx {
     int ctas_per_sm[dsa::kPipelines];  // resident CTAs per SM of each launch pipeline (0: unavailable)
     int forced_split;
     int forced_pipe;  // 0: automatic, else launch pipeline + 1
+    int xm_ok[dsa::kPipelines];  // 1: the CTA merge's shared memory keeps the pipeline's occupancy
+    int merge_launch_only;       // 1: split streams always go through merge_kernel (test knob)
     int pstride;
     uint32_t wait_limit;
     void *prefix, *ring;
@@ -226,20 +228,34 @@ void shape_plan(const dsa_ctx *h, int pi, Plan &p, bool fewest = false)
 // picks took 1.7 % (bf16) and 0.2 % (FP8) longer in total than the fastest
 // measured plan of each.  fp32 rows take the 2-byte fit (bandwidth bound at
 // twice the bytes).
+// Pieces of a stream merged inside the CTA (see cta_merge) cost far less
+// than the merge launch: measured on the same launches, two pieces added
+// about 0.5 us (bf16) and 0.1 us (FP8) over the unsplit cost model, against
+// about 3 us through the merge launch.  Four bf16 pieces merged inside the
+// CTA (its warps wait for the slowest of four) cost about what the merge
+// launch does; four FP8 pieces, whose warps are bound by their own work,
+// as little as two (the 512-stream lumina launches: 10.6 against 12.6 us
+// in two pieces and 13.6 us in three through the merge launch).
 struct CostFit {
     double gbs[dsa::kPipelines];       // streaming rate, GB/s
     double us_stage[dsa::kPipelines];  // one stage in sequence, us
-    double split_us;                   // partials + merge of a split step, us
+    double split_us;                   // partials + merge launch of a split step, us
+    double cta2_us, cta4_us;           // 2 or 4 pieces merged inside the CTA, us
 };
-constexpr CostFit kFit16 = {{6533, 6535, 6740, 6655}, {0.846, 0.999, 0.827, 0.433}, 2.32};
-constexpr CostFit kFitFp8 = {{6286, 5864, 6736, 6219}, {1.644, 1.108, 1.420, 1.321}, 2.64};
+constexpr CostFit kFit16 = {{6533, 6535, 6740, 6655}, {0.846, 0.999, 0.827, 0.433}, 2.32, 0.5, 2.32};
+constexpr CostFit kFitFp8 = {{6286, 5864, 6736, 6219}, {1.644, 1.108, 1.420, 1.321}, 2.64, 0.1, 0.1};
 
-double launch_cost(const Plan &p, int dtype)
+bool cta_merge(const dsa_ctx *h, const Plan &pl);
+
+double launch_cost(const dsa_ctx *h, const Plan &p)
 {
-    const CostFit &f = dtype == DSA_FP8_E4M3 ? kFitFp8 : kFit16;
+    const CostFit &f = h->dtype == DSA_FP8_E4M3 ? kFitFp8 : kFit16;
     const double bw = (double)p.bytes / (f.gbs[p.pipe] * 1e3);
     const double lat = f.us_stage[p.pipe] * (double)p.stages;
-    return (bw > lat ? bw : lat) + (p.nsplit > 1 ? f.split_us : 0.0);
+    const double split = p.nsplit == 1       ? 0.0
+                         : !cta_merge(h, p) ? f.split_us
+                                            : (p.nsplit == 2 ? f.cta2_us : f.cta4_us);
+    return (bw > lat ? bw : lat) + split;
 }
 
 // The plan of a step: every launch pipeline the device can hold (or the one
@@ -285,7 +301,7 @@ Plan make_plan(const dsa_ctx *h, int t)
         for (int fewest = 0; fewest < (h->forced_split > 0 ? 1 : 2); ++fewest) {
             Plan q = p;
             shape_plan(h, pi, q, fewest != 0);
-            const double c = launch_cost(q, h->dtype);
+            const double c = launch_cost(h, q);
             if (!have || c < best_cost) {
                 best = q;
                 best_cost = c;
@@ -294,6 +310,15 @@ Plan make_plan(const dsa_ctx *h, int t)
         }
     }
     return best;
+}
+
+// Pieces of a split stream merged inside the CTA (no merge launch): the
+// pieces fill whole groups of the CTA's warps (nsplit 2 or 4), and the
+// exchange area costs the pipeline no occupancy.
+bool cta_merge(const dsa_ctx *h, const Plan &pl)
+{
+    return (pl.nsplit == 2 || pl.nsplit == 4) && kWarpsPerCta % pl.nsplit == 0 && h->xm_ok[pl.pipe] &&
+           !h->merge_launch_only;
 }
 
 // The most work items per stream any step takes (steps from N_att - 1 on
@@ -380,46 +405,55 @@ int encode_ring_map(dsa_ctx *h)
     return DSA_OK;
 }
 
+// Resident CTAs per SM of the decode kernel with nbuf stages per warp,
+// without (xm 0) or with (xm 1) the CTA merge's shared memory.
 template <typename T, int D, int SH>
-int occupancy(int nbuf)
+int occupancy(int nbuf, int xm)
 {
     using C = dsa::KCfg<T, D, SH>;
-    static int cached[dsa::kMaxNbuf + 1] = {-1, -1, -1, -1};
+    static int cached[2][dsa::kMaxNbuf + 1] = {{-1, -1, -1, -1}, {-1, -1, -1, -1}};
     static_assert(dsa::kMaxNbuf == 3, "one cache entry per stage count");
-    if (cached[nbuf] < 0) {
+    if (cached[xm][nbuf] < 0) {
         // The attribute allows the largest layout, so every stage count launches.
         cudaError_t e = cudaFuncSetAttribute(dsa::decode_kernel<T, D, SH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::smem(dsa::kMaxNbuf));
+                                             C::smem(dsa::kMaxNbuf) + C::xm_bytes());
         if (e != cudaSuccess) return -1;
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dsa::decode_kernel<T, D, SH>, C::THREADS, C::smem(nbuf));
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, dsa::decode_kernel<T, D, SH>, C::THREADS,
+                                                          C::smem(nbuf) + (xm ? C::xm_bytes() : 0));
         if (e != cudaSuccess) return -1;
-        cached[nbuf] = n;
+        cached[xm][nbuf] = n;
     }
-    return cached[nbuf];
+    return cached[xm][nbuf];
 }
 
 template <int SH>
-int occupancy_sh(int dtype, int D, int nbuf)
+int occupancy_sh(int dtype, int D, int nbuf, int xm)
 {
     if (dtype == DSA_BF16)
-        return D == 64 ? occupancy<__nv_bfloat16, 64, SH>(nbuf) : occupancy<__nv_bfloat16, 128, SH>(nbuf);
+        return D == 64 ? occupancy<__nv_bfloat16, 64, SH>(nbuf, xm) : occupancy<__nv_bfloat16, 128, SH>(nbuf, xm);
     if (dtype == DSA_FP8_E4M3)
-        return D == 64 ? occupancy<__nv_fp8_e4m3, 64, SH>(nbuf) : occupancy<__nv_fp8_e4m3, 128, SH>(nbuf);
-    return D == 64 ? occupancy<float, 64, SH>(nbuf) : occupancy<float, 128, SH>(nbuf);
+        return D == 64 ? occupancy<__nv_fp8_e4m3, 64, SH>(nbuf, xm) : occupancy<__nv_fp8_e4m3, 128, SH>(nbuf, xm);
+    return D == 64 ? occupancy<float, 64, SH>(nbuf, xm) : occupancy<float, 128, SH>(nbuf, xm);
 }
 
 // Resident CTAs per SM of every launch pipeline (0: cannot launch); the
-// first (shape 0, two stages per warp) must be launchable.
-int query_occupancy(int dtype, int D, int *ctas)
+// first (shape 0, two stages per warp) must be launchable.  xm_ok (may be
+// NULL): 1 where the CTA merge's shared memory leaves that number unchanged.
+int query_occupancy(int dtype, int D, int *ctas, int *xm_ok = nullptr)
 {
     for (int pi = 0; pi < dsa::kPipelines; ++pi) {
         const int nbuf = 2 + (pi >> 1);
-        ctas[pi] = (pi & 1) ? occupancy_sh<1>(dtype, D, nbuf) : occupancy_sh<0>(dtype, D, nbuf);
+        ctas[pi] = (pi & 1) ? occupancy_sh<1>(dtype, D, nbuf, 0) : occupancy_sh<0>(dtype, D, nbuf, 0);
         if (ctas[pi] < 1) {
             if (pi == 0) return cuda_fail(cudaGetLastError(), "kernel occupancy query (is this an sm_103 device?)");
             ctas[pi] = 0;
             cudaGetLastError();
+        }
+        if (xm_ok) {
+            const int n = ctas[pi] < 1 ? 0 : (pi & 1) ? occupancy_sh<1>(dtype, D, nbuf, 1) : occupancy_sh<0>(dtype, D, nbuf, 1);
+            if (n < 1) cudaGetLastError();
+            xm_ok[pi] = (ctas[pi] >= 1 && n == ctas[pi]) ? 1 : 0;
         }
     }
     return DSA_OK;
@@ -435,7 +469,7 @@ cudaError_t launch_decode(const dsa::DecodeParams &p, const CUtensorMap &map, in
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::smem(p.nbuf);
+    cfg.dynamicSmemBytes = C::smem(p.nbuf) + (p.cta_merge ? C::xm_bytes() : 0);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -474,13 +508,14 @@ cudaError_t launch_decode_sh(int dtype, int D, const dsa::DecodeParams &p, const
     return D == 64 ? launch_decode<float, 64, SH>(p, map, grid, st) : launch_decode<float, 128, SH>(p, map, grid, st);
 }
 
-// Decode launch plus, when streams are split, the merge launch.
+// Decode launch plus, when streams are split and not merged inside the
+// CTA, the merge launch.
 cudaError_t launch_step(int dtype, int D, int shape, const dsa::DecodeParams &p, const CUtensorMap &map, int grid,
                         cudaStream_t st)
 {
     cudaError_t e = shape == 0 ? launch_decode_sh<0>(dtype, D, p, map, grid, st)
                                : launch_decode_sh<1>(dtype, D, p, map, grid, st);
-    if (e != cudaSuccess || p.nsplit == 1) return e;
+    if (e != cudaSuccess || p.nsplit == 1 || p.cta_merge) return e;
     if (dtype == DSA_BF16)
         return D == 64 ? launch_merge<__nv_bfloat16, 64>(p, st) : launch_merge<__nv_bfloat16, 128>(p, st);
     if (dtype == DSA_FP8_E4M3)
@@ -614,7 +649,7 @@ int dsa_create_ex(int heads, int head_dim, int L_p, int N_r, int N_att, int sink
         free_ctx(h);
         return cuda_fail(e, "cudaDeviceGetAttribute");
     }
-    rc = query_occupancy(dtype, head_dim, h->ctas_per_sm);
+    rc = query_occupancy(dtype, head_dim, h->ctas_per_sm, h->xm_ok);
     if (rc != DSA_OK) {
         std::string msg = g_err;
         free_ctx(h);
@@ -713,6 +748,7 @@ int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out)
     out->grid = p.grid;
     out->pipeline = p.pipe + 1;
     out->algo_bytes = p.bytes;
+    out->cta_merge = cta_merge(h, p) ? 1 : 0;
     return DSA_OK;
 }
 
@@ -811,6 +847,7 @@ int launch_decode_step(dsa_handle h, const void *q, const void *k_new, const voi
     p.LS = h->LS;
     p.list_mode = list_mode(h, pl);
     p.appended = appended ? 1 : 0;
+    p.cta_merge = cta_merge(h, pl) ? 1 : 0;
 
     const bool other = note_launch(st, h);
     p.early = (other || after_proj) ? 1 : 0;
@@ -929,6 +966,14 @@ int dsa_set_splits(dsa_handle h, int nsplit)
         if (rc != DSA_OK) return rc;
     }
     h->forced_split = nsplit;
+    return DSA_OK;
+}
+
+int dsa_set_merge(dsa_handle h, int mode)
+{
+    if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
+    if (mode != 0 && mode != 1) return fail(DSA_ERR_ARG, "merge mode must be 0 or 1 (got %d)", mode);
+    h->merge_launch_only = mode;
     return DSA_OK;
 }
 
@@ -1201,6 +1246,7 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
     p.LS = 0;
     p.list_mode = 0;
     p.appended = 0;
+    p.cta_merge = 0;  // split partials in the static scratch, merged by merge_kernel
     e = launch_step(dtype, head_dim, pl.shape, p, h.ring_map, pl.grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return DSA_OK;

@@ -19,11 +19,13 @@
 //       shared-memory stages; fp32 logits q.k with 8 lanes per row;
 //   a6  online softmax and P.V, combined over the warp's row groups with
 //       shuffles;
-//   a7  split combine: split items write (m, l, acc, argmin) partials that
-//       merge_kernel, launched right after, combines;
+//   a7  split combine: when a stream is split into 2 or 4 pieces, they are
+//       warps of one CTA and the piece-0 warp combines them through shared
+//       memory; otherwise split items write (m, l, acc, argmin) partials
+//       that merge_kernel, launched right after, combines;
 //   a8  fused argmin over the attended decode logits on selection steps; the
-//       warp (or merge_kernel, for split streams) sets bit r* of the stream's
-//       relative-offset skip mask.
+//       warp (the piece-0 warp, or merge_kernel, for split streams) sets bit
+//       r* of the stream's relative-offset skip mask.
 // The diagonal shift (+1 per step) costs nothing: skipped entries are kept as
 // relative offsets r = t' - position, which the shift leaves unchanged, and
 // the slot of offset r is (t' - r) mod R.  Many independent warps per SM each
@@ -118,6 +120,8 @@ struct DecodeParams {
     int list_mode;        // 0: list from the mask; 1: list from the mask and store it to glist;
                           // 2: read the list from glist (the mask no longer changes)
     int appended;         // 1: the current token is already stored in its slot (read there, no append)
+    int cta_merge;        // 1 (nsplit 2 or 4): the pieces of a stream are warps of one CTA, and the
+                          // piece-0 warp combines them through shared memory (no partials, no merge launch)
     float qscale;         // log2(e) / sqrt(D), applied to q.k
     const float *kscale;  // [S] FP8 storage: K scale, V scale and their fp32 inverses
     const float *vscale;  //     (NULL for bf16 / fp32 storage)
@@ -399,6 +403,11 @@ struct KCfg {
     static constexpr __host__ __device__ int off_list(int nbuf) { return off_bar(nbuf) + kMaxNbuf * 8; }
     static constexpr __host__ __device__ int warp_smem(int nbuf) { return (off_list(nbuf) + 2 * CHUNK_MAX * 2 + 127) / 128 * 128; }
     static constexpr __host__ __device__ int smem(int nbuf) { return WARPS * warp_smem(nbuf); }
+    // CTA merge (DecodeParams::cta_merge), after the warps' areas: two
+    // barriers per stream group (pieces done, pieces read) and one slot per
+    // warp for its piece (acc[D], m, l, min logit, min offset).
+    static constexpr int XSLOT = D + 4;  // floats
+    static constexpr __host__ __device__ int xm_bytes() { return 32 + WARPS * XSLOT * 4; }
     static_assert(LPR >= 2 && LPR <= 16 && 32 % LPR == 0, "row must span a power-of-two lane group");
     static_assert(SROWS % RPW == 0 && NIT >= 1, "stage rows must fill whole warp instructions");
     static_assert(ROW % 128 == 0 || ROW == 256, "gather destinations must stay 128-byte aligned");
@@ -446,6 +455,21 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
         fence_barrier_init();
     }
     __syncwarp();
+    // CTA merge: the pieces of a stream are warps [nsplit k, nsplit k + nsplit)
+    // of the CTA (items are dealt to the grid's warps in order and nsplit
+    // divides the CTA's warps); group k's barriers: pieces 1.. written (every
+    // lane of those warps arrives), piece 0 done reading (its every lane).
+    unsigned char *const xm = smem + C::smem(nbuf);
+    if (p.cta_merge) {
+        if (threadIdx.x == 0) {
+            for (int k = 0; k < C::WARPS / p.nsplit; ++k) {
+                mbar_init(smem_u32(xm) + 16 * k, 32 * (p.nsplit - 1));
+                mbar_init(smem_u32(xm) + 16 * k + 8, 32);
+            }
+            fence_barrier_init();
+        }
+        __syncthreads();
+    }
     const uint32_t bar0 = smem_u32(&bars[0]);
     const uint32_t buf0 = smem_u32(ws);
 
@@ -938,6 +962,81 @@ __global__ void __launch_bounds__(KCfg<T, D, SH>::THREADS, SH == 0 ? 3 : 4) deco
             if (lane == 0 && p.select && minr >= 0) {
                 p.last_sel[s] = minr;
                 p.mask[(size_t)s * p.MW + (minr >> 5)] |= 1u << (minr & 31);
+            }
+        } else if (p.cta_merge) {
+            // ---- a7 inside the CTA: pieces 1.. leave (acc, m, l, argmin) in
+            // their slots; piece 0 combines the pieces in split order with the
+            // arithmetic of merge_kernel (so the two paths agree bit for bit),
+            // writes out and the skip bit, and frees the slots.
+            float *const xs = reinterpret_cast<float *>(xm + 32);
+            const uint32_t xfull = smem_u32(xm) + 16 * (warp / p.nsplit), xfree = xfull + 8;
+            const uint32_t xpar = (uint32_t)(con_seq & 1);
+            bool ok;
+            if (c != 0) {
+                float *slot = xs + warp * C::XSLOT;
+                if (g == 0) {
+                    float4 *s4 = reinterpret_cast<float4 *>(slot);
+#pragma unroll
+                    for (int e = 0; e < C::VEC / 4; ++e) {
+                        s4[cl * (C::VEC / 4) + e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+                        s4[(cl + C::LPR) * (C::VEC / 4) + e] = make_float4(acc[C::VEC + 4 * e], acc[C::VEC + 4 * e + 1],
+                                                                           acc[C::VEC + 4 * e + 2], acc[C::VEC + 4 * e + 3]);
+                    }
+                }
+                if (lane == 0) {
+                    slot[D] = m;
+                    slot[D + 1] = l;
+                    slot[D + 2] = minv;
+                    slot[D + 3] = __int_as_float(minr);
+                }
+                mbar_arrive(xfull);
+                ok = wait_phase(xfree, xpar, p.wait_limit);  // piece 0 has read the slot
+            } else {
+                ok = wait_phase(xfull, xpar, p.wait_limit);
+                if (__all_sync(0xffffffffu, ok)) {
+                    float Mx = m;
+                    for (int i = 1; i < p.nsplit; ++i) Mx = fmaxf(Mx, xs[(warp + i) * C::XSLOT + D]);
+                    float O[2 * C::VEC];
+#pragma unroll
+                    for (int e = 0; e < 2 * C::VEC; ++e) O[e] = 0.f;
+                    float Lx = 0.f;
+                    float bv = minv;
+                    int br = minr;
+                    for (int i = 0; i < p.nsplit; ++i) {
+                        const float *sl = xs + (warp + i) * C::XSLOT;
+                        const float mi = i == 0 ? m : sl[D];
+                        const float li = i == 0 ? l : sl[D + 1];
+                        if (mi != -INFINITY) {
+                            const float f = ex2(mi - Mx);
+                            Lx = fmaf(li, f, Lx);
+#pragma unroll
+                            for (int e = 0; e < C::VEC; ++e) {
+                                O[e] = fmaf(i == 0 ? acc[e] : sl[cl * C::VEC + e], f, O[e]);
+                                O[C::VEC + e] = fmaf(i == 0 ? acc[C::VEC + e] : sl[(cl + C::LPR) * C::VEC + e], f, O[C::VEC + e]);
+                            }
+                        }
+                        if (i > 0 && better(sl[D + 2], __float_as_int(sl[D + 3]), bv, br)) {
+                            bv = sl[D + 2];
+                            br = __float_as_int(sl[D + 3]);
+                        }
+                    }
+                    if (g == 0) {
+                        const float inv = (EL::SCALED ? __ldg(p.vscale + s) : 1.f) / Lx;
+                        uint4 *o = reinterpret_cast<uint4 *>(reinterpret_cast<IO *>(p.out) + (size_t)s * D);
+                        o[cl] = EL::pack(O, inv);
+                        o[cl + C::LPR] = EL::pack(O + C::VEC, inv);
+                    }
+                    if (lane == 0 && p.select && br >= 0) {
+                        p.last_sel[s] = br;
+                        p.mask[(size_t)s * p.MW + (br >> 5)] |= 1u << (br & 31);
+                    }
+                }
+                mbar_arrive(xfree);
+            }
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) atomicOr(p.status, ST_TIMEOUT);
+                aborted = true;
+                break;
             }
         } else {
             // ---- a7: partial (m, l, acc, argmin) of this split; merge_kernel,

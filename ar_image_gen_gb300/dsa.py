@@ -44,7 +44,7 @@ STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_ARG", -2: "DSA_ERR_STATE", -3: "DSA_ER
 EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa_destroy", "dsa_get_step",
            "dsa_get_skip_mask", "dsa_get_last_selection", "dsa_sync_status", "dsa_last_error",
            "dsa_state_bytes", "dsa_plan_step", "dsa_set_kv_scales", "dsa_set_splits", "dsa_set_pipeline",
-           "dsa_set_wait_limit", "dsa_debug_copy_state", "dsa_debug_set_step",
+           "dsa_set_merge", "dsa_set_wait_limit", "dsa_debug_copy_state", "dsa_debug_set_step",
            "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc", "dsa_decode_step_noalloc_status", "dsa_diag_trace", "dsa_set_graph_mode",
            "dsa_sync_step",
            "dsa_proj_create", "dsa_proj_destroy", "dsa_qkv_rope", "dsa_decode_step_fused", "dsa_proj_sync_status",
@@ -57,7 +57,7 @@ class dsa_step_plan(ctypes.Structure):
     _fields_ = [("phase", ctypes.c_int), ("t_inner", ctypes.c_int), ("n_prefix", ctypes.c_int),
                 ("n_decode", ctypes.c_int), ("select", ctypes.c_int), ("nsplit", ctypes.c_int),
                 ("chunk", ctypes.c_int), ("grid", ctypes.c_int), ("pipeline", ctypes.c_int),
-                ("algo_bytes", ctypes.c_ulonglong)]
+                ("algo_bytes", ctypes.c_ulonglong), ("cta_merge", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -80,6 +80,7 @@ _L.dsa_set_kv_scales.argtypes = [_P, _P, _P]
 _L.dsa_debug_copy_state.argtypes = [_P, _P, _P]
 _L.dsa_debug_set_step.argtypes = [_P, _I, _P]
 _L.dsa_set_pipeline.argtypes = [_P, _I]
+_L.dsa_set_merge.argtypes = [_P, _I]
 _L.dsa_set_wait_limit.argtypes = [_P, ctypes.c_uint32]
 _L.dsa_debug_fail_alloc_after.argtypes = [_I]
 _L.dsa_set_graph_mode.argtypes = [_P, _I]
@@ -225,6 +226,10 @@ def dsa_set_splits(h, nsplit) -> int:
 
 def dsa_set_pipeline(h, pipeline) -> int:
     return _L.dsa_set_pipeline(h, pipeline)
+
+
+def dsa_set_merge(h, mode) -> int:
+    return _L.dsa_set_merge(h, mode)
 
 
 def dsa_set_wait_limit(h, limit) -> int:
@@ -506,6 +511,10 @@ class DSA:
 
     def set_pipeline(self, pipeline: int):
         _check(dsa_set_pipeline(self.h, pipeline), "dsa_set_pipeline")
+
+    def set_merge(self, mode: int):
+        """0: split streams merged inside the CTA where possible; 1: always by the merge launch."""
+        _check(dsa_set_merge(self.h, mode), "dsa_set_merge")
 
     def set_wait_limit(self, limit: int):
         _check(dsa_set_wait_limit(self.h, limit), "dsa_set_wait_limit")

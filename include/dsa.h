@@ -182,6 +182,7 @@ typedef struct dsa_step_plan {
     int grid;                  /* CTAs of the decode launch */
     int pipeline;              /* launch pipeline (1 .. 4, see dsa_set_pipeline) */
     unsigned long long algo_bytes;
+    int cta_merge;             /* 1: split streams combined inside the decode launch (see dsa_set_merge) */
 } dsa_step_plan;
 
 int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out);
@@ -266,6 +267,19 @@ int dsa_set_splits(dsa_handle h, int nsplit);
  * beyond fp32 rounding order (selections are identical).  DSA_ERR_ARG for
  * other values or a pipeline the device cannot launch. */
 int dsa_set_pipeline(dsa_handle h, int pipeline);
+
+/* How split streams are combined.  0 (default): where a step splits every
+ * stream into 2 or 4 pieces and the pipeline has the shared memory to
+ * spare, the pieces of a stream run on warps of one CTA and its piece-0
+ * warp combines them through shared memory inside the decode launch (no
+ * partials in global memory, no merge launch); otherwise a merge launch
+ * combines the pieces' partials.  1: always the merge launch.  Both combine
+ * the pieces in piece order with the same arithmetic: for the same plan
+ * (pipeline and pieces, see dsa_set_pipeline and dsa_set_splits) results
+ * are identical bit for bit.  The automatic plan weighs the cost of the
+ * merge the mode implies, so the two modes may plan a step differently.
+ * DSA_ERR_ARG for other values. */
+int dsa_set_merge(dsa_handle h, int mode);
 
 /* Copy the stored KV state to host memory (synchronizes the device): the
  * prompt prefix [heads, L_p + sink, 2, head_dim] and the decode ring

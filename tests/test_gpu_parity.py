@@ -158,13 +158,17 @@ def test_pipeline_choice_is_reported():
     assert h.plan(400).nsplit == 3
     h.close()
     # a longer stream (164 rows), which the automatic two-stage plans split
-    # in two, stays one item: three stages for bf16 rows; FP8 rows (half the
-    # stages) in the fewest pieces of any pipeline
+    # in two, stays one item with three stages for bf16 rows; FP8 rows, whose
+    # warps are bound by their own work, take the two pieces, merged inside
+    # the CTA (no merge launch)
     h = DSA(6 * sms, 128, 64, 288, 100, 0, "bf16")
     p = h.plan(400)
     assert (p.pipeline, p.nsplit) == (3, 1), (p.pipeline, p.nsplit)
     h.close()
     h = DSA(6 * sms, 128, 64, 288, 100, 0, "fp8e4m3")
+    p = h.plan(400)
+    assert p.nsplit == 2 and p.cta_merge == 1, (p.pipeline, p.nsplit, p.cta_merge)
+    h.set_merge(1)  # with the merge launch's cost the plan stays unsplit
     assert h.plan(400).nsplit == 1
     h.close()
     # 512 streams of 269 rows: three stages in two pieces (one round) for
@@ -172,7 +176,7 @@ def test_pipeline_choice_is_reported():
     # plan's shorter pieces
     h = DSA(512, 128, 64, 2048, 205, 0, "bf16")
     p = h.plan(3000)
-    assert p.pipeline in (3, 4) and p.nsplit == 2, (p.pipeline, p.nsplit)
+    assert p.pipeline in (3, 4) and p.nsplit == 2 and p.cta_merge == 1, (p.pipeline, p.nsplit, p.cta_merge)
     h.close()
     h = DSA(512, 128, 64, 2048, 205, 0, "fp8e4m3")
     p = h.plan(3000)
@@ -334,3 +338,48 @@ def test_steady_state_with_a_list_slice_too_long_to_prefetch():
     rep = run_parity(wl, steps=1160, splits=2, pipeline=1, mask_every=100)
     assert rep.ok, rep.summary()
     assert rep.selections == 2 * (1100 - 1023)
+
+
+@pytest.mark.parametrize("pipeline", [1, 2, 3, 4])
+@pytest.mark.parametrize("dtype,d,splits", [("bf16", 128, 2), ("bf16", 64, 4), ("fp8e4m3", 128, 4), ("f32", 128, 2)])
+def test_cta_merge_matches_the_merge_launch(pipeline, dtype, d, splits):
+    """Split streams combined inside the decode launch (the pieces on warps
+    of one CTA, piece 0 combining them through shared memory) and by the
+    merge launch: outputs, selections and skip masks identical bit for bit,
+    step after step through the sink fill, selection and eviction; ragged
+    pieces (the prompt and the window do not divide evenly)."""
+    from ar_image_gen_gb300.dsa import DSA
+    from ar_image_gen_gb300.synth import TraceGen
+
+    wl = replace(small("ctamerge", 37, 60, 14, sink=2, grid=10, heads=6, d=d), dtype=dtype)
+    gen = TraceGen(wl, device="cuda")
+    Kp, Vp = gen.prompt()
+    hs = []
+    for mode in (0, 1):
+        h = DSA(wl.streams, d, wl.L_p, wl.N_r, wl.N_att, wl.sink, dtype)
+        h.set_pipeline(pipeline)
+        h.set_splits(splits)
+        h.set_merge(mode)
+        if dtype == "fp8e4m3":
+            h.set_kv_scales(*gen.kv_scales())
+        h.prefill(Kp, Vp)
+        hs.append(h)
+    io = torch.float32 if dtype == "f32" else torch.bfloat16
+    outs = [torch.empty((wl.streams, d), dtype=io, device="cuda") for _ in hs]
+    merged_inside = 0
+    for t in range(wl.L_dec):
+        q, k, v = gen.step(t)
+        pl = hs[0].plan(t)
+        merged_inside += pl.cta_merge
+        assert hs[1].plan(t).cta_merge == 0
+        for h, o in zip(hs, outs):
+            h.decode_step(q, k, v, o)
+        assert torch.equal(outs[0], outs[1]), f"t={t}: outputs differ"
+        if t % 10 == 9 or t == wl.L_dec - 1:
+            assert (hs[0].skip_mask() == hs[1].skip_mask()).all(), f"t={t}: skip masks differ"
+            assert (hs[0].last_selection() == hs[1].last_selection()).all(), f"t={t}: selections differ"
+    for h in hs:
+        assert h.sync_status() == 0
+        h.close()
+    if pipeline == 3:  # three stages per warp (two CTAs per SM) leave room for the exchange area
+        assert merged_inside == wl.L_dec
