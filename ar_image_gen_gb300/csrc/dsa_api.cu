@@ -160,7 +160,8 @@ struct Plan {
 long long resident_warps(const dsa_ctx *h, int pi) { return (long long)h->sm_count * h->ctas_per_sm[pi] * kWarpsPerCta; }
 
 // Work items per stream under launch pipeline pi.  Splitting a stream costs a
-// partial write and a merge; it pays when the streams alone leave most warps
+// merge (inside the CTA, or partials and a merge launch; launch_cost weighs
+// it); it pays when the streams alone leave most warps
 // idle (each warp streams its rows through a short pipeline, so few warps
 // cannot keep HBM busy).  Streams are split into about resident-warps /
 // streams pieces (one round of items) once they fill at most half the warps,
@@ -216,18 +217,18 @@ void shape_plan(const dsa_ctx *h, int pi, Plan &p, bool fewest = false)
 // Cost model of a launch, in microseconds: a launch is bound either by HBM
 // bandwidth (its bytes at the rate its pipeline streams) or by the stages
 // each warp waits on in sequence (rounds x stages per item, one loaded copy
-// latency each); splitting streams adds the partial writes and the merge
-// launch.  The rates, stage latencies and split cost are fitted per pipeline
+// latency each); splitting streams adds the merge of the pieces.  The rates,
+// stage latencies and the merge launch's cost are fitted per pipeline
 // (least squares on the relative error) to launch times measured on GB300
 // (152 SMs) for every pipeline, with the automatic and with the fewest
 // pieces per stream, over 20 decode launches (13 sparse steady states and 7
-// dense settings: 512 to 3072 streams of 93 to 8196 rows), separately for
-// 2-byte and for 1-byte rows: FP8 stages hold twice the rows of a bf16
-// stage and take longer, their warps being bound by their own widening
-// arithmetic as much as by HBM.  Over those launches the plans this model
-// picks took 1.7 % (bf16) and 0.2 % (FP8) longer in total than the fastest
-// measured plan of each.  fp32 rows take the 2-byte fit (bandwidth bound at
-// twice the bytes).
+// dense settings: 512 to 3072 streams of 93 to 8196 rows; all splits then
+// merged by the merge launch), separately for 2-byte and for 1-byte rows:
+// FP8 stages hold twice the rows of a bf16 stage and take longer, their
+// warps being bound by their own widening arithmetic as much as by HBM.
+// Over those launches the plans this model picks took 1.7 % (bf16) and
+// 0.2 % (FP8) longer in total than the fastest measured plan of each.  fp32
+// rows take the 2-byte fit (bandwidth bound at twice the bytes).
 // Pieces of a stream merged inside the CTA (see cta_merge) cost far less
 // than the merge launch: measured on the same launches, two pieces added
 // about 0.5 us (bf16) and 0.1 us (FP8) over the unsplit cost model, against
