@@ -322,6 +322,40 @@ bool cta_merge(const dsa_ctx *h, const Plan &pl)
            !h->merge_launch_only;
 }
 
+// The plan of a step as the C ABI reports it.
+void fill_plan(const dsa_ctx *h, const Plan &p, dsa_step_plan *out)
+{
+    out->phase = p.phase;
+    out->t_inner = p.tin;
+    out->n_prefix = p.P;
+    out->n_decode = p.a;
+    out->select = p.select;
+    out->nsplit = p.nsplit;
+    out->chunk = p.chunk;
+    out->grid = p.grid;
+    out->pipeline = p.pipe + 1;
+    out->algo_bytes = p.bytes;
+    out->cta_merge = cta_merge(h, p) ? 1 : 0;
+}
+
+// A handle-shaped description of a state of these sizes (nothing allocated,
+// no device queried): what the plan reads.
+void describe(dsa_ctx &h, int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int dtype)
+{
+    h.magic = kMagic;
+    h.S = heads;
+    h.D = head_dim;
+    h.L_p = L_p;
+    h.N_r = N_r;
+    h.N_att = N_att;
+    h.sink = sink;
+    h.dtype = dtype;
+    h.R = N_r - sink;
+    h.A = N_att - sink;
+    h.Lcap = L_p + sink;
+    h.MW = (h.R + 31) / 32;
+}
+
 // The most work items per stream any step takes (steps from N_att - 1 on
 // all attend the same row count), so that partials are sized once.
 int max_splits(const dsa_ctx *h)
@@ -738,18 +772,26 @@ int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out)
 {
     if (!valid(h)) return fail(DSA_ERR_STATE, "invalid handle");
     if (!out || t < 0) return fail(DSA_ERR_ARG, "out must be non-NULL and t >= 0");
-    const Plan p = make_plan(h, t);
-    out->phase = p.phase;
-    out->t_inner = p.tin;
-    out->n_prefix = p.P;
-    out->n_decode = p.a;
-    out->select = p.select;
-    out->nsplit = p.nsplit;
-    out->chunk = p.chunk;
-    out->grid = p.grid;
-    out->pipeline = p.pipe + 1;
-    out->algo_bytes = p.bytes;
-    out->cta_merge = cta_merge(h, p) ? 1 : 0;
+    fill_plan(h, make_plan(h, t), out);
+    return DSA_OK;
+}
+
+int dsa_plan_query(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int dtype, int t, int sm_count,
+                   const int *ctas_per_sm, const int *cta_merge_ok, dsa_step_plan *out)
+{
+    int rc = validate(heads, head_dim, L_p, N_r, N_att, sink, dtype);
+    if (rc != DSA_OK) return rc;
+    if (!out || !ctas_per_sm || t < 0 || sm_count < 1)
+        return fail(DSA_ERR_ARG, "out and ctas_per_sm must be non-NULL, t >= 0 and sm_count >= 1");
+    if (ctas_per_sm[0] < 1) return fail(DSA_ERR_ARG, "pipeline 1 must have at least one resident CTA per SM");
+    dsa_ctx h{};
+    describe(h, heads, head_dim, L_p, N_r, N_att, sink, dtype);
+    h.sm_count = sm_count;
+    for (int pi = 0; pi < dsa::kPipelines; ++pi) {
+        h.ctas_per_sm[pi] = ctas_per_sm[pi] > 0 ? ctas_per_sm[pi] : 0;
+        h.xm_ok[pi] = (cta_merge_ok && cta_merge_ok[pi] && h.ctas_per_sm[pi] > 0) ? 1 : 0;
+    }
+    fill_plan(&h, make_plan(&h, t), out);
     return DSA_OK;
 }
 
@@ -1158,18 +1200,7 @@ extern "C" int dsa_decode_step_noalloc(int heads, int head_dim, int L_p, int N_r
 
     // A handle-shaped description of the caller's state; nothing is allocated.
     dsa_ctx h{};
-    h.magic = kMagic;
-    h.S = heads;
-    h.D = head_dim;
-    h.L_p = L_p;
-    h.N_r = N_r;
-    h.N_att = N_att;
-    h.sink = sink;
-    h.dtype = dtype;
-    h.R = N_r - sink;
-    h.A = N_att - sink;
-    h.Lcap = L_p + sink;
-    h.MW = (h.R + 31) / 32;
+    describe(h, heads, head_dim, L_p, N_r, N_att, sink, dtype);
     h.sm_count = sms;
     for (int pi = 0; pi < dsa::kPipelines; ++pi) h.ctas_per_sm[pi] = occ[pi];
     const Plan pl = make_plan(&h, t);

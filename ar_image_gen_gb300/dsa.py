@@ -43,7 +43,7 @@ STATUS_NAMES = {0: "DSA_OK", -1: "DSA_ERR_ARG", -2: "DSA_ERR_STATE", -3: "DSA_ER
 
 EXPORTS = ["dsa_create", "dsa_create_ex", "dsa_prefill", "dsa_decode_step", "dsa_destroy", "dsa_get_step",
            "dsa_get_skip_mask", "dsa_get_last_selection", "dsa_sync_status", "dsa_last_error",
-           "dsa_state_bytes", "dsa_plan_step", "dsa_set_kv_scales", "dsa_set_splits", "dsa_set_pipeline",
+           "dsa_state_bytes", "dsa_plan_step", "dsa_plan_query", "dsa_set_kv_scales", "dsa_set_splits", "dsa_set_pipeline",
            "dsa_set_merge", "dsa_set_wait_limit", "dsa_debug_copy_state", "dsa_debug_set_step",
            "dsa_debug_fail_alloc_after", "dsa_decode_step_noalloc", "dsa_decode_step_noalloc_status", "dsa_diag_trace", "dsa_set_graph_mode",
            "dsa_sync_step",
@@ -75,6 +75,7 @@ _L.dsa_last_error.restype = ctypes.c_char_p
 _L.dsa_state_bytes.argtypes = [_I] * 6
 _L.dsa_state_bytes.restype = ctypes.c_size_t
 _L.dsa_plan_step.argtypes = [_P, _I, ctypes.POINTER(dsa_step_plan)]
+_L.dsa_plan_query.argtypes = [_I] * 9 + [_P, _P, ctypes.POINTER(dsa_step_plan)]
 _L.dsa_set_splits.argtypes = [_P, _I]
 _L.dsa_set_kv_scales.argtypes = [_P, _P, _P]
 _L.dsa_debug_copy_state.argtypes = [_P, _P, _P]
@@ -203,6 +204,17 @@ def dsa_state_bytes(heads, head_dim, L_p, N_r, sink=0, dtype=DSA_BF16) -> int:
 def dsa_plan_step(h, t):
     p = dsa_step_plan()
     return _L.dsa_plan_step(h, t, ctypes.byref(p)), p
+
+
+def dsa_plan_query(heads, head_dim, L_p, N_r, N_att, sink, dtype, t, sm_count, ctas_per_sm, cta_merge_ok=None):
+    """Host-only plan of step t for a state of these sizes on a device of
+    `sm_count` SMs with the given resident CTAs per SM of the 4 launch
+    pipelines (and where the in-CTA merge fits); returns (status, plan)."""
+    ctas = (ctypes.c_int * 4)(*[int(c) for c in ctas_per_sm])
+    ok = None if cta_merge_ok is None else (ctypes.c_int * 4)(*[int(c) for c in cta_merge_ok])
+    p = dsa_step_plan()
+    code = _L.dsa_plan_query(heads, head_dim, L_p, N_r, N_att, sink, dtype, t, sm_count, ctas, ok, ctypes.byref(p))
+    return code, p
 
 
 def dsa_set_kv_scales(h, k_scale: np.ndarray, v_scale: np.ndarray) -> int:

@@ -188,6 +188,20 @@ typedef struct dsa_step_plan {
 int dsa_plan_step(dsa_handle h, int t, dsa_step_plan *out);
 
 /*
+ * dsa_plan_query -- the plan dsa_plan_step would report for step t of a
+ * handle of these sizes on a device with `sm_count` SMs whose decode kernel
+ * keeps ctas_per_sm[p] CTAs resident per SM under launch pipeline p + 1
+ * (0: the pipeline cannot launch; [0] must be >= 1), cta_merge_ok[p] != 0
+ * where the in-CTA merge of split streams keeps that occupancy (NULL: no
+ * in-CTA merge).  Host only: touches no device and allocates nothing, so
+ * the planning logic (Algorithm 1's step counts, the split and grid sizing,
+ * the launch cost model) can be checked without a GPU.  Arrays have 4
+ * entries.  DSA_ERR_ARG for sizes dsa_create would reject or bad arguments.
+ */
+int dsa_plan_query(int heads, int head_dim, int L_p, int N_r, int N_att, int sink, int dtype, int t, int sm_count,
+                   const int *ctas_per_sm, const int *cta_merge_ok, dsa_step_plan *out);
+
+/*
  * dsa_decode_step_noalloc -- one decode step on state buffers the caller
  * owns, without any device allocation.  The paper has no counterpart: it is
  * an interface for callers that cannot allocate device memory while they
