@@ -20,8 +20,10 @@ def _free_port() -> int:
 
 
 def _rank_main(rank, world, port, out_q):
+    # CPU ranks (gloo) wherever the test runs, also on a machine with fewer
+    # GPUs than ranks: no device is visible to them
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
-                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="")
     sys.path.insert(0, ROOT)
     import bench
     import torch.distributed as dist
